@@ -1,0 +1,141 @@
+/* ls_kernels.h — kernel-level C ABI of libls.so: each hot-path kernel of one
+ * streamed training step, callable on its own (parity tests, custom schedules).
+ *
+ * Every call enqueues device work on `stream` (a cudaStream_t passed as void*) and
+ * returns LS_OK or a negative LS_ERR_* status (codes from ls.h); argument errors are
+ * caught on the host before any launch.  All pointers are device pointers to
+ * caller-owned memory unless named h_*.  bf16 travels as uint16_t; matrices are
+ * dense row-major with the given leading dimension (elements).  Shapes: T tokens,
+ * H hidden, NF4 matrices W [N, K] in nn.Linear order with K % 64 == 0.
+ */
+#ifndef LS_KERNELS_H_
+#define LS_KERNELS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* NF4 dequantisation to bf16: out[r, c] = bf16_rne(q[code] * absmax[r, c/64]) with
+ * one fp32 multiply (QLoRA's NormalFloat-4 table; Soup: Fine-Tune an 8B Model on a
+ * 4 GB GPU, "The Core Idea: Layer Streaming", "quantization: 4bit # NF4").
+ * packed [rows, cols/2], absmax [rows, cols/64], out [rows, cols]. */
+int lsk_nf4_dequant(const uint8_t* packed, const float* absmax, int64_t rows, int32_t cols, uint16_t* out,
+                    void* stream);
+
+/* NF4-dequant-fused matrix product on the tcgen05 tensor cores (fp32 accumulation).
+ *  mode 0 (forward):  out[M, N] = A[M, K] . deq(W)^T            W [N, K]
+ *  mode 1 (input grad): out[M, K] = A[M, N] . deq(W)            W [N, K]
+ * A: bf16, row pitch lda (multiple of 8); the reduction length must be a multiple
+ * of 64.  Optional LoRA extra stage (ext_k = 16 or 32, else 0): ext_a bf16 [M, 64]
+ * and ext_b bf16 [out_cols, 64], adding ext_a[:, :ext_k] . ext_b[:, :ext_k]^T into
+ * the same accumulator.  epi 0: bf16 out (+ residual bf16 [M, out_cols] when given,
+ * added before the one rounding); epi 1: fp32 out; epi 2: fp32 out +=.  ldo, ldr:
+ * row pitches of out / residual.  force_bn (0, 128, 256), force_nacc (0, 1, 2) pin
+ * the tile shape (0 = automatic). */
+int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const uint8_t* w_packed,
+                 const float* w_absmax, int32_t N, int32_t K, const uint16_t* ext_a, const uint16_t* ext_b,
+                 int32_t ext_k, int32_t epi, void* out, int64_t ldo, const uint16_t* residual, int64_t ldr,
+                 int32_t force_bn, int32_t force_nacc, void* stream);
+
+/* RMSNorm: y = bf16(w * bf16(x * rstd)), rstd = 1/sqrt(mean(x^2) + eps) (fp32).
+ * x, y bf16 [T, H] (H % 8 == 0), w bf16 [H], rstd fp32 [T] (may be NULL). */
+int lsk_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, float* rstd, int32_t T, int32_t H,
+                    float eps, void* stream);
+
+/* RMSNorm input gradient: dx (+)= rstd (g - n mean(g n)), g = dy w, n = x rstd.
+ * dy, dx fp32 [T, H]; optional dx_bf16 receives bf16(dx) after the update. */
+int lsk_rmsnorm_bwd(const float* dy, const uint16_t* x, const float* rstd, const uint16_t* w, float* dx,
+                    uint16_t* dx_bf16, int32_t T, int32_t H, int32_t accumulate, void* stream);
+
+/* Host: RoPE tables cos/sin [max_pos, hd/2] for angle p * theta^(-2i/hd) (computed
+ * in double, stored fp32). */
+int ls_rope_table(float* h_cos, float* h_sin, int32_t max_pos, int32_t head_dim, float theta);
+
+/* Rotate-half RoPE in place on heads 0..nheads-1 of qkv [T, ld] bf16 (pair (i,
+ * i+hd/2)), positions pos int32 [T] (each < table rows). */
+int lsk_rope_fwd(uint16_t* qkv, int64_t ld, const int32_t* pos, const float* cos_tab, const float* sin_tab,
+                 int32_t T, int32_t nheads, int32_t head_dim, void* stream);
+
+/* RoPE backward on an fp32 gradient g [T, ld] (heads 0..nrot_heads-1 rotated back,
+ * columns up to ncols copied) written as bf16 into out [T, ld]. */
+int lsk_rope_bwd_cast(const float* g, uint16_t* out, int64_t ld, const int32_t* pos, const float* cos_tab,
+                      const float* sin_tab, int32_t T, int32_t nrot_heads, int32_t head_dim, int32_t ncols,
+                      void* stream);
+
+/* Causal GQA attention forward.  qkv bf16 [T, ld] holds q heads (nh*hd columns),
+ * then k heads, then v heads (kv*hd each); sequences by cu int32 [nseq+1];
+ * max_len = longest sequence.  out bf16 [T, ldo] (nh*hd columns); lse fp32 [nh, T]. */
+int lsk_attn_fwd(const uint16_t* qkv, int64_t ld, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh,
+                 int32_t nkv, int32_t head_dim, uint16_t* out, int64_t ldo, float* lse, int32_t T, void* stream);
+
+/* Causal GQA attention backward: from dout bf16 [T, lddo] and the forward's out and
+ * lse, writes dq, dk, dv (fp32) into the q/k/v columns of dqkv [T, ldg].
+ * d_scratch: fp32 [nh, T]. */
+int lsk_attn_bwd(const uint16_t* qkv, int64_t ld, const uint16_t* dout, const uint16_t* out, int64_t lddo,
+                 const float* lse, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh, int32_t nkv,
+                 int32_t head_dim, float* d_scratch, float* dqkv, int64_t ldg, int32_t T, void* stream);
+
+/* SwiGLU: h = bf16(silu(gate) * up) with gu = [gate | up] bf16 [T, 2I]; backward
+ * from dh fp32 [T, I] to dgu bf16 [T, 2I]. */
+int lsk_swiglu_fwd(const uint16_t* gu, uint16_t* h, int32_t T, int32_t I, void* stream);
+int lsk_swiglu_bwd(const float* dh, const uint16_t* gu, uint16_t* dgu, int32_t T, int32_t I, void* stream);
+
+/* LoRA down-projection for the forward extra stage: u_ext bf16 [T, 64] =
+ * [bf16(s x A_q^T) | bf16(s x A_v^T) | 0]; x bf16 [T, ldx], A bf16 [r, K] (either
+ * may be NULL), r <= 16 (Soup: Fine-Tune an 8B Model on a 4 GB GPU, soup.yaml
+ * listing: r 16 on q_proj, v_proj). */
+int lsk_lora_down(const uint16_t* x, int64_t ldx, const uint16_t* a_q, const uint16_t* a_v, int32_t r,
+                  int32_t K, float s, uint16_t* u_ext, int32_t T, void* stream);
+
+/* du fp32 [T, 32] = s [dY_q B_q | dY_v B_v] (dY columns at col_q / col_v of dy
+ * [T, ldy]) and its bf16 copy du_ext [T, 64] (columns 32..63 zero). */
+int lsk_lora_du(const uint16_t* dy, int64_t ldy, int32_t col_q, int32_t nq, const uint16_t* b_q,
+                int32_t col_v, int32_t nv, const uint16_t* b_v, int32_t r, float s, float* du, uint16_t* du_ext,
+                int32_t T, void* stream);
+
+/* Deterministic outer product over tokens: out (+)= X^T U with X bf16 [T, ldx]
+ * (ncols columns) and U (fp32 u_f32 or bf16 u_bf16, [T, ldu], first r columns).
+ * layout 0: out [ncols, r] (dB shape); layout 1: out [r, ncols] (dA shape).
+ * scratch fp32 of nchunks * ncols * 16 floats, nchunks = ceil(T / rows_per_chunk). */
+int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* u_f32, const uint16_t* u_bf16,
+                   int32_t ldu, int32_t r, int32_t T, int32_t layout, int32_t accumulate, float* scratch,
+                   int32_t rows_per_chunk, float* out, void* stream);
+
+/* Extra-stage operands built from the adapter: B_ext [N, 64] (q rows [q0, q0+nq)
+ * take B_q in columns 0..r-1, v rows [v0, v0+nv) take B_v in columns 16..16+r-1)
+ * and A_ext [K, 64] (row k = [A_q[:, k] | A_v[:, k] | 0]). */
+int lsk_build_ext_fwd(const uint16_t* b_q, int32_t q0, int32_t nq, const uint16_t* b_v, int32_t v0, int32_t nv,
+                      int32_t r, int32_t N, uint16_t* ext, void* stream);
+int lsk_build_ext_bwd(const uint16_t* a_q, const uint16_t* a_v, int32_t r, int32_t K, uint16_t* ext,
+                      void* stream);
+
+/* NF4 embedding gather: x[t] = dequant(row tokens[t]); packed/absmax may be mapped
+ * pinned host memory. */
+int lsk_embed_gather(const int32_t* tokens, const uint8_t* packed, const float* absmax, uint16_t* x, int32_t T,
+                     int32_t H, void* stream);
+
+/* Vocabulary logprobs without materialising the logits: logits = h . deq(W)^T
+ * (h bf16 [T, H], W NF4 [V, H]) reduced on the fly to per-128-column (max, sum-exp)
+ * partials (scratch fp32 2 * T * ceil(V/128)), then lse [T], the target logit, and
+ * lp[t] = logit[t, target[t]] - lse[t] (0 where target[t] < 0).  tgt_logit scratch
+ * fp32 [T]. */
+int lsk_vocab_logprob(const uint16_t* h, int32_t T, int32_t H, const uint8_t* w_packed, const float* w_absmax,
+                      int32_t V, const int32_t* targets, float* scratch, float* tgt_logit, float* lse, float* lp,
+                      void* stream);
+
+/* Vocabulary backward for one chunk of rows [v0, v0 + n) of W: dlogits bf16
+ * [T, n] = coef[t] (onehot(target[t] - v0) - exp(logit - lse[t])), then
+ * dh (+)= dlogits . deq(W_chunk) (fp32 [T, H]). */
+int lsk_vocab_bwd(const uint16_t* h, int32_t T, int32_t H, const uint8_t* w_packed, const float* w_absmax,
+                  int32_t v0, int32_t n, const int32_t* targets, const float* lse, const float* coef,
+                  uint16_t* dlogits, float* dh, int32_t accumulate, void* stream);
+
+/* Device error flag raised by kernels whose bounded waits ran out (0 = none). */
+int lsk_device_error(int32_t* h_out, int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LS_KERNELS_H_ */

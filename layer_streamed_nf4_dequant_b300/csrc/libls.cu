@@ -1,0 +1,1422 @@
+// libls: layer-streamed NF4 LoRA fine-tuning on one B300 — C ABI implementation.
+//
+// The frozen base lives in pinned host RAM and is copied one decoder layer at a time
+// into one of two device slots on a dedicated copy stream while the other slot's
+// layer computes ("The Core Idea: Layer Streaming" and FAQ of Soup: Fine-Tune an 8B
+// Model on a 4 GB GPU).  Forward passes store each layer's input (the activation
+// store); the backward re-streams layers in reverse and recomputes each from its
+// stored input.  DPO's reference pass re-streams the same base with the adapter off
+// (Show HN: Fine-tune an 8B model on a 4 GB laptop GPU).  Every kernel is
+// deterministic, so a streamed pass equals a resident pass bit for bit.
+//
+// One translation unit: kernels and host code are compiled together.
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "common.cuh"
+#include "nf4_gemm.cuh"
+#include "gemm_host.cuh"
+#include "pointwise.cuh"
+#include "attention.cuh"
+#include "ls.h"
+#include "ls_kernels.h"
+
+using ls::GemmArgs;
+using ls::GemmCall;
+typedef __nv_bfloat16 bf16;
+
+namespace {
+
+thread_local std::string g_thread_err;
+
+int set_thread_err(int code, const std::string& m) {
+  g_thread_err = m;
+  return code;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ host NF4 quantiser
+// QLoRA's NormalFloat-4 code values (Dettmers et al. 2023, Appendix E).
+const float kNF4Host[16] = {-1.0f, -0.6961928009986877f, -0.5250730514526367f, -0.39491748809814453f,
+                            -0.28444138169288635f, -0.18477343022823334f, -0.09105003625154495f, 0.0f,
+                            0.07958029955625534f, 0.16093020814657211f, 0.24611230194568634f,
+                            0.33791524171829224f, 0.44070982933044434f, 0.5626170039176941f,
+                            0.7229568362236023f, 1.0f};
+
+void quantize_rows(const float* w, int64_t r0, int64_t r1, int64_t cols, uint8_t* packed, float* absmax) {
+  const int64_t nb = cols / 64;
+  for (int64_t r = r0; r < r1; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* blk = w + r * cols + b * 64;
+      float a = 0.f;
+      for (int i = 0; i < 64; ++i) a = std::max(a, std::fabs(blk[i]));
+      absmax[r * nb + b] = a;
+      uint8_t* out = packed + r * (cols / 2) + b * 32;
+      for (int i = 0; i < 64; i += 2) {
+        uint8_t c[2];
+        for (int e = 0; e < 2; ++e) {
+          if (a == 0.f) {
+            c[e] = 7;
+            continue;
+          }
+          const float x = blk[i + e] / a;   // fp32 quotient
+          int best = 0;
+          float bd = std::fabs(x - kNF4Host[0]);
+          for (int j = 1; j < 16; ++j) {
+            const float d = std::fabs(x - kNF4Host[j]);
+            if (d < bd) {   // strict: ties keep the lower index
+              bd = d;
+              best = j;
+            }
+          }
+          c[e] = (uint8_t)best;
+        }
+        out[i / 2] = (uint8_t)((c[0] << 4) | c[1]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+// ====================================================================== context
+
+struct LayerLayout {
+  size_t off[16];
+  size_t bytes;
+};
+
+struct ls_ctx {
+  ls_config cfg{};
+  cudaStream_t cs = nullptr, cp = nullptr;
+  uint8_t* ws = nullptr;
+  uint64_t ws_bytes = 0;
+  int err = 0;
+  std::string msg;
+
+  int L, H, nh, nkv, hd, I, V, r, nq, nkvd, nqkv, Tmax, maxlen;
+  LayerLayout lay{};
+  size_t slot_bytes = 0;
+  int vrows = 0, nvch = 0;
+  size_t vch_abs_off = 0;   // absmax offset inside a vocabulary chunk image
+
+  uint8_t* slot[2] = {nullptr, nullptr};
+  int slot_item[2] = {-1, -1};
+  long long slot_use[2] = {0, 0};
+  long long use_clock = 0;
+  cudaEvent_t ev_ready[2] = {}, ev_free[2] = {};
+  bool free_rec[2] = {false, false};
+  std::vector<uint8_t*> res_img;   // resident mode: one image per item
+  std::vector<char> res_loaded;
+
+  std::vector<ls_layer_host> hl;
+  std::vector<char> hl_ok;
+  ls_vocab_host hv{};
+  bool hv_ok = false;
+  const uint8_t* emb_p = nullptr;   // device-visible pointers to the mapped pinned embedding
+  const float* emb_a = nullptr;
+
+  struct Ad {
+    const bf16 *aq = nullptr, *bq = nullptr, *av = nullptr, *bv = nullptr;
+    float *gaq = nullptr, *gbq = nullptr, *gav = nullptr, *gbv = nullptr;
+    bool on = false;
+  };
+  std::vector<Ad> ad;
+
+  // device buffers (inside the workspace)
+  bf16* wf = nullptr;
+  float *rope_cos = nullptr, *rope_sin = nullptr;
+  bf16 *acts = nullptr, *xping = nullptr;
+  bf16 *n1, *qkv, *attn_o, *x1, *n2, *gu, *hbuf, *u_ext, *ext_fwd;
+  float *rstd1, *rstd2, *lse_attn;
+  float *gx, *dh, *dn, *Dattn, *dqkv_f, *du, *lora_part;
+  bf16 *gx_bf, *dgu, *do_bf, *dqkv_bf, *du_ext, *ext_bwd;
+  bf16 *hf_save, *hf_tmp, *dlogits;
+  float *rstdf_save, *rstdf_tmp, *pmax, *psum, *tgt_logit, *lse_save, *lse_tmp, *lp, *coef, *dhf, *loss_tmp;
+  int32_t *tgt, *pos;
+  int P = 0;
+  size_t lora_part_floats = 0;
+
+  bool saved = false;
+  const int32_t* s_tokens = nullptr;
+  const int32_t* s_cu = nullptr;
+  const uint8_t* s_mask = nullptr;
+  int s_T = 0, s_nseq = 0;
+  int last_T = 0;
+  const float* last_lse = nullptr;
+
+  ls_stats_t st{};
+  int copy_delay_ms = 0;
+};
+
+namespace {
+
+int fail(ls_ctx* c, int code, const std::string& m) {
+  if (c && c->err == 0) {
+    c->err = code;
+    c->msg = m;
+  }
+  g_thread_err = m;
+  return code;
+}
+
+#define CK(call)                                                                              \
+  do {                                                                                        \
+    cudaError_t e_ = (call);                                                                  \
+    if (e_ != cudaSuccess) return fail(c, LS_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+#define CKL()                                                                                 \
+  do {                                                                                        \
+    cudaError_t e_ = cudaGetLastError();                                                      \
+    if (e_ != cudaSuccess) return fail(c, LS_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e_)); \
+  } while (0)
+
+int check_cfg(const ls_config* cfg, std::string& why) {
+  if (!cfg) { why = "null config"; return LS_ERR_ARG; }
+  const ls_config& k = *cfg;
+  if (k.layers < 1 || k.hidden < 64 || k.hidden % 64) { why = "hidden must be a positive multiple of 64"; return LS_ERR_ARG; }
+  if (k.heads < 1 || k.kv_heads < 1 || k.heads % k.kv_heads) { why = "heads must be a multiple of kv_heads"; return LS_ERR_ARG; }
+  if (k.head_dim != 64 && k.head_dim != 128) { why = "head_dim must be 64 or 128"; return LS_ERR_ARG; }
+  if (k.inter < 64 || k.inter % 64) { why = "inter must be a multiple of 64"; return LS_ERR_ARG; }
+  if (k.vocab < 64 || k.vocab % 64) { why = "vocab must be a multiple of 64"; return LS_ERR_ARG; }
+  if ((k.heads * k.head_dim) % 64 || (k.kv_heads * k.head_dim) % 64) { why = "head widths must be multiples of 64"; return LS_ERR_ARG; }
+  if (k.lora_r < 1 || k.lora_r > 16) { why = "lora_r must be in 1..16"; return LS_ERR_ARG; }
+  if (k.max_tokens < 1 || k.max_seqs < 1) { why = "max_tokens and max_seqs must be positive"; return LS_ERR_ARG; }
+  if (k.vocab_chunk_rows < 0 || k.vocab_chunk_rows % 256) { why = "vocab_chunk_rows must be a multiple of 256"; return LS_ERR_ARG; }
+  return LS_OK;
+}
+
+LayerLayout layer_layout(const ls_config& k) {
+  const size_t H = k.hidden, I = k.inter, nq = (size_t)k.heads * k.head_dim, nkv = (size_t)k.kv_heads * k.head_dim;
+  const size_t rows[7] = {nq, nkv, nkv, H, I, I, H};
+  const size_t cols[7] = {H, H, H, nq, H, H, I};
+  LayerLayout L{};
+  size_t o = 0;
+  // packed groups: [q k v] [o] [gate up] [down], each group 256-aligned
+  const int group_start[7] = {1, 0, 0, 1, 1, 0, 1};
+  for (int m = 0; m < 7; ++m) {
+    if (group_start[m]) o = align_up(o, 256);
+    L.off[m] = o;
+    o += rows[m] * cols[m] / 2;
+  }
+  for (int m = 0; m < 7; ++m) {
+    if (group_start[m]) o = align_up(o, 256);
+    L.off[7 + m] = o;
+    o += rows[m] * (cols[m] / 64) * 4;
+  }
+  o = align_up(o, 256);
+  L.off[14] = o;
+  o += H * 2;
+  o = align_up(o, 256);
+  L.off[15] = o;
+  o += H * 2;
+  L.bytes = align_up(o, 256);
+  return L;
+}
+
+struct Planned {
+  size_t total = 0;
+  size_t slot_bytes = 0, act_bytes = 0;
+  int vrows = 0, nvch = 0, P = 0;
+  size_t vch_abs_off = 0;
+};
+
+// Bump allocation of the workspace.  With base == nullptr only sizes are computed.
+struct Bump {
+  uint8_t* base;
+  size_t off = 0;
+  template <class T>
+  T* take(size_t count) {
+    off = align_up(off, 256);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+void vocab_chunking(const ls_config& k, size_t slot_bytes, int& vrows, int& nvch, size_t& abs_off) {
+  const size_t H = k.hidden;
+  const size_t row_bytes = H / 2 + (H / 64) * 4;
+  int rows = k.vocab_chunk_rows;
+  if (rows == 0) {
+    rows = (int)((slot_bytes - 512) / row_bytes / 256 * 256);
+    if (rows < 256) rows = 256;
+  }
+  if (rows > k.vocab) rows = (k.vocab + 255) / 256 * 256;
+  vrows = rows;
+  nvch = (k.vocab + rows - 1) / rows;
+  abs_off = align_up((size_t)rows * (H / 2), 256);
+}
+
+// Lay the whole workspace out (ctx may be null: sizes only).
+Planned lay_out(const ls_config& k, ls_ctx* c) {
+  Planned p;
+  const LayerLayout ll = layer_layout(k);
+  const size_t T = k.max_tokens, H = k.hidden, I = k.inter;
+  const size_t nq = (size_t)k.heads * k.head_dim, nkvd = (size_t)k.kv_heads * k.head_dim, nqkv = nq + 2 * nkvd;
+  const int maxlen = k.max_seq_len > 0 ? k.max_seq_len : k.max_tokens;
+  size_t slot = ll.bytes;
+  int vrows, nvch;
+  size_t abs_off;
+  vocab_chunking(k, slot, vrows, nvch, abs_off);
+  const size_t vimg = abs_off + (size_t)vrows * (H / 64) * 4;
+  if (vimg > slot) slot = align_up(vimg, 256);
+  p.slot_bytes = slot;
+  p.vrows = vrows;
+  p.nvch = nvch;
+  p.vch_abs_off = abs_off;
+  p.P = (k.vocab + 127) / 128;
+
+  Bump b{c ? c->ws : nullptr};
+  uint8_t* slots = nullptr;
+  if (k.resident) {
+    slots = b.take<uint8_t>((size_t)k.layers * ll.bytes + (size_t)nvch * align_up(vimg, 256) + 256);
+  } else {
+    slots = b.take<uint8_t>(2 * slot);
+  }
+  bf16* wf = b.take<bf16>(H);
+  float* rc = b.take<float>((size_t)maxlen * k.head_dim / 2);
+  float* rsn = b.take<float>((size_t)maxlen * k.head_dim / 2);
+  const size_t act0 = b.off;
+  bf16* acts = b.take<bf16>((size_t)(k.layers + 1) * T * H);
+  p.act_bytes = b.off - act0;
+  bf16* xping = b.take<bf16>(2 * T * H);
+  // forward layer scratch
+  bf16* n1 = b.take<bf16>(T * H);
+  bf16* qkv = b.take<bf16>(T * nqkv);
+  bf16* ao = b.take<bf16>(T * nq);
+  bf16* x1 = b.take<bf16>(T * H);
+  bf16* n2 = b.take<bf16>(T * H);
+  bf16* gu = b.take<bf16>(T * 2 * I);
+  bf16* hb = b.take<bf16>(T * I);
+  bf16* uext = b.take<bf16>(T * 64);
+  bf16* extf = b.take<bf16>(nqkv * 64);
+  float* rstd1 = b.take<float>(T);
+  float* rstd2 = b.take<float>(T);
+  float* lsea = b.take<float>((size_t)k.heads * T);
+  // backward
+  float* gx = b.take<float>(T * H);
+  bf16* gxb = b.take<bf16>(T * H);
+  float* dn = b.take<float>(T * H);
+  bf16* dob = b.take<bf16>(T * nq);
+  float* Da = b.take<float>((size_t)k.heads * T);
+  float* dqf = b.take<float>(T * nqkv);
+  bf16* dqb = b.take<bf16>(T * nqkv);
+  float* du = b.take<float>(T * 32);
+  bf16* duext = b.take<bf16>(T * 64);
+  bf16* extb = b.take<bf16>(H * 64);
+  const int chunks = (int)((T + 127) / 128);
+  const size_t lpf = (size_t)chunks * std::max(nqkv, H) * 16;
+  float* lpart = b.take<float>(lpf);
+  // union: layer-backward big buffers / vocabulary dlogits
+  const size_t u0 = align_up(b.off, 256);
+  Bump u1{c ? c->ws : nullptr, u0};
+  float* dh = u1.take<float>(T * I);
+  bf16* dgu = u1.take<bf16>(T * 2 * I);
+  Bump u2{c ? c->ws : nullptr, u0};
+  bf16* dl = u2.take<bf16>(T * (size_t)vrows);
+  b.off = std::max(u1.off, u2.off);
+  // vocabulary / loss
+  bf16* hfs = b.take<bf16>(T * H);
+  bf16* hft = b.take<bf16>(T * H);
+  float* rfs = b.take<float>(T);
+  float* rft = b.take<float>(T);
+  float* pmax = b.take<float>(T * (size_t)p.P);
+  float* psum = b.take<float>(T * (size_t)p.P);
+  float* tl = b.take<float>(T);
+  float* lses = b.take<float>(T);
+  float* lset = b.take<float>(T);
+  float* lp = b.take<float>(T);
+  float* coef = b.take<float>(T);
+  float* dhf = b.take<float>(T * H);
+  float* losst = b.take<float>(64);
+  int32_t* tgt = b.take<int32_t>(T);
+  int32_t* pos = b.take<int32_t>(T);
+  p.total = align_up(b.off, 256);
+
+  if (c) {
+    c->slot_bytes = slot;
+    if (k.resident) {
+      c->res_img.resize(k.layers + nvch);
+      size_t o = 0;
+      for (int i = 0; i < k.layers; ++i) { c->res_img[i] = slots + o; o += ll.bytes; }
+      for (int i = 0; i < nvch; ++i) { c->res_img[k.layers + i] = slots + o; o += align_up(vimg, 256); }
+      c->res_loaded.assign(k.layers + nvch, 0);
+    } else {
+      c->slot[0] = slots;
+      c->slot[1] = slots + slot;
+    }
+    c->wf = wf; c->rope_cos = rc; c->rope_sin = rsn; c->acts = acts; c->xping = xping;
+    c->n1 = n1; c->qkv = qkv; c->attn_o = ao; c->x1 = x1; c->n2 = n2; c->gu = gu; c->hbuf = hb;
+    c->u_ext = uext; c->ext_fwd = extf; c->rstd1 = rstd1; c->rstd2 = rstd2; c->lse_attn = lsea;
+    c->gx = gx; c->gx_bf = gxb; c->dn = dn; c->do_bf = dob; c->Dattn = Da; c->dqkv_f = dqf; c->dqkv_bf = dqb;
+    c->du = du; c->du_ext = duext; c->ext_bwd = extb; c->lora_part = lpart; c->lora_part_floats = lpf;
+    c->dh = dh; c->dgu = dgu; c->dlogits = dl;
+    c->hf_save = hfs; c->hf_tmp = hft; c->rstdf_save = rfs; c->rstdf_tmp = rft; c->pmax = pmax; c->psum = psum;
+    c->tgt_logit = tl; c->lse_save = lses; c->lse_tmp = lset; c->lp = lp; c->coef = coef; c->dhf = dhf;
+    c->loss_tmp = losst; c->tgt = tgt; c->pos = pos; c->P = p.P;
+    c->vrows = vrows; c->nvch = nvch; c->vch_abs_off = abs_off;
+  }
+  return p;
+}
+
+// ------------------------------------------------------------------ kernel launch helpers
+
+inline int grid1d(long long n, int threads, int cap = 148 * 16) {
+  long long g = (n + threads - 1) / threads;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return (int)g;
+}
+
+cudaError_t gemm(int mode, const bf16* A, long long lda, int M, const uint8_t* Wp, const float* Wa, int Nw, int Kw,
+                 const bf16* ext_a, const bf16* ext_b, int ext_k, int epi, void* out, long long ldo,
+                 const bf16* residual, long long ldr, cudaStream_t st, int force_bn = 0, int force_nacc = 0) {
+  GemmCall c{};
+  c.mode = mode;
+  c.A = A;
+  c.lda = lda;
+  c.Wp = Wp;
+  c.ext_a = ext_a;
+  c.force_bn = force_bn;
+  c.force_nacc = force_nacc;
+  GemmArgs& g = c.g;
+  g.M = M;
+  g.Nw = Nw;
+  g.Kw = Kw;
+  g.Nout = mode == ls::GEMM_FWD ? Nw : Kw;
+  g.Kred = mode == ls::GEMM_FWD ? Kw : Nw;
+  g.absmax = Wa;
+  g.ext_k = ext_k;
+  g.ext_b = ext_b;
+  g.epi = epi;
+  g.out = out;
+  g.ldo = ldo;
+  g.residual = residual;
+  g.ldr = ldr;
+  if (M <= 0) return cudaSuccess;
+  return ls::launch_nf4_gemm(c, st);
+}
+
+template <int HD>
+cudaError_t attn_fwd_launch(const bf16* qkv, long long ld, const int* cu, int nseq, int maxlen, int nh, int nkv,
+                            bf16* out, long long ldo, float* lse, int T, cudaStream_t st) {
+  const int smem = 3 * 64 * (HD + 8) * 2;
+  static bool set = false;
+  if (!set) {
+    cudaFuncSetAttribute(ls::attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    set = true;
+  }
+  dim3 grid((maxlen + 63) / 64, nh, nseq);
+  ls::attn_fwd_kernel<HD><<<grid, 128, smem, st>>>(qkv, ld, cu, nh, nkv, 1.0f / sqrtf((float)HD), out, ldo, lse, T);
+  return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t attn_bwd_launch(const bf16* qkv, long long ld, const bf16* dout, const bf16* o, long long lddo,
+                            const float* lse, const int* cu, int nseq, int maxlen, int nh, int nkv, float* D,
+                            float* dqkv, long long ldg, int T, cudaStream_t st) {
+  const int smem_q = 4 * 64 * (HD + 8) * 2;
+  const int smem_k = 4 * 64 * (HD + 8) * 2 + 2 * 64 * 4;
+  static bool set = false;
+  if (!set) {
+    cudaFuncSetAttribute(ls::attn_bwd_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
+    cudaFuncSetAttribute(ls::attn_bwd_dkdv_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_k);
+    set = true;
+  }
+  const float scale = 1.0f / sqrtf((float)HD);
+  {
+    const long long w = (long long)T * nh;
+    ls::attn_bwd_dot_kernel<<<(unsigned)((w + 7) / 8), 256, 0, st>>>(dout, o, lddo, nh, HD, D, T);
+  }
+  dim3 gq((maxlen + 63) / 64, nh, nseq);
+  ls::attn_bwd_dq_kernel<HD><<<gq, 128, smem_q, st>>>(qkv, ld, dout, lddo, lse, D, cu, nh, nkv, scale, dqkv, ldg, T);
+  dim3 gk((maxlen + 63) / 64, nkv, nseq);
+  ls::attn_bwd_dkdv_kernel<HD><<<gk, 128, smem_k, st>>>(qkv, ld, dout, lddo, lse, D, cu, nh, nkv, scale, dqkv, ldg, T);
+  return cudaGetLastError();
+}
+
+cudaError_t attn_fwd(int hd, const bf16* qkv, long long ld, const int* cu, int nseq, int maxlen, int nh, int nkv,
+                     bf16* out, long long ldo, float* lse, int T, cudaStream_t st) {
+  return hd == 64 ? attn_fwd_launch<64>(qkv, ld, cu, nseq, maxlen, nh, nkv, out, ldo, lse, T, st)
+                  : attn_fwd_launch<128>(qkv, ld, cu, nseq, maxlen, nh, nkv, out, ldo, lse, T, st);
+}
+cudaError_t attn_bwd(int hd, const bf16* qkv, long long ld, const bf16* dout, const bf16* o, long long lddo,
+                     const float* lse, const int* cu, int nseq, int maxlen, int nh, int nkv, float* D, float* dqkv,
+                     long long ldg, int T, cudaStream_t st) {
+  return hd == 64 ? attn_bwd_launch<64>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st)
+                  : attn_bwd_launch<128>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st);
+}
+
+cudaError_t lora_outer(const bf16* X, long long ldx, int ncols, const float* Uf, const bf16* Ub, int ldu, int r, int T,
+                       int layout, int accumulate, float* scratch, int rows_per_chunk, float* out, cudaStream_t st) {
+  const int nch = (T + rows_per_chunk - 1) / rows_per_chunk;
+  dim3 g1((ncols + 127) / 128, nch);
+  ls::lora_outer_partial_kernel<<<g1, 128, 0, st>>>(X, ldx, ncols, Uf, Ub, ldu, T, rows_per_chunk, scratch);
+  const int n = ncols * r;
+  ls::lora_outer_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(scratch, nch, ncols, r, layout, accumulate, out);
+  return cudaGetLastError();
+}
+
+void CUDART_CB host_sleep(void* p) {
+  const int ms = *reinterpret_cast<int*>(p);
+  std::this_thread::sleep_for(std::chrono::milliseconds(ms));
+}
+
+}  // namespace
+
+// ====================================================================== streaming engine
+
+namespace {
+
+size_t item_layer_component_bytes(const ls_ctx* c, int m, bool absmax) {
+  const size_t H = c->H, I = c->I, nq = c->nq, nkv = c->nkvd;
+  const size_t rows[7] = {nq, nkv, nkv, H, I, I, H};
+  const size_t cols[7] = {H, H, H, nq, H, H, I};
+  return absmax ? rows[m] * (cols[m] / 64) * 4 : rows[m] * cols[m] / 2;
+}
+
+int copy_item(ls_ctx* c, int item, uint8_t* img, cudaStream_t st) {
+  if (c->copy_delay_ms > 0) CK(cudaLaunchHostFunc(st, host_sleep, &c->copy_delay_ms));
+  if (item < c->L) {
+    const ls_layer_host& h = c->hl[item];
+    const ls_nf4_host* m7[7] = {&h.q, &h.k, &h.v, &h.o, &h.gate, &h.up, &h.down};
+    const void* src[16];
+    size_t sz[16];
+    for (int m = 0; m < 7; ++m) {
+      src[m] = m7[m]->packed;
+      sz[m] = item_layer_component_bytes(c, m, false);
+      src[7 + m] = m7[m]->absmax;
+      sz[7 + m] = item_layer_component_bytes(c, m, true);
+    }
+    src[14] = h.attn_norm;
+    sz[14] = (size_t)c->H * 2;
+    src[15] = h.mlp_norm;
+    sz[15] = (size_t)c->H * 2;
+    // one copy when the host image already has the slot layout
+    const uint8_t* hb = reinterpret_cast<const uint8_t*>(src[0]) - c->lay.off[0];
+    bool contiguous = true;
+    for (int i = 0; i < 16; ++i)
+      if (reinterpret_cast<const uint8_t*>(src[i]) != hb + c->lay.off[i]) contiguous = false;
+    if (contiguous) {
+      CK(cudaMemcpyAsync(img, hb, c->lay.off[15] + sz[15], cudaMemcpyHostToDevice, st));
+    } else {
+      for (int i = 0; i < 16; ++i) CK(cudaMemcpyAsync(img + c->lay.off[i], src[i], sz[i], cudaMemcpyHostToDevice, st));
+    }
+    c->st.layer_reads++;
+    c->st.h2d_bytes += c->lay.off[15] + sz[15];
+  } else {
+    const int ch = item - c->L;
+    const ls_nf4_host& m = c->cfg.tied ? c->hv.embed : c->hv.lm_head;
+    const size_t v0 = (size_t)ch * c->vrows;
+    const size_t n = std::min((size_t)c->vrows, (size_t)c->V - v0);
+    const size_t pb = n * (c->H / 2), ab = n * (c->H / 64) * 4;
+    CK(cudaMemcpyAsync(img, m.packed + v0 * (c->H / 2), pb, cudaMemcpyHostToDevice, st));
+    CK(cudaMemcpyAsync(img + c->vch_abs_off, m.absmax + v0 * (c->H / 64), ab, cudaMemcpyHostToDevice, st));
+    c->st.vocab_reads++;
+    c->st.h2d_bytes += pb + ab;
+  }
+  return LS_OK;
+}
+
+// Start bringing `item` into a slot (unless one already holds it); returns the slot.
+int prefetch(ls_ctx* c, int item, int busy, int* slot_out) {
+  for (int s = 0; s < 2; ++s)
+    if (c->slot_item[s] == item) {
+      c->st.slot_reuses++;
+      *slot_out = s;
+      return LS_OK;
+    }
+  int v;
+  if (busy >= 0) v = 1 - busy;
+  else v = c->slot_use[0] <= c->slot_use[1] ? 0 : 1;
+  if (c->free_rec[v]) CK(cudaStreamWaitEvent(c->cp, c->ev_free[v], 0));
+  c->slot_item[v] = -1;
+  int rc = copy_item(c, item, c->slot[v], c->cp);
+  if (rc) return rc;
+  CK(cudaEventRecord(c->ev_ready[v], c->cp));
+  c->slot_item[v] = item;
+  *slot_out = v;
+  return LS_OK;
+}
+
+// Run body(item, image) over items in order, double-buffering the host->device copies.
+int run_items(ls_ctx* c, const std::vector<int>& items, const std::function<int(int, uint8_t*)>& body) {
+  if (items.empty()) return LS_OK;
+  if (c->cfg.resident) {
+    for (int it : items) {
+      if (!c->res_loaded[it]) {
+        int rc = copy_item(c, it, c->res_img[it], c->cs);
+        if (rc) return rc;
+        c->res_loaded[it] = 1;
+      }
+      int rc = body(it, c->res_img[it]);
+      if (rc) return rc;
+    }
+    return LS_OK;
+  }
+  int s_cur;
+  int rc = prefetch(c, items[0], -1, &s_cur);
+  if (rc) return rc;
+  for (size_t j = 0; j < items.size(); ++j) {
+    CK(cudaStreamWaitEvent(c->cs, c->ev_ready[s_cur], 0));
+    int s_next = -1;
+    if (j + 1 < items.size()) {
+      rc = prefetch(c, items[j + 1], s_cur, &s_next);
+      if (rc) return rc;
+    }
+    c->slot_use[s_cur] = ++c->use_clock;
+    rc = body(items[j], c->slot[s_cur]);
+    if (rc) return rc;
+    CK(cudaEventRecord(c->ev_free[s_cur], c->cs));
+    c->free_rec[s_cur] = true;
+    s_cur = s_next;
+  }
+  return LS_OK;
+}
+
+struct LayerW {
+  const uint8_t *pqkv, *po, *pgu, *pd;
+  const float *aqkv, *ao, *agu, *ad;
+  const bf16 *w1, *w2;
+};
+
+LayerW layer_ptrs(const ls_ctx* c, uint8_t* img) {
+  LayerW w;
+  w.pqkv = img + c->lay.off[0];
+  w.po = img + c->lay.off[3];
+  w.pgu = img + c->lay.off[4];
+  w.pd = img + c->lay.off[6];
+  w.aqkv = reinterpret_cast<const float*>(img + c->lay.off[7]);
+  w.ao = reinterpret_cast<const float*>(img + c->lay.off[10]);
+  w.agu = reinterpret_cast<const float*>(img + c->lay.off[11]);
+  w.ad = reinterpret_cast<const float*>(img + c->lay.off[13]);
+  w.w1 = reinterpret_cast<const bf16*>(img + c->lay.off[14]);
+  w.w2 = reinterpret_cast<const bf16*>(img + c->lay.off[15]);
+  return w;
+}
+
+// Forward of one decoder layer up to (recompute == true) the MLP input projections,
+// or to the layer output x_out.
+int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16* x_out, int T, int nseq,
+                  const int32_t* cu, bool adapter, bool recompute) {
+  cudaStream_t st = c->cs;
+  const int H = c->H;
+  ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(x_in, w.w1, c->n1, c->rstd1, T, H, c->cfg.eps);
+  CKL();
+  const ls_ctx::Ad& a = c->ad[layer];
+  const bool use = adapter && a.on;
+  if (use) {
+    ls::lora_down_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->n1, H, a.aq, a.av, c->r, H, c->cfg.lora_scale, c->u_ext, T);
+    CKL();
+    const int n = c->nqkv * 64;
+    ls::build_ext_fwd_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.bq, 0, c->nq, a.bv, c->nq + c->nkvd, c->nkvd, c->r,
+                                                              c->nqkv, c->ext_fwd);
+    CKL();
+  }
+  CK(gemm(ls::GEMM_FWD, c->n1, H, T, w.pqkv, w.aqkv, c->nqkv, H, c->u_ext, c->ext_fwd, use ? 32 : 0, ls::EPI_BF16,
+          c->qkv, c->nqkv, nullptr, 0, st));
+  {
+    const long long n = (long long)T * (c->nh + c->nkv) * (c->hd / 2);
+    ls::rope_fwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->qkv, c->nqkv, c->pos, c->rope_cos, c->rope_sin, T,
+                                                       c->nh + c->nkv, c->hd);
+    CKL();
+  }
+  CK(attn_fwd(c->hd, c->qkv, c->nqkv, cu, nseq, c->maxlen, c->nh, c->nkv, c->attn_o, c->nq, c->lse_attn, T, st));
+  CK(gemm(ls::GEMM_FWD, c->attn_o, c->nq, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->x1, H, x_in,
+          H, st));
+  ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->x1, w.w2, c->n2, c->rstd2, T, H, c->cfg.eps);
+  CKL();
+  CK(gemm(ls::GEMM_FWD, c->n2, H, T, w.pgu, w.agu, 2 * c->I, H, nullptr, nullptr, 0, ls::EPI_BF16, c->gu, 2 * c->I,
+          nullptr, 0, st));
+  if (recompute) return LS_OK;
+  {
+    const long long n = (long long)T * (c->I / 8);
+    ls::swiglu_fwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->gu, c->hbuf, T, c->I);
+    CKL();
+  }
+  CK(gemm(ls::GEMM_FWD, c->hbuf, c->I, T, w.pd, w.ad, H, c->I, nullptr, nullptr, 0, ls::EPI_BF16, x_out, H, c->x1, H,
+          st));
+  return LS_OK;
+}
+
+// Backward of one layer: gx (fp32, dL/d layer output) becomes dL/d layer input;
+// gx_bf mirrors it in bf16.  LoRA gradients are added into the bound buffers.
+int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int T, int nseq, const int32_t* cu) {
+  cudaStream_t st = c->cs;
+  const int H = c->H, I = c->I;
+  const ls_ctx::Ad& a = c->ad[layer];
+  int rc = layer_forward(c, w, layer, x_in, nullptr, T, nseq, cu, true, true);
+  if (rc) return rc;
+  // MLP
+  CK(gemm(ls::GEMM_DX, c->gx_bf, H, T, w.pd, w.ad, H, I, nullptr, nullptr, 0, ls::EPI_F32, c->dh, I, nullptr, 0, st));
+  {
+    const long long n = (long long)T * (I / 4);
+    ls::swiglu_bwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->dh, c->gu, c->dgu, T, I);
+    CKL();
+  }
+  CK(gemm(ls::GEMM_DX, c->dgu, 2 * I, T, w.pgu, w.agu, 2 * I, H, nullptr, nullptr, 0, ls::EPI_F32, c->dn, H, nullptr,
+          0, st));
+  ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, c->x1, c->rstd2, w.w2, c->gx, c->gx_bf, T, H, 1);
+  CKL();
+  // attention
+  CK(gemm(ls::GEMM_DX, c->gx_bf, H, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->do_bf, c->nq,
+          nullptr, 0, st));
+  CK(attn_bwd(c->hd, c->qkv, c->nqkv, c->do_bf, c->attn_o, c->nq, c->lse_attn, cu, nseq, c->maxlen, c->nh, c->nkv,
+              c->Dattn, c->dqkv_f, c->nqkv, T, st));
+  {
+    const long long n = (long long)T * c->nqkv;
+    ls::rope_bwd_cast_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->dqkv_f, c->dqkv_bf, c->nqkv, c->pos, c->rope_cos,
+                                                            c->rope_sin, T, c->nh + c->nkv, c->hd, c->nqkv);
+    CKL();
+  }
+  const bool use = a.on;
+  if (use) {
+    const float s = c->cfg.lora_scale;
+    ls::lora_du_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dqkv_bf, c->nqkv, 0, c->nq, a.bq, c->nq + c->nkvd, c->nkvd,
+                                                   a.bv, c->r, s, c->du, c->du_ext, T);
+    CKL();
+    // dB = dY^T u ;  dA = (s du)^T x
+    CK(lora_outer(c->dqkv_bf, c->nqkv, c->nq, nullptr, c->u_ext, 64, c->r, T, 0, 1, c->lora_part, 128, a.gbq, st));
+    CK(lora_outer(c->dqkv_bf + c->nq + c->nkvd, c->nqkv, c->nkvd, nullptr, c->u_ext + 16, 64, c->r, T, 0, 1,
+                  c->lora_part, 128, a.gbv, st));
+    CK(lora_outer(c->n1, H, H, c->du, nullptr, 32, c->r, T, 1, 1, c->lora_part, 128, a.gaq, st));
+    CK(lora_outer(c->n1, H, H, c->du + 16, nullptr, 32, c->r, T, 1, 1, c->lora_part, 128, a.gav, st));
+    const int n = H * 64;
+    ls::build_ext_bwd_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.aq, a.av, c->r, H, c->ext_bwd);
+    CKL();
+  }
+  CK(gemm(ls::GEMM_DX, c->dqkv_bf, c->nqkv, T, w.pqkv, w.aqkv, c->nqkv, H, c->du_ext, c->ext_bwd, use ? 32 : 0,
+          ls::EPI_F32, c->dn, H, nullptr, 0, st));
+  ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, x_in, c->rstd1, w.w1, c->gx, c->gx_bf, T, H, 1);
+  CKL();
+  return LS_OK;
+}
+
+int sticky(ls_ctx* c) {
+  if (!c) return set_thread_err(LS_ERR_ARG, "null context");
+  if (c->err) {
+    g_thread_err = c->msg;
+    return c->err;
+  }
+  return LS_OK;
+}
+
+}  // namespace
+
+// ====================================================================== exported API
+
+extern "C" {
+
+int ls_plan(const ls_config* cfg, uint64_t* device_bytes) {
+  std::string why;
+  int rc = check_cfg(cfg, why);
+  if (rc) return set_thread_err(rc, why);
+  Planned p = lay_out(*cfg, nullptr);
+  if (device_bytes) *device_bytes = p.total;
+  if (cfg->cap_bytes && p.total > cfg->cap_bytes) {
+    char b[256];
+    snprintf(b, sizeof b, "pre-flight: workspace %.3f GB exceeds the cap %.3f GB", p.total / 1e9,
+             cfg->cap_bytes / 1e9);
+    return set_thread_err(LS_ERR_CAP, b);
+  }
+  return LS_OK;
+}
+
+int ls_layer_layout(const ls_config* cfg, uint64_t* offsets16, uint64_t* image_bytes) {
+  std::string why;
+  int rc = check_cfg(cfg, why);
+  if (rc) return set_thread_err(rc, why);
+  LayerLayout L = layer_layout(*cfg);
+  if (offsets16)
+    for (int i = 0; i < 16; ++i) offsets16[i] = L.off[i];
+  if (image_bytes) *image_bytes = L.bytes;
+  return LS_OK;
+}
+
+int ls_create(const ls_config* cfg, void* d_workspace, uint64_t ws_bytes, void* compute_stream, void* copy_stream,
+              ls_ctx** out) {
+  if (!out) return set_thread_err(LS_ERR_ARG, "null output pointer");
+  *out = nullptr;
+  uint64_t need = 0;
+  int rc = ls_plan(cfg, &need);
+  if (rc) return rc;
+  if (!d_workspace || ws_bytes < need)
+    return set_thread_err(LS_ERR_ARG, "workspace missing or smaller than ls_plan's size");
+  if (reinterpret_cast<uintptr_t>(d_workspace) % 256) return set_thread_err(LS_ERR_ARG, "workspace not 256-byte aligned");
+  if (!compute_stream || !copy_stream || compute_stream == copy_stream)
+    return set_thread_err(LS_ERR_ARG, "need two distinct caller streams");
+  cudaPointerAttributes pa{};
+  if (cudaPointerGetAttributes(&pa, d_workspace) != cudaSuccess || pa.type != cudaMemoryTypeDevice) {
+    cudaGetLastError();
+    return set_thread_err(LS_ERR_ARG, "workspace is not device memory");
+  }
+  ls_ctx* c = new ls_ctx();
+  c->cfg = *cfg;
+  c->cs = reinterpret_cast<cudaStream_t>(compute_stream);
+  c->cp = reinterpret_cast<cudaStream_t>(copy_stream);
+  c->ws = reinterpret_cast<uint8_t*>(d_workspace);
+  c->ws_bytes = ws_bytes;
+  c->L = cfg->layers; c->H = cfg->hidden; c->nh = cfg->heads; c->nkv = cfg->kv_heads; c->hd = cfg->head_dim;
+  c->I = cfg->inter; c->V = cfg->vocab; c->r = cfg->lora_r;
+  c->nq = c->nh * c->hd; c->nkvd = c->nkv * c->hd; c->nqkv = c->nq + 2 * c->nkvd;
+  c->Tmax = cfg->max_tokens;
+  c->maxlen = cfg->max_seq_len > 0 ? cfg->max_seq_len : cfg->max_tokens;
+  c->lay = layer_layout(*cfg);
+  Planned p = lay_out(*cfg, c);
+  c->hl.assign(c->L, ls_layer_host{});
+  c->hl_ok.assign(c->L, 0);
+  c->ad.assign(c->L, ls_ctx::Ad{});
+  c->st.workspace_bytes = p.total;
+  c->st.slot_bytes = p.slot_bytes;
+  c->st.act_store_bytes = p.act_bytes;
+  c->st.vocab_chunks = c->nvch;
+  c->st.vocab_chunk_rows = c->vrows;
+  for (int s = 0; s < 2; ++s) {
+    if (cudaEventCreateWithFlags(&c->ev_ready[s], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_free[s], cudaEventDisableTiming) != cudaSuccess) {
+      ls_destroy(c);
+      return set_thread_err(LS_ERR_CUDA, "event creation failed");
+    }
+  }
+  // RoPE tables
+  const int half = c->hd / 2;
+  std::vector<float> hc((size_t)c->maxlen * half), hs((size_t)c->maxlen * half);
+  ls_rope_table(hc.data(), hs.data(), c->maxlen, c->hd, cfg->rope_theta);
+  if (cudaMemcpyAsync(c->rope_cos, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice, c->cs) != cudaSuccess ||
+      cudaMemcpyAsync(c->rope_sin, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice, c->cs) != cudaSuccess ||
+      cudaStreamSynchronize(c->cs) != cudaSuccess) {
+    ls_destroy(c);
+    return set_thread_err(LS_ERR_CUDA, "rope table upload failed");
+  }
+  *out = c;
+  return LS_OK;
+}
+
+int ls_destroy(ls_ctx* c) {
+  if (!c) return LS_OK;
+  if (c->cs) cudaStreamSynchronize(c->cs);
+  if (c->cp) cudaStreamSynchronize(c->cp);
+  for (int s = 0; s < 2; ++s) {
+    if (c->ev_ready[s]) cudaEventDestroy(c->ev_ready[s]);
+    if (c->ev_free[s]) cudaEventDestroy(c->ev_free[s]);
+  }
+  delete c;
+  return LS_OK;
+}
+
+const char* ls_last_error(const ls_ctx* c) {
+  if (c && c->err) return c->msg.c_str();
+  return g_thread_err.c_str();
+}
+
+int nf4_quantize(const float* w, int64_t rows, int64_t cols, uint8_t* packed, float* absmax, int32_t nthreads) {
+  if (!w || !packed || !absmax || rows < 0 || cols <= 0 || cols % 64)
+    return set_thread_err(LS_ERR_ARG, "nf4_quantize: null pointer or cols not a positive multiple of 64");
+  int nt = nthreads > 0 ? nthreads : (int)std::max(1u, std::thread::hardware_concurrency());
+  if (rows < nt * 4) nt = (int)std::max<int64_t>(1, rows / 4);
+  std::vector<std::thread> th;
+  const int64_t per = (rows + nt - 1) / nt;
+  for (int i = 0; i < nt; ++i) {
+    const int64_t r0 = i * per, r1 = std::min(rows, r0 + per);
+    if (r0 >= r1) break;
+    th.emplace_back(quantize_rows, w, r0, r1, cols, packed, absmax);
+  }
+  for (auto& t : th) t.join();
+  return LS_OK;
+}
+
+static int check_pinned(const void* p, const char* what, std::string& why) {
+  if (!p) { why = std::string(what) + ": null pointer"; return LS_ERR_ARG; }
+  cudaPointerAttributes a{};
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess || a.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    why = std::string(what) + ": not pinned host memory (use cudaHostAlloc or cudaHostRegister)";
+    return LS_ERR_ARG;
+  }
+  return LS_OK;
+}
+
+int load_layer_nf4(ls_ctx* c, int32_t layer, const ls_layer_host* h) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!h || layer < 0 || layer >= c->L) return fail(c, LS_ERR_ARG, "load_layer_nf4: bad layer index or null");
+  std::string why;
+  const ls_nf4_host* m7[7] = {&h->q, &h->k, &h->v, &h->o, &h->gate, &h->up, &h->down};
+  const char* names[7] = {"q", "k", "v", "o", "gate", "up", "down"};
+  for (int m = 0; m < 7; ++m) {
+    if ((rc = check_pinned(m7[m]->packed, names[m], why)) || (rc = check_pinned(m7[m]->absmax, names[m], why)))
+      return set_thread_err(rc, "load_layer_nf4: " + why);
+  }
+  if ((rc = check_pinned(h->attn_norm, "attn_norm", why)) || (rc = check_pinned(h->mlp_norm, "mlp_norm", why)))
+    return set_thread_err(rc, "load_layer_nf4: " + why);
+  c->hl[layer] = *h;
+  c->hl_ok[layer] = 1;
+  if (c->cfg.resident) c->res_loaded[layer] = 0;
+  for (int s = 0; s < 2; ++s)
+    if (c->slot_item[s] == layer) c->slot_item[s] = -1;
+  return LS_OK;
+}
+
+int load_vocab_nf4(ls_ctx* c, const ls_vocab_host* h) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!h) return fail(c, LS_ERR_ARG, "load_vocab_nf4: null");
+  std::string why;
+  if ((rc = check_pinned(h->embed.packed, "embed", why)) || (rc = check_pinned(h->embed.absmax, "embed", why)) ||
+      (rc = check_pinned(h->final_norm, "final_norm", why)))
+    return set_thread_err(rc, "load_vocab_nf4: " + why);
+  if (!c->cfg.tied && ((rc = check_pinned(h->lm_head.packed, "lm_head", why)) ||
+                       (rc = check_pinned(h->lm_head.absmax, "lm_head", why))))
+    return set_thread_err(rc, "load_vocab_nf4: " + why);
+  void* dp = nullptr;
+  void* da = nullptr;
+  if (cudaHostGetDevicePointer(&dp, const_cast<uint8_t*>(h->embed.packed), 0) != cudaSuccess ||
+      cudaHostGetDevicePointer(&da, const_cast<float*>(h->embed.absmax), 0) != cudaSuccess) {
+    cudaGetLastError();
+    return set_thread_err(LS_ERR_ARG, "load_vocab_nf4: embedding memory is not mapped for device access");
+  }
+  c->hv = *h;
+  c->hv_ok = true;
+  c->emb_p = reinterpret_cast<const uint8_t*>(dp);
+  c->emb_a = reinterpret_cast<const float*>(da);
+  CK(cudaMemcpyAsync(c->wf, h->final_norm, (size_t)c->H * 2, cudaMemcpyHostToDevice, c->cs));
+  CK(cudaStreamSynchronize(c->cs));
+  for (int i = 0; i < c->nvch; ++i) {
+    if (c->cfg.resident) c->res_loaded[c->L + i] = 0;
+    for (int s = 0; s < 2; ++s)
+      if (c->slot_item[s] == c->L + i) c->slot_item[s] = -1;
+  }
+  return LS_OK;
+}
+
+int ls_set_adapter(ls_ctx* c, int32_t layer, const uint16_t* aq, const uint16_t* bq, const uint16_t* av,
+                   const uint16_t* bv, float* gaq, float* gbq, float* gav, float* gbv) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (layer < 0 || layer >= c->L) return fail(c, LS_ERR_ARG, "ls_set_adapter: bad layer");
+  ls_ctx::Ad a;
+  a.aq = reinterpret_cast<const bf16*>(aq); a.bq = reinterpret_cast<const bf16*>(bq);
+  a.av = reinterpret_cast<const bf16*>(av); a.bv = reinterpret_cast<const bf16*>(bv);
+  a.gaq = gaq; a.gbq = gbq; a.gav = gav; a.gbv = gbv;
+  a.on = aq && bq && av && bv;
+  if (a.on && !(gaq && gbq && gav && gbv)) return fail(c, LS_ERR_ARG, "ls_set_adapter: gradient buffers missing");
+  c->ad[layer] = a;
+  return LS_OK;
+}
+
+int stream_step_fwd(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t nseq, const int32_t* d_cu,
+                    const uint8_t* d_mask, int32_t adapter_on, int32_t save_acts, float* d_sums) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!d_tokens || !d_cu || !d_mask || T < 1 || T > c->Tmax || nseq < 1 || nseq > c->cfg.max_seqs)
+    return fail(c, LS_ERR_ARG, "stream_step_fwd: bad tokens/offsets/mask or T/nseq outside the configured bounds");
+  for (int l = 0; l < c->L; ++l)
+    if (!c->hl_ok[l]) return fail(c, LS_ERR_STATE, "stream_step_fwd: layer " + std::to_string(l) + " not loaded");
+  if (!c->hv_ok) return fail(c, LS_ERR_STATE, "stream_step_fwd: vocabulary not loaded");
+  cudaStream_t st = c->cs;
+  const int H = c->H;
+  const bool save = save_acts != 0;
+  ls::seq_setup_kernel<<<(T + 255) / 256, 256, 0, st>>>(d_tokens, d_cu, nseq, nullptr, nullptr, c->pos, c->tgt,
+                                                       nullptr, T);
+  CKL();
+  bf16* x0 = save ? c->acts : c->xping;
+  {
+    const long long n = (long long)T * (H / 8);
+    ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, st>>>(d_tokens, c->emb_p, c->emb_a, x0, T, H);
+    CKL();
+  }
+  bf16* hf = save ? c->hf_save : c->hf_tmp;
+  float* rstdf = save ? c->rstdf_save : c->rstdf_tmp;
+  float* lse = save ? c->lse_save : c->lse_tmp;
+  const size_t TH = (size_t)T * H;
+  std::vector<int> items;
+  for (int l = 0; l < c->L; ++l) items.push_back(l);
+  for (int v = 0; v < c->nvch; ++v) items.push_back(c->L + v);
+  rc = run_items(c, items, [&](int item, uint8_t* img) -> int {
+    if (item < c->L) {
+      const int l = item;
+      const bf16* xin = save ? c->acts + (size_t)l * (size_t)c->Tmax * H : c->xping + (size_t)(l & 1) * TH;
+      bf16* xout = save ? c->acts + (size_t)(l + 1) * (size_t)c->Tmax * H : c->xping + (size_t)((l + 1) & 1) * TH;
+      return layer_forward(c, layer_ptrs(c, img), l, xin, xout, T, nseq, d_cu, adapter_on != 0, false);
+    }
+    const int ch = item - c->L;
+    if (ch == 0) {
+      const bf16* xL = save ? c->acts + (size_t)c->L * (size_t)c->Tmax * H : c->xping + (size_t)(c->L & 1) * TH;
+      ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(xL, c->wf, hf, rstdf, T, H, c->cfg.eps);
+      CKL();
+    }
+    const int v0 = ch * c->vrows;
+    const int n = std::min(c->vrows, c->V - v0);
+    GemmCall g{};
+    g.mode = ls::GEMM_FWD;
+    g.A = hf;
+    g.lda = H;
+    g.Wp = img;
+    g.force_bn = 256;
+    g.g.M = T; g.g.Nw = n; g.g.Kw = H; g.g.Nout = n; g.g.Kred = H;
+    g.g.absmax = reinterpret_cast<const float*>(img + c->vch_abs_off);
+    g.g.epi = ls::EPI_LOGPROB;
+    g.g.targets = c->tgt;
+    g.g.vocab_off = v0;
+    g.g.part_max = c->pmax; g.g.part_sum = c->psum; g.g.part_ld = c->P;
+    g.g.tgt_logit = c->tgt_logit;
+    CK(ls::launch_nf4_gemm(g, st));
+    return LS_OK;
+  });
+  if (rc) return rc;
+  ls::logprob_combine_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->pmax, c->psum, c->P, c->P, c->tgt_logit, c->tgt, lse,
+                                                         c->lp, T);
+  CKL();
+  if (d_sums) {
+    ls::seq_sum_kernel<<<nseq, 256, 0, st>>>(c->lp, d_mask, d_cu, d_sums);
+    CKL();
+  }
+  c->last_T = T;
+  c->last_lse = lse;
+  if (save) {
+    c->saved = true;
+    c->s_tokens = d_tokens; c->s_cu = d_cu; c->s_mask = d_mask; c->s_T = T; c->s_nseq = nseq;
+  }
+  return LS_OK;
+}
+
+int seq_logprobs(ls_ctx* c, float* d_lp, float* d_lse) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!c->last_T) return fail(c, LS_ERR_STATE, "seq_logprobs: no forward pass yet");
+  if (d_lp) CK(cudaMemcpyAsync(d_lp, c->lp, (size_t)c->last_T * 4, cudaMemcpyDeviceToDevice, c->cs));
+  if (d_lse) CK(cudaMemcpyAsync(d_lse, c->last_lse, (size_t)c->last_T * 4, cudaMemcpyDeviceToDevice, c->cs));
+  return LS_OK;
+}
+
+int dpo_loss(ls_ctx* c, const float* d_pi, const float* d_ref, int32_t npairs, float beta, float* d_loss,
+             float* d_coeffs) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!d_pi || !d_ref || npairs < 1) return fail(c, LS_ERR_ARG, "dpo_loss: bad arguments");
+  ls::dpo_loss_kernel<<<1, 32, 0, c->cs>>>(d_pi, d_ref, npairs, beta, d_loss, d_coeffs);
+  CKL();
+  return LS_OK;
+}
+
+}  // extern "C"
+
+namespace ls {
+__global__ void sft_loss_kernel(const float* sums, int nseq, float count, float* loss, float* coeffs) {
+  if (threadIdx.x != 0) return;
+  float s = 0.f;
+  for (int i = 0; i < nseq; ++i) s += sums[i];
+  if (loss) *loss = -s / count;
+  if (coeffs)
+    for (int i = 0; i < nseq; ++i) coeffs[i] = -1.f / count;
+}
+}  // namespace ls
+
+extern "C" {
+
+int sft_loss(ls_ctx* c, const float* d_sums, int32_t nseq, float count, float* d_loss, float* d_coeffs) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!d_sums || nseq < 1 || !(count > 0.f)) return fail(c, LS_ERR_ARG, "sft_loss: bad arguments");
+  ls::sft_loss_kernel<<<1, 32, 0, c->cs>>>(d_sums, nseq, count, d_loss, d_coeffs);
+  CKL();
+  return LS_OK;
+}
+
+int stream_step_bwd(ls_ctx* c, const float* d_coeffs) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!c->saved) return fail(c, LS_ERR_STATE, "stream_step_bwd: no forward pass with save_acts=1");
+  if (!d_coeffs) return fail(c, LS_ERR_ARG, "stream_step_bwd: null coefficients");
+  cudaStream_t st = c->cs;
+  const int T = c->s_T, nseq = c->s_nseq, H = c->H;
+  const int32_t* cu = c->s_cu;
+  ls::seq_setup_kernel<<<(T + 255) / 256, 256, 0, st>>>(c->s_tokens, cu, nseq, c->s_mask, d_coeffs, c->pos, c->tgt,
+                                                       c->coef, T);
+  CKL();
+  std::vector<int> items;
+  for (int v = c->nvch - 1; v >= 0; --v) items.push_back(c->L + v);
+  for (int l = c->L - 1; l >= 0; --l) items.push_back(l);
+  bool first_chunk = true;
+  rc = run_items(c, items, [&](int item, uint8_t* img) -> int {
+    if (item >= c->L) {
+      const int ch = item - c->L;
+      const int v0 = ch * c->vrows;
+      const int n = std::min(c->vrows, c->V - v0);
+      const float* wa = reinterpret_cast<const float*>(img + c->vch_abs_off);
+      GemmCall g{};
+      g.mode = ls::GEMM_FWD;
+      g.A = c->hf_save;
+      g.lda = H;
+      g.Wp = img;
+      g.force_bn = 256;
+      g.g.M = T; g.g.Nw = n; g.g.Kw = H; g.g.Nout = n; g.g.Kred = H;
+      g.g.absmax = wa;
+      g.g.epi = ls::EPI_DLOGITS;
+      g.g.out = c->dlogits; g.g.ldo = n;
+      g.g.targets = c->tgt; g.g.vocab_off = v0;
+      g.g.lse = c->lse_save; g.g.coef = c->coef;
+      CK(ls::launch_nf4_gemm(g, st));
+      CK(gemm(ls::GEMM_DX, c->dlogits, n, T, img, wa, n, H, nullptr, nullptr, 0,
+              first_chunk ? ls::EPI_F32 : ls::EPI_F32_ACC, c->dhf, H, nullptr, 0, st));
+      first_chunk = false;
+      if (ch == 0) {
+        const bf16* xL = c->acts + (size_t)c->L * (size_t)c->Tmax * H;
+        ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dhf, xL, c->rstdf_save, c->wf, c->gx, c->gx_bf, T, H, 0);
+        CKL();
+      }
+      return LS_OK;
+    }
+    const int l = item;
+    const bf16* xin = c->acts + (size_t)l * (size_t)c->Tmax * H;
+    return layer_backward(c, layer_ptrs(c, img), l, xin, T, nseq, cu);
+  });
+  return rc;
+}
+
+int lora_grads(ls_ctx* c, float* d_flat, int32_t zero_after) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  size_t off = 0;
+  for (int l = 0; l < c->L; ++l) {
+    const ls_ctx::Ad& a = c->ad[l];
+    if (!a.on) continue;
+    float* g4[4] = {a.gaq, a.gbq, a.gav, a.gbv};
+    const size_t n4[4] = {(size_t)c->r * c->H, (size_t)c->nq * c->r, (size_t)c->r * c->H, (size_t)c->nkvd * c->r};
+    for (int i = 0; i < 4; ++i) {
+      if (d_flat) CK(cudaMemcpyAsync(d_flat + off, g4[i], n4[i] * 4, cudaMemcpyDeviceToDevice, c->cs));
+      if (zero_after) CK(cudaMemsetAsync(g4[i], 0, n4[i] * 4, c->cs));
+      off += n4[i];
+    }
+  }
+  return LS_OK;
+}
+
+int ls_sync(ls_ctx* c, int32_t timeout_ms) {
+  if (!c) return set_thread_err(LS_ERR_ARG, "null context");
+  cudaEvent_t e[2];
+  CK(cudaEventCreateWithFlags(&e[0], cudaEventDisableTiming));
+  CK(cudaEventCreateWithFlags(&e[1], cudaEventDisableTiming));
+  CK(cudaEventRecord(e[0], c->cs));
+  CK(cudaEventRecord(e[1], c->cp));
+  const auto t0 = std::chrono::steady_clock::now();
+  int result = LS_OK;
+  for (int i = 0; i < 2; ++i) {
+    for (;;) {
+      cudaError_t q = cudaEventQuery(e[i]);
+      if (q == cudaSuccess) break;
+      if (q != cudaErrorNotReady) {
+        result = fail(c, LS_ERR_CUDA, std::string("ls_sync: ") + cudaGetErrorString(q));
+        break;
+      }
+      const double ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+      if (timeout_ms > 0 && ms > timeout_ms) {
+        result = LS_ERR_TIMEOUT;
+        g_thread_err = "ls_sync: streams still busy after " + std::to_string(timeout_ms) + " ms";
+        break;
+      }
+      std::this_thread::sleep_for(std::chrono::microseconds(100));
+    }
+    if (result) break;
+  }
+  cudaEventDestroy(e[0]);
+  cudaEventDestroy(e[1]);
+  if (result) return result;
+  int dev = 0;
+  CK(cudaMemcpyFromSymbol(&dev, ls::g_device_error, sizeof(int)));
+  if (dev) return fail(c, LS_ERR_DEVICE, "a kernel raised device error " + std::to_string(dev));
+  return LS_OK;
+}
+
+int ls_stats(ls_ctx* c, ls_stats_t* out, int32_t reset) {
+  if (!c || !out) return set_thread_err(LS_ERR_ARG, "ls_stats: null argument");
+  *out = c->st;
+  if (reset) {
+    c->st.layer_reads = c->st.vocab_reads = c->st.h2d_bytes = c->st.slot_reuses = 0;
+  }
+  return LS_OK;
+}
+
+int ls_debug_copy_delay(ls_ctx* c, int32_t ms) {
+  if (!c) return set_thread_err(LS_ERR_ARG, "null context");
+  c->copy_delay_ms = ms > 0 ? ms : 0;
+  return LS_OK;
+}
+
+// ====================================================================== kernel-level API
+
+#define KCK(expr)                                                                      \
+  do {                                                                                 \
+    cudaError_t e_ = (expr);                                                           \
+    if (e_ != cudaSuccess) return set_thread_err(LS_ERR_CUDA, cudaGetErrorString(e_)); \
+  } while (0)
+#define KLAUNCH() KCK(cudaGetLastError())
+#define STREAM(s) reinterpret_cast<cudaStream_t>(s)
+
+int lsk_nf4_dequant(const uint8_t* packed, const float* absmax, int64_t rows, int32_t cols, uint16_t* out, void* s) {
+  if (!packed || !absmax || !out || rows < 0 || cols <= 0 || cols % 64) return set_thread_err(LS_ERR_ARG, "lsk_nf4_dequant: bad args");
+  const long long n = rows * (cols / 8);
+  if (n == 0) return LS_OK;
+  ls::nf4_dequant_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(packed, absmax, reinterpret_cast<bf16*>(out), rows, cols);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const uint8_t* wp, const float* wa,
+                 int32_t N, int32_t K, const uint16_t* ext_a, const uint16_t* ext_b, int32_t ext_k, int32_t epi,
+                 void* out, int64_t ldo, const uint16_t* residual, int64_t ldr, int32_t force_bn, int32_t force_nacc,
+                 void* s) {
+  if (mode != 0 && mode != 1) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: mode must be 0 or 1");
+  if (!A || !wp || !wa || !out || M < 0 || N <= 0 || K <= 0 || K % 64 || N % 64)
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: null pointer or N, K not positive multiples of 64");
+  if (epi < 0 || epi > 2) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: epi must be 0, 1 or 2");
+  if (ext_k != 0 && ext_k != 16 && ext_k != 32) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: ext_k must be 0, 16, 32");
+  if (ext_k && (!ext_a || !ext_b)) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: ext operands missing");
+  const int outc = mode == 0 ? N : K;
+  const int red = mode == 0 ? K : N;
+  if (lda < red || lda % 8 || ldo < outc || ldo % 8 || (residual && (ldr < outc || ldr % 8)))
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: leading dimensions too small or not multiples of 8");
+  if (force_bn != 0 && force_bn != 128 && force_bn != 256) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: force_bn");
+  if (force_nacc < 0 || force_nacc > 2) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: force_nacc");
+  if (residual && epi != 0) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: residual only with bf16 output");
+  KCK(gemm(mode, reinterpret_cast<const bf16*>(A), lda, M, wp, wa, N, K, reinterpret_cast<const bf16*>(ext_a),
+           reinterpret_cast<const bf16*>(ext_b), ext_k, epi, out, ldo, reinterpret_cast<const bf16*>(residual), ldr,
+           STREAM(s), force_bn, force_nacc));
+  return LS_OK;
+}
+
+int lsk_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, float* rstd, int32_t T, int32_t H, float eps,
+                    void* s) {
+  if (!x || !w || !y || T < 0 || H <= 0 || H % 8) return set_thread_err(LS_ERR_ARG, "lsk_rmsnorm_fwd: bad args");
+  if (T == 0) return LS_OK;
+  ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(x), reinterpret_cast<const bf16*>(w),
+                                                            reinterpret_cast<bf16*>(y), rstd, T, H, eps);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_rmsnorm_bwd(const float* dy, const uint16_t* x, const float* rstd, const uint16_t* w, float* dx,
+                    uint16_t* dx_bf16, int32_t T, int32_t H, int32_t accumulate, void* s) {
+  if (!dy || !x || !rstd || !w || !dx || T < 0 || H <= 0 || H % 4) return set_thread_err(LS_ERR_ARG, "lsk_rmsnorm_bwd: bad args");
+  if (T == 0) return LS_OK;
+  ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, STREAM(s)>>>(dy, reinterpret_cast<const bf16*>(x), rstd,
+                                                            reinterpret_cast<const bf16*>(w), dx,
+                                                            reinterpret_cast<bf16*>(dx_bf16), T, H, accumulate);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int ls_rope_table(float* hc, float* hs, int32_t max_pos, int32_t hd, float theta) {
+  if (!hc || !hs || max_pos < 1 || hd < 2 || hd % 2) return set_thread_err(LS_ERR_ARG, "ls_rope_table: bad args");
+  const int half = hd / 2;
+  for (int i = 0; i < half; ++i) {
+    const double inv = std::pow((double)theta, -2.0 * i / hd);
+    for (int p = 0; p < max_pos; ++p) {
+      const double a = p * inv;
+      hc[(size_t)p * half + i] = (float)std::cos(a);
+      hs[(size_t)p * half + i] = (float)std::sin(a);
+    }
+  }
+  return LS_OK;
+}
+
+int lsk_rope_fwd(uint16_t* qkv, int64_t ld, const int32_t* pos, const float* ct, const float* stt, int32_t T,
+                 int32_t nheads, int32_t hd, void* s) {
+  if (!qkv || !pos || !ct || !stt || T < 0 || nheads < 1 || hd % 2 || ld < (int64_t)nheads * hd)
+    return set_thread_err(LS_ERR_ARG, "lsk_rope_fwd: bad args");
+  const long long n = (long long)T * nheads * (hd / 2);
+  if (n == 0) return LS_OK;
+  ls::rope_fwd_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(reinterpret_cast<bf16*>(qkv), ld, pos, ct, stt, T, nheads, hd);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_rope_bwd_cast(const float* g, uint16_t* out, int64_t ld, const int32_t* pos, const float* ct,
+                      const float* stt, int32_t T, int32_t nrot, int32_t hd, int32_t ncols, void* s) {
+  if (!g || !out || !pos || !ct || !stt || T < 0 || ncols > ld || nrot * hd > ncols)
+    return set_thread_err(LS_ERR_ARG, "lsk_rope_bwd_cast: bad args");
+  const long long n = (long long)T * ncols;
+  if (n == 0) return LS_OK;
+  ls::rope_bwd_cast_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(g, reinterpret_cast<bf16*>(out), ld, pos, ct, stt, T,
+                                                                  nrot, hd, ncols);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_attn_fwd(const uint16_t* qkv, int64_t ld, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh,
+                 int32_t nkv, int32_t hd, uint16_t* out, int64_t ldo, float* lse, int32_t T, void* s) {
+  if (!qkv || !cu || !out || !lse || nseq < 1 || max_len < 1 || nh < 1 || nkv < 1 || nh % nkv ||
+      (hd != 64 && hd != 128) || ld < (int64_t)(nh + 2 * nkv) * hd || ld % 8 || ldo % 8)
+    return set_thread_err(LS_ERR_ARG, "lsk_attn_fwd: bad args");
+  KCK(attn_fwd(hd, reinterpret_cast<const bf16*>(qkv), ld, cu, nseq, max_len, nh, nkv, reinterpret_cast<bf16*>(out),
+               ldo, lse, T, STREAM(s)));
+  return LS_OK;
+}
+
+int lsk_attn_bwd(const uint16_t* qkv, int64_t ld, const uint16_t* dout, const uint16_t* o, int64_t lddo,
+                 const float* lse, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh, int32_t nkv,
+                 int32_t hd, float* D, float* dqkv, int64_t ldg, int32_t T, void* s) {
+  if (!qkv || !dout || !o || !lse || !cu || !D || !dqkv || nseq < 1 || max_len < 1 || nh % nkv ||
+      (hd != 64 && hd != 128) || ld % 8 || lddo % 8 || ldg % 2)
+    return set_thread_err(LS_ERR_ARG, "lsk_attn_bwd: bad args");
+  KCK(attn_bwd(hd, reinterpret_cast<const bf16*>(qkv), ld, reinterpret_cast<const bf16*>(dout),
+               reinterpret_cast<const bf16*>(o), lddo, lse, cu, nseq, max_len, nh, nkv, D, dqkv, ldg, T, STREAM(s)));
+  return LS_OK;
+}
+
+int lsk_swiglu_fwd(const uint16_t* gu, uint16_t* h, int32_t T, int32_t I, void* s) {
+  if (!gu || !h || T < 0 || I <= 0 || I % 8) return set_thread_err(LS_ERR_ARG, "lsk_swiglu_fwd: bad args");
+  const long long n = (long long)T * (I / 8);
+  if (n == 0) return LS_OK;
+  ls::swiglu_fwd_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(gu), reinterpret_cast<bf16*>(h), T, I);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_swiglu_bwd(const float* dh, const uint16_t* gu, uint16_t* dgu, int32_t T, int32_t I, void* s) {
+  if (!dh || !gu || !dgu || T < 0 || I <= 0 || I % 4) return set_thread_err(LS_ERR_ARG, "lsk_swiglu_bwd: bad args");
+  const long long n = (long long)T * (I / 4);
+  if (n == 0) return LS_OK;
+  ls::swiglu_bwd_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(dh, reinterpret_cast<const bf16*>(gu), reinterpret_cast<bf16*>(dgu), T, I);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_lora_down(const uint16_t* x, int64_t ldx, const uint16_t* aq, const uint16_t* av, int32_t r, int32_t K,
+                  float sc, uint16_t* u_ext, int32_t T, void* s) {
+  if (!x || !u_ext || r < 1 || r > 16 || K <= 0 || K % 8 || ldx < K || ldx % 8 || T < 0)
+    return set_thread_err(LS_ERR_ARG, "lsk_lora_down: bad args");
+  if (T == 0) return LS_OK;
+  ls::lora_down_kernel<<<(T + 7) / 8, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(x), ldx,
+                                                          reinterpret_cast<const bf16*>(aq),
+                                                          reinterpret_cast<const bf16*>(av), r, K, sc,
+                                                          reinterpret_cast<bf16*>(u_ext), T);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_lora_du(const uint16_t* dy, int64_t ldy, int32_t col_q, int32_t nq, const uint16_t* bq, int32_t col_v,
+                int32_t nv, const uint16_t* bv, int32_t r, float sc, float* du, uint16_t* du_ext, int32_t T, void* s) {
+  if (!dy || !du || !du_ext || r < 1 || r > 16 || T < 0) return set_thread_err(LS_ERR_ARG, "lsk_lora_du: bad args");
+  if (T == 0) return LS_OK;
+  ls::lora_du_kernel<<<(T + 7) / 8, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(dy), ldy, col_q, nq,
+                                                        reinterpret_cast<const bf16*>(bq), col_v, nv,
+                                                        reinterpret_cast<const bf16*>(bv), r, sc, du,
+                                                        reinterpret_cast<bf16*>(du_ext), T);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* uf, const uint16_t* ub, int32_t ldu,
+                   int32_t r, int32_t T, int32_t layout, int32_t accumulate, float* scratch, int32_t rpc, float* out,
+                   void* s) {
+  if (!X || (!uf && !ub) || !scratch || !out || r < 1 || r > 16 || ncols < 1 || T < 1 || rpc < 1 ||
+      (layout != 0 && layout != 1))
+    return set_thread_err(LS_ERR_ARG, "lsk_lora_outer: bad args");
+  KCK(lora_outer(reinterpret_cast<const bf16*>(X), ldx, ncols, uf, reinterpret_cast<const bf16*>(ub), ldu, r, T,
+                 layout, accumulate, scratch, rpc, out, STREAM(s)));
+  return LS_OK;
+}
+
+int lsk_build_ext_fwd(const uint16_t* bq, int32_t q0, int32_t nq, const uint16_t* bv, int32_t v0, int32_t nv,
+                      int32_t r, int32_t N, uint16_t* ext, void* s) {
+  if (!ext || N < 1 || r < 1 || r > 16) return set_thread_err(LS_ERR_ARG, "lsk_build_ext_fwd: bad args");
+  const int n = N * 64;
+  ls::build_ext_fwd_kernel<<<(n + 255) / 256, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(bq), q0, nq,
+                                                                  reinterpret_cast<const bf16*>(bv), v0, nv, r, N,
+                                                                  reinterpret_cast<bf16*>(ext));
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_build_ext_bwd(const uint16_t* aq, const uint16_t* av, int32_t r, int32_t K, uint16_t* ext, void* s) {
+  if (!ext || K < 1 || r < 1 || r > 16) return set_thread_err(LS_ERR_ARG, "lsk_build_ext_bwd: bad args");
+  const int n = K * 64;
+  ls::build_ext_bwd_kernel<<<(n + 255) / 256, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(aq),
+                                                                  reinterpret_cast<const bf16*>(av), r, K,
+                                                                  reinterpret_cast<bf16*>(ext));
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_embed_gather(const int32_t* tokens, const uint8_t* packed, const float* absmax, uint16_t* x, int32_t T,
+                     int32_t H, void* s) {
+  if (!tokens || !packed || !absmax || !x || T < 0 || H % 64) return set_thread_err(LS_ERR_ARG, "lsk_embed_gather: bad args");
+  const long long n = (long long)T * (H / 8);
+  if (n == 0) return LS_OK;
+  ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(tokens, packed, absmax, reinterpret_cast<bf16*>(x), T, H);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_vocab_logprob(const uint16_t* h, int32_t T, int32_t H, const uint8_t* wp, const float* wa, int32_t V,
+                      const int32_t* targets, float* scratch, float* tgt_logit, float* lse, float* lp, void* s) {
+  if (!h || !wp || !wa || !targets || !scratch || !tgt_logit || !lse || !lp || T < 1 || H % 64 || V % 64 || V < 64)
+    return set_thread_err(LS_ERR_ARG, "lsk_vocab_logprob: bad args");
+  const int P = (V + 127) / 128;
+  float* pmax = scratch;
+  float* psum = scratch + (size_t)T * P;
+  GemmCall g{};
+  g.mode = ls::GEMM_FWD;
+  g.A = reinterpret_cast<const bf16*>(h);
+  g.lda = H;
+  g.Wp = wp;
+  g.force_bn = 256;
+  g.g.M = T; g.g.Nw = V; g.g.Kw = H; g.g.Nout = V; g.g.Kred = H;
+  g.g.absmax = wa;
+  g.g.epi = ls::EPI_LOGPROB;
+  g.g.targets = targets; g.g.vocab_off = 0;
+  g.g.part_max = pmax; g.g.part_sum = psum; g.g.part_ld = P;
+  g.g.tgt_logit = tgt_logit;
+  KCK(ls::launch_nf4_gemm(g, STREAM(s)));
+  ls::logprob_combine_kernel<<<(T + 7) / 8, 256, 0, STREAM(s)>>>(pmax, psum, P, P, tgt_logit, targets, lse, lp, T);
+  KLAUNCH();
+  return LS_OK;
+}
+
+int lsk_vocab_bwd(const uint16_t* h, int32_t T, int32_t H, const uint8_t* wp, const float* wa, int32_t v0, int32_t n,
+                  const int32_t* targets, const float* lse, const float* coef, uint16_t* dlogits, float* dh,
+                  int32_t accumulate, void* s) {
+  if (!h || !wp || !wa || !targets || !lse || !coef || !dlogits || !dh || T < 1 || H % 64 || n % 64 || n < 64)
+    return set_thread_err(LS_ERR_ARG, "lsk_vocab_bwd: bad args");
+  GemmCall g{};
+  g.mode = ls::GEMM_FWD;
+  g.A = reinterpret_cast<const bf16*>(h);
+  g.lda = H;
+  g.Wp = wp;
+  g.force_bn = 256;
+  g.g.M = T; g.g.Nw = n; g.g.Kw = H; g.g.Nout = n; g.g.Kred = H;
+  g.g.absmax = wa;
+  g.g.epi = ls::EPI_DLOGITS;
+  g.g.out = dlogits; g.g.ldo = n;
+  g.g.targets = targets; g.g.vocab_off = v0;
+  g.g.lse = lse; g.g.coef = coef;
+  KCK(ls::launch_nf4_gemm(g, STREAM(s)));
+  KCK(gemm(ls::GEMM_DX, reinterpret_cast<const bf16*>(dlogits), n, T, wp, wa, n, H, nullptr, nullptr, 0,
+           accumulate ? ls::EPI_F32_ACC : ls::EPI_F32, dh, H, nullptr, 0, STREAM(s)));
+  return LS_OK;
+}
+
+int lsk_device_error(int32_t* h_out, int32_t reset) {
+  int v = 0;
+  KCK(cudaMemcpyFromSymbol(&v, ls::g_device_error, sizeof(int)));
+  if (h_out) *h_out = v;
+  if (reset) {
+    int z = 0;
+    KCK(cudaMemcpyToSymbol(ls::g_device_error, &z, sizeof(int)));
+  }
+  return LS_OK;
+}
+
+}  // extern "C"

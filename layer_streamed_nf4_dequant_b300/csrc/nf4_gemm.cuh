@@ -1,0 +1,427 @@
+// NF4-dequant-fused bf16 GEMM on the 5th-gen tensor cores (tcgen05 + TMEM).
+//
+// Frozen base weights of the streamed decoder layers are held as NF4: 4-bit codes
+// into the 16-value NormalFloat table, one fp32 absmax per 64 consecutive weights
+// of a row (the format QLoRA published; the Soup pages' "quantization: 4bit # NF4",
+// Soup: Fine-Tune an 8B Model on a 4 GB GPU, "The Core Idea: Layer Streaming").
+//
+//   FWD:  Y[M, N]  = X[M, K]  · deq(W)[N, K]^T   (q/k/v/o/gate/up/down, vocab logits)
+//   DX:   dX[M, K] = dY[M, N] · deq(W)[N, K]     (frozen-base backward: input grads only)
+//
+// plus an optional extra reduction stage of 16/32 columns that carries the LoRA
+// up-projection:  Y += [u_q | u_v] · B_ext^T  (forward) or  dX += [s du_q | s du_v] · A_ext
+// (backward).  deq(w) = bf16_rne(fp32(q[code]) * absmax): one fp32 multiply and one
+// rounding, identical bit for bit to the host definition.
+//
+// Pipeline per CTA (one BM x BN output tile, BM = 128 x NACC):
+//   warp 0      TMA producer: activation tile (SW128, K-major) + packed code tile,
+//               and the tile's absmax values by cp.async, into an S-deep ring.
+//   warps 2..9  dequantise codes into a K-major SW128 bf16 tile (transposed in
+//               registers for DX), an SB-deep ring; then run the epilogue.
+//   warp 1      one thread issues tcgen05.mma (M=128, N=BN, K=16) into TMEM
+//               accumulators, NACC of them sharing each dequantised B tile.
+// Epilogues: bf16 store (+ residual), fp32 store / accumulate, vocabulary
+// log-sum-exp partials with target-logit capture, and dlogits for the backward.
+#pragma once
+#include "common.cuh"
+
+namespace ls {
+
+__device__ __constant__ float kNF4Table[16] = {
+    -1.0f, -0.6961928009986877f, -0.5250730514526367f, -0.39491748809814453f,
+    -0.28444138169288635f, -0.18477343022823334f, -0.09105003625154495f, 0.0f,
+    0.07958029955625534f, 0.16093020814657211f, 0.24611230194568634f, 0.33791524171829224f,
+    0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
+
+__device__ float g_zero_word[4] = {0.f, 0.f, 0.f, 0.f};
+
+enum GemmMode : int { GEMM_FWD = 0, GEMM_DX = 1 };
+enum GemmEpi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_F32_ACC = 2, EPI_LOGPROB = 3, EPI_DLOGITS = 4 };
+
+struct GemmArgs {
+  int M, Nout, Kred;                 // output [M, Nout]; reduction length (multiple of 64)
+  int Nw, Kw;                        // W is [Nw, Kw]: FWD Nw=Nout, Kw=Kred; DX Nw=Kred, Kw=Nout
+  const float* absmax;               // [Nw, Kw/64]
+  int ext_k;                         // 0, 16 or 32 extra reduction columns
+  const __nv_bfloat16* ext_b;        // [Nout, 64] (columns >= ext_k are zero)
+  int epi;
+  void* out;
+  long long ldo;
+  const __nv_bfloat16* residual;     // EPI_BF16: optional [M, Nout] added before rounding
+  long long ldr;
+  const int* targets;                // EPI_LOGPROB / EPI_DLOGITS: global target id per row, -1 none
+  int vocab_off;                     // global id of output column 0
+  float* part_max;                   // EPI_LOGPROB: [M, part_ld] partial max / sum-exp
+  float* part_sum;
+  int part_ld;
+  float* tgt_logit;                  // EPI_LOGPROB: [M] logit of the target
+  const float* lse;                  // EPI_DLOGITS: [M]
+  const float* coef;                 // EPI_DLOGITS: [M] dL/dlogprob per row
+};
+
+template <int NACC, int BN, int S, int SB>
+struct GemmCfg {
+  static constexpr int BM = 128 * NACC;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int W_BYTES = BN * 32;
+  static constexpr int NDQ_WARPS = 8;
+  static constexpr int NDQ = NDQ_WARPS * 32;
+  static constexpr int THREADS = 64 + NDQ;
+  static constexpr int TMEM_COLS = NACC * BN;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + S * A_BYTES;
+  static constexpr int OFF_W = OFF_B + SB * B_BYTES;
+  static constexpr int OFF_ABS = OFF_W + S * W_BYTES;
+  static constexpr int OFF_TAB = OFF_ABS + S * BN * 4;
+  static constexpr int OFF_BAR = OFF_TAB + 64;
+  static constexpr int NBAR = 2 * S + 2 * SB + 1;
+  static constexpr int OFF_SLOT = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_SLOT + 16 + 1024;   // + slack to align the base to 1024
+  static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
+  static_assert(BN == 128 || BN == 256, "BN");
+};
+
+// -------------------------------------------------------------------------- dequantisers
+
+// FWD: B tile row j (output column n0 + j) holds 64 reduction values; unit = (row, 16-byte chunk).
+template <int BN, int NDQ>
+__device__ __forceinline__ void dequant_fwd(const uint8_t* Wt, const float* absS, uint8_t* Bt, int tq,
+                                            const float* tab) {
+#pragma unroll 2
+  for (int u = tq; u < BN * 8; u += NDQ) {
+    const int j = u >> 3, c = u & 7;
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(Wt + j * 32 + c * 4);
+    const float a = absS[j];
+    uint32_t o[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float e0 = tab[(w >> (8 * b + 4)) & 15] * a;   // element 2b: high nibble
+      const float e1 = tab[(w >> (8 * b)) & 15] * a;       // element 2b+1: low nibble
+      o[b] = pack_bf16x2(e0, e1);
+    }
+    *reinterpret_cast<uint4*>(Bt + j * 128 + ((c ^ (j & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// DX: W tile = 64 rows n (reduction) x BN columns k (output).  B tile row k holds the
+// 64 n-values.  Unit = 8 n x 8 k, transposed in registers; the k-row order is rotated
+// by the lane's column group so the 8 lanes of a store phase hit distinct banks.
+template <int BN, int NDQ>
+__device__ __forceinline__ void dequant_dx(const uint8_t* Wt, const float* absS, uint8_t* Bt, int tq,
+                                           const float* tab) {
+  constexpr int KG = BN / 8;
+  for (int u = tq; u < BN; u += NDQ) {
+    const int kg = u % KG, ng = u / KG;
+    uint32_t w[8];
+    float a[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      w[r] = *reinterpret_cast<const uint32_t*>(Wt + (8 * ng + r) * (BN / 2) + kg * 4);
+      a[r] = absS[(8 * ng + r) * (BN / 64) + (kg >> 3)];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int ip = (i + kg) & 7;
+      const int sh = 8 * (ip >> 1) + ((ip & 1) ? 0 : 4);
+      uint32_t o[4];
+#pragma unroll
+      for (int r = 0; r < 8; r += 2) {
+        const float e0 = tab[(w[r] >> sh) & 15] * a[r];
+        const float e1 = tab[(w[r + 1] >> sh) & 15] * a[r + 1];
+        o[r >> 1] = pack_bf16x2(e0, e1);
+      }
+      const int k = 8 * kg + ip;
+      *reinterpret_cast<uint4*>(Bt + k * 128 + ((ng ^ (k & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+template <int BN, int NDQ>
+__device__ __forceinline__ void copy_ext_tile(const __nv_bfloat16* ext_b, int n0, int Nout, uint8_t* Bt,
+                                              int tq) {
+  for (int u = tq; u < BN * 8; u += NDQ) {
+    const int j = u >> 3, c = u & 7;
+    const int n = n0 + j;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (n < Nout) v = *reinterpret_cast<const uint4*>(ext_b + (size_t)n * 64 + c * 8);
+    *reinterpret_cast<uint4*>(Bt + j * 128 + ((c ^ (j & 7)) << 4)) = v;
+  }
+}
+
+// -------------------------------------------------------------------------- epilogue pieces
+
+__device__ __forceinline__ void store_bf16_32(__nv_bfloat16* dst, const float (&f)[32], int nvalid) {
+  if (nvalid >= 32) {
+    uint32_t p[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+  } else {
+    for (int i = 0; i < nvalid; ++i) dst[i] = __float2bfloat16_rn(f[i]);
+  }
+}
+
+// -------------------------------------------------------------------------- kernel
+
+template <int NACC, int BN, int S, int SB, int MODE>
+__global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
+    nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmX, const GemmArgs g) {
+  using C = GemmCfg<NACC, BN, S, SB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * C::BM, n0 = blockIdx.y * BN;
+  const int KB = g.Kred / 64;
+  const int KBw = g.Kw / 64;
+  const int niter = KB + (g.ext_k > 0 ? 1 : 0);
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar0 = sb + C::OFF_BAR;
+  auto full = [&](int s) { return bar0 + s * 8; };
+  auto empty = [&](int s) { return bar0 + (S + s) * 8; };
+  auto bfull = [&](int s) { return bar0 + (2 * S + s) * 8; };
+  auto bempty = [&](int s) { return bar0 + (2 * S + SB + s) * 8; };
+  const uint32_t accfull = bar0 + (2 * S + 2 * SB) * 8;
+  float* s_tab = reinterpret_cast<float*>(smem + C::OFF_TAB);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1 + 32);
+      mbar_init(empty(s), 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(bfull(s), C::NDQ_WARPS);
+      mbar_init(bempty(s), 1);
+    }
+    mbar_init(accfull, 1);
+    fence_barrier_init();
+    s_abort = 0;
+  }
+  if (threadIdx.x < 16) s_tab[threadIdx.x] = kNF4Table[threadIdx.x];
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmW);
+    if (g.ext_k > 0) prefetch_tensormap(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + C::OFF_SLOT, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    for (int it = 0; it < niter; ++it) {
+      const int s = it % S;
+      if (s_abort || !mbar_wait(empty(s), ((it / S) & 1) ^ 1)) { s_abort = 1; break; }
+      const uint32_t a_dst = sb + C::OFF_A + s * C::A_BYTES;
+      if (lane == 0) {
+        if (it < KB) {
+          mbar_arrive_expect_tx(full(s), C::A_BYTES + C::W_BYTES);
+          tma_load_2d(a_dst, &tmA, it * 64, m0, full(s));
+          const uint32_t w_dst = sb + C::OFF_W + s * C::W_BYTES;
+          if (MODE == GEMM_FWD) tma_load_2d(w_dst, &tmW, it * 32, n0, full(s));
+          else tma_load_2d(w_dst, &tmW, n0 / 2, it * 64, full(s));
+        } else {
+          mbar_arrive_expect_tx(full(s), C::A_BYTES);
+          tma_load_2d(a_dst, &tmX, 0, m0, full(s));
+        }
+      }
+      if (it < KB) {
+        const uint32_t abs_dst = sb + C::OFF_ABS + s * BN * 4;
+        if (MODE == GEMM_FWD) {
+          for (int j = lane; j < BN; j += 32) {
+            const int n = n0 + j;
+            const float* src = n < g.Nw ? g.absmax + (size_t)n * KBw + it : g_zero_word;
+            cp_async_4(abs_dst + j * 4, src);
+          }
+        } else {
+          constexpr int CB = BN / 64;
+          for (int e = lane; e < 64 * CB; e += 32) {
+            const int r = e / CB, c = e % CB;
+            const int kb = n0 / 64 + c;
+            const float* src = kb < KBw ? g.absmax + (size_t)(it * 64 + r) * KBw + kb : g_zero_word;
+            cp_async_4(abs_dst + e * 4, src);
+          }
+        }
+      }
+      cp_async_mbar_arrive_noinc(full(s));
+      ++issued;
+    }
+    if (s_abort) {
+      // let copies already in flight land before the CTA's shared memory goes away
+      for (int j = issued - S < 0 ? 0 : issued - S; j < issued; ++j) mbar_wait(full(j % S), (j / S) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
+      for (int it = 0; it < niter; ++it) {
+        const int s = it % S, b = it % SB;
+        if (s_abort || !mbar_wait(full(s), (it / S) & 1) || !mbar_wait(bfull(b), (it / SB) & 1)) {
+          s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const int nk = it < KB ? 4 : g.ext_k / 16;
+        const uint32_t a_base = sb + C::OFF_A + s * C::A_BYTES;
+        const uint32_t b_base = sb + C::OFF_B + b * C::B_BYTES;
+        for (int k = 0; k < nk; ++k) {
+          const uint64_t bd = sw128_kmajor_desc(b_base + k * 32);
+#pragma unroll
+          for (int a = 0; a < NACC; ++a) {
+            const uint64_t ad = sw128_kmajor_desc(a_base + a * 16384 + k * 32);
+            tc_mma_bf16(tmem + a * BN, ad, bd, IDESC, (it > 0 || k > 0) ? 1u : 0u);
+          }
+        }
+        tc_commit(empty(s));
+        tc_commit(bempty(b));
+      }
+      tc_commit(accfull);
+      mbar_wait(accfull, 0);   // every MMA has retired before TMEM is released
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ dequant warps
+    const int tq = threadIdx.x - 64;
+    for (int it = 0; it < niter; ++it) {
+      const int s = it % S, b = it % SB;
+      if (s_abort || !mbar_wait(full(s), (it / S) & 1) || !mbar_wait(bempty(b), ((it / SB) & 1) ^ 1)) {
+        s_abort = 1;
+        break;
+      }
+      uint8_t* Bt = smem + C::OFF_B + b * C::B_BYTES;
+      if (it < KB) {
+        const uint8_t* Wt = smem + C::OFF_W + s * C::W_BYTES;
+        const float* absS = reinterpret_cast<const float*>(smem + C::OFF_ABS + s * BN * 4);
+        if (MODE == GEMM_FWD) dequant_fwd<BN, C::NDQ>(Wt, absS, Bt, tq, s_tab);
+        else dequant_dx<BN, C::NDQ>(Wt, absS, Bt, tq, s_tab);
+      } else {
+        copy_ext_tile<BN, C::NDQ>(g.ext_b, n0, g.Nout, Bt, tq);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bfull(b));
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (!s_abort && mbar_wait(accfull, 0)) {
+      tc_fence_after();
+      const int wq = warp & 3;
+      const int half = (warp - 2) >> 2;
+      for (int a = 0; a < NACC; ++a) {
+        const int row = m0 + a * 128 + wq * 32 + lane;
+        const bool rok = row < g.M;
+        float run_m = -INFINITY, run_s = 0.f;
+        int tgt = -1;
+        float lse_r = 0.f, coef_r = 0.f;
+        if (g.epi == EPI_LOGPROB || g.epi == EPI_DLOGITS) {
+          tgt = rok ? g.targets[row] - g.vocab_off : -1;
+          if (g.epi == EPI_DLOGITS && rok) {
+            lse_r = g.lse[row];
+            coef_r = g.coef[row];
+          }
+        }
+        for (int cc = 0; cc < BN / 64; ++cc) {
+          const int c0 = half * (BN / 2) + cc * 32;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * BN + c0), v);
+          tmem_ld_wait();
+          const int gc = n0 + c0;
+          const int nvalid = min(32, g.Nout - gc);
+          if (!rok || nvalid <= 0) continue;
+          float f[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          if (g.epi == EPI_BF16) {
+            if (g.residual) {
+              const __nv_bfloat16* rp = g.residual + (size_t)row * g.ldr + gc;
+              if (nvalid >= 32) {
+                const uint4* r4 = reinterpret_cast<const uint4*>(rp);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const uint4 rv = r4[q];
+                  const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    f[8 * q + 2 * e] += bf16lo(w4[e]);
+                    f[8 * q + 2 * e + 1] += bf16hi(w4[e]);
+                  }
+                }
+              } else {
+                for (int i = 0; i < nvalid; ++i) f[i] += bf2f(rp[i]);
+              }
+            }
+            store_bf16_32(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
+          } else if (g.epi == EPI_F32 || g.epi == EPI_F32_ACC) {
+            float* op = reinterpret_cast<float*>(g.out) + (size_t)row * g.ldo + gc;
+            if (nvalid >= 32) {
+              float4* o4 = reinterpret_cast<float4*>(op);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                float4 x = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                if (g.epi == EPI_F32_ACC) {
+                  const float4 y = o4[q];
+                  x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+                }
+                o4[q] = x;
+              }
+            } else {
+              for (int i = 0; i < nvalid; ++i) op[i] = (g.epi == EPI_F32_ACC ? op[i] : 0.f) + f[i];
+            }
+          } else if (g.epi == EPI_LOGPROB) {
+            float cm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) cm = fmaxf(cm, f[i]);
+            if (cm > run_m) {
+              run_s *= __expf(run_m - cm);
+              run_m = cm;
+            }
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) acc += __expf(f[i] - run_m);
+            run_s += acc;
+            const int rel = tgt - gc;
+            if (rel >= 0 && rel < nvalid) {
+              float t = 0.f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i == rel) t = f[i];
+              g.tgt_logit[row] = t;
+            }
+          } else {  // EPI_DLOGITS: coef * (onehot(target) - softmax)
+            const int rel = tgt - gc;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = coef_r * ((i == rel ? 1.f : 0.f) - __expf(f[i] - lse_r));
+            store_bf16_32(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
+          }
+        }
+        if (g.epi == EPI_LOGPROB && rok && n0 + half * (BN / 2) < g.Nout) {
+          const int p = (g.vocab_off + n0 + half * (BN / 2)) / (BN / 2);
+          g.part_max[(size_t)row * g.part_ld + p] = run_m;
+          g.part_sum[(size_t)row * g.part_ld + p] = run_s;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace ls

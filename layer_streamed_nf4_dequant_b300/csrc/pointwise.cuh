@@ -1,0 +1,468 @@
+// Bandwidth-bound kernels of the decoder layer and the loss: RMSNorm, RoPE, SwiGLU,
+// NF4 embedding gather, next-token targets, vocabulary log-sum-exp combine,
+// per-sequence logprob sums, the DPO loss, and the LoRA low-rank pieces.
+//
+// Rows are handled one warp each with 16-byte vector accesses; every reduction has
+// a fixed order (lane-strided partials, then a butterfly), so results do not depend
+// on scheduling and a streamed run repeats a resident one bit for bit.
+#pragma once
+#include "common.cuh"
+
+namespace ls {
+
+// ------------------------------------------------------------------ RMSNorm
+// y = bf16(w * bf16(x * rstd)), rstd = 1 / sqrt(mean(x^2) + eps)   (x bf16 [T, H])
+__global__ void rmsnorm_fwd_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
+                                   __nv_bfloat16* __restrict__ y, float* __restrict__ rstd, int T, int H,
+                                   float eps) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * H);
+  const int nv = H >> 3;
+  float ss = 0.f;
+  for (int v = lane; v < nv; v += 32) {
+    const uint4 p = xr[v];
+    const uint32_t q[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = bf16lo(q[e]), b = bf16hi(q[e]);
+      ss += a * a;
+      ss += b * b;
+    }
+  }
+  ss = warp_sum(ss);
+  const float r = 1.0f / sqrtf(ss / (float)H + eps);
+  if (lane == 0 && rstd) rstd[row] = r;
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * H);
+  for (int v = lane; v < nv; v += 32) {
+    const uint4 p = xr[v], wv = wr[v];
+    const uint32_t q[4] = {p.x, p.y, p.z, p.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float n0 = __bfloat162float(__float2bfloat16_rn(bf16lo(q[e]) * r));
+      const float n1 = __bfloat162float(__float2bfloat16_rn(bf16hi(q[e]) * r));
+      o[e] = pack_bf16x2(bf16lo(ww[e]) * n0, bf16hi(ww[e]) * n1);
+    }
+    yr[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// dx += rstd * (g - n * mean(g * n)),  g = dy * w,  n = x * rstd.   dx fp32, and an
+// optional bf16 copy of the updated dx (the next matrix product's input).
+__global__ void rmsnorm_bwd_kernel(const float* __restrict__ dy, const __nv_bfloat16* __restrict__ x,
+                                   const float* __restrict__ rstd, const __nv_bfloat16* __restrict__ w,
+                                   float* __restrict__ dx, __nv_bfloat16* __restrict__ dx_bf16, int T, int H,
+                                   int accumulate) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;
+  const float r = rstd[row];
+  const int nv = H >> 2;
+  const float4* dyr = reinterpret_cast<const float4*>(dy + (size_t)row * H);
+  const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)row * H);
+  const uint2* wr = reinterpret_cast<const uint2*>(w);
+  float dot = 0.f;
+  for (int v = lane; v < nv; v += 32) {
+    const float4 d = dyr[v];
+    const uint2 xv = xr[v], wv = wr[v];
+    dot += d.x * bf16lo(wv.x) * (bf16lo(xv.x) * r);
+    dot += d.y * bf16hi(wv.x) * (bf16hi(xv.x) * r);
+    dot += d.z * bf16lo(wv.y) * (bf16lo(xv.y) * r);
+    dot += d.w * bf16hi(wv.y) * (bf16hi(xv.y) * r);
+  }
+  dot = warp_sum(dot);
+  const float c = dot / (float)H;
+  float4* dxr = reinterpret_cast<float4*>(dx + (size_t)row * H);
+  uint2* db = dx_bf16 ? reinterpret_cast<uint2*>(dx_bf16 + (size_t)row * H) : nullptr;
+  for (int v = lane; v < nv; v += 32) {
+    const float4 d = dyr[v];
+    const uint2 xv = xr[v], wv = wr[v];
+    float4 o = accumulate ? dxr[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+    o.x += r * (d.x * bf16lo(wv.x) - bf16lo(xv.x) * r * c);
+    o.y += r * (d.y * bf16hi(wv.x) - bf16hi(xv.x) * r * c);
+    o.z += r * (d.z * bf16lo(wv.y) - bf16lo(xv.y) * r * c);
+    o.w += r * (d.w * bf16hi(wv.y) - bf16hi(xv.y) * r * c);
+    dxr[v] = o;
+    if (db) db[v] = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+  }
+}
+
+// ------------------------------------------------------------------ RoPE
+// In place on the q and k heads of qkv [T, ld] (bf16): pair (i, i + hd/2) turned by
+// the angle pos * theta^(-2i/hd); cos/sin come from a [max_pos, hd/2] fp32 table.
+__global__ void rope_fwd_kernel(__nv_bfloat16* __restrict__ qkv, long long ld, const int* __restrict__ pos,
+                                const float* __restrict__ cs, const float* __restrict__ sn, int T, int nheads,
+                                int hd) {
+  const int half = hd >> 1;
+  const long long total = (long long)T * nheads * half;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int i = (int)(idx % half);
+    const long long th = idx / half;
+    const int h = (int)(th % nheads);
+    const int t = (int)(th / nheads);
+    __nv_bfloat16* p = qkv + (size_t)t * ld + (size_t)h * hd;
+    const int ps = pos[t];
+    const float c = cs[(size_t)ps * half + i], s = sn[(size_t)ps * half + i];
+    const float x1 = bf2f(p[i]), x2 = bf2f(p[i + half]);
+    p[i] = __float2bfloat16_rn(x1 * c - x2 * s);
+    p[i + half] = __float2bfloat16_rn(x2 * c + x1 * s);
+  }
+}
+
+// Backward of RoPE (rotation by -angle) on the q and k columns of an fp32 gradient,
+// written as bf16 together with the untouched v columns: dqkv = bf16(R^T dqkv_f).
+__global__ void rope_bwd_cast_kernel(const float* __restrict__ g, __nv_bfloat16* __restrict__ out, long long ld,
+                                     const int* __restrict__ pos, const float* __restrict__ cs,
+                                     const float* __restrict__ sn, int T, int nrot_heads, int hd, int ncols) {
+  const int half = hd >> 1;
+  const int rot_cols = nrot_heads * hd;
+  const long long total = (long long)T * ncols;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int col = (int)(idx % ncols);
+    const int t = (int)(idx / ncols);
+    const float* gr = g + (size_t)t * ld;
+    float v;
+    if (col < rot_cols) {
+      const int i = col % hd, base = col - i;
+      const int ii = i < half ? i : i - half;
+      const int ps = pos[t];
+      const float c = cs[(size_t)ps * half + ii], s = sn[(size_t)ps * half + ii];
+      const float y1 = gr[base + ii], y2 = gr[base + ii + half];
+      v = i < half ? (y1 * c + y2 * s) : (y2 * c - y1 * s);
+    } else {
+      v = gr[col];
+    }
+    out[(size_t)t * ld + col] = __float2bfloat16_rn(v);
+  }
+}
+
+// ------------------------------------------------------------------ SwiGLU
+// gu [T, 2I] = [gate | up] (bf16)  ->  h [T, I] = bf16(silu(gate) * up)
+__global__ void swiglu_fwd_kernel(const __nv_bfloat16* __restrict__ gu, __nv_bfloat16* __restrict__ h, int T,
+                                  int I) {
+  const long long n8 = (long long)T * (I >> 3);
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n8;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / (I >> 3)), c = (int)(idx % (I >> 3));
+    const uint4 gv = reinterpret_cast<const uint4*>(gu + (size_t)t * 2 * I)[c];
+    const uint4 uv = reinterpret_cast<const uint4*>(gu + (size_t)t * 2 * I + I)[c];
+    const uint32_t ga[4] = {gv.x, gv.y, gv.z, gv.w}, ua[4] = {uv.x, uv.y, uv.z, uv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float g0 = bf16lo(ga[e]), g1 = bf16hi(ga[e]);
+      const float s0 = g0 / (1.f + __expf(-g0)), s1 = g1 / (1.f + __expf(-g1));
+      o[e] = pack_bf16x2(s0 * bf16lo(ua[e]), s1 * bf16hi(ua[e]));
+    }
+    reinterpret_cast<uint4*>(h + (size_t)t * I)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// dh fp32 [T, I]  ->  dgu [T, 2I] bf16:  d gate = dh * up * silu'(gate),  d up = dh * silu(gate)
+__global__ void swiglu_bwd_kernel(const float* __restrict__ dh, const __nv_bfloat16* __restrict__ gu,
+                                  __nv_bfloat16* __restrict__ dgu, int T, int I) {
+  const long long n4 = (long long)T * (I >> 2);
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n4;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / (I >> 2)), c = (int)(idx % (I >> 2));
+    const float4 d = reinterpret_cast<const float4*>(dh + (size_t)t * I)[c];
+    const uint2 gv = reinterpret_cast<const uint2*>(gu + (size_t)t * 2 * I)[c];
+    const uint2 uv = reinterpret_cast<const uint2*>(gu + (size_t)t * 2 * I + I)[c];
+    const float dd[4] = {d.x, d.y, d.z, d.w};
+    const float g[4] = {bf16lo(gv.x), bf16hi(gv.x), bf16lo(gv.y), bf16hi(gv.y)};
+    const float u[4] = {bf16lo(uv.x), bf16hi(uv.x), bf16lo(uv.y), bf16hi(uv.y)};
+    float dg[4], du[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float sg = 1.f / (1.f + __expf(-g[e]));
+      const float silu = g[e] * sg;
+      dg[e] = dd[e] * u[e] * (sg * (1.f + g[e] * (1.f - sg)));
+      du[e] = dd[e] * silu;
+    }
+    reinterpret_cast<uint2*>(dgu + (size_t)t * 2 * I)[c] = make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
+    reinterpret_cast<uint2*>(dgu + (size_t)t * 2 * I + I)[c] = make_uint2(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]));
+  }
+}
+
+// ------------------------------------------------------------------ embedding
+// x[t] = dequant(row tokens[t] of the NF4 embedding); packed/absmax may live in
+// mapped pinned host memory (only the T selected rows cross the host link).
+__global__ void embed_gather_kernel(const int* __restrict__ tokens, const uint8_t* __restrict__ packed,
+                                    const float* __restrict__ absmax, __nv_bfloat16* __restrict__ x, int T,
+                                    int H) {
+  const int nch = H >> 3;   // 8-element chunks per row
+  const long long total = (long long)T * nch;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / nch), c = (int)(idx % nch);
+    const long long tok = tokens[t];
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(packed + tok * (H >> 1) + c * 4);
+    const float a = absmax[tok * (H >> 6) + (c >> 3)];
+    uint32_t o[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      o[b] = pack_bf16x2(kNF4Table[(w >> (8 * b + 4)) & 15] * a, kNF4Table[(w >> (8 * b)) & 15] * a);
+    reinterpret_cast<uint4*>(x + (size_t)t * H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Plain NF4 dequantisation of a whole matrix (rows x cols) to bf16.
+__global__ void nf4_dequant_kernel(const uint8_t* __restrict__ packed, const float* __restrict__ absmax,
+                                   __nv_bfloat16* __restrict__ out, long long rows, int cols) {
+  const int nch = cols >> 3;
+  const long long total = rows * nch;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long r = idx / nch;
+    const int c = (int)(idx % nch);
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(packed + r * (cols >> 1) + c * 4);
+    const float a = absmax[r * (cols >> 6) + (c >> 3)];
+    uint32_t o[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      o[b] = pack_bf16x2(kNF4Table[(w >> (8 * b + 4)) & 15] * a, kNF4Table[(w >> (8 * b)) & 15] * a);
+    reinterpret_cast<uint4*>(out + r * cols)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ------------------------------------------------------------------ sequences
+// Per position: position within its sequence, next-token target (-1 at a sequence's
+// last position), and the loss coefficient seq_coef[seq] * mask (when given).
+__global__ void seq_setup_kernel(const int* __restrict__ tokens, const int* __restrict__ cu, int nseq,
+                                 const uint8_t* __restrict__ mask, const float* __restrict__ seq_coef,
+                                 int* __restrict__ pos, int* __restrict__ tgt, float* __restrict__ coef, int T) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  int s = 0;
+  while (s + 1 < nseq && cu[s + 1] <= t) ++s;
+  const int a = cu[s], b = cu[s + 1];
+  if (pos) pos[t] = t - a;
+  if (tgt) tgt[t] = (t + 1 < b) ? tokens[t + 1] : -1;
+  if (coef) coef[t] = (seq_coef && mask && mask[t] && t + 1 < b) ? seq_coef[s] : 0.f;
+}
+
+// lse[t] = log sum_v exp(logit) from per-column-group (max, sum-exp) partials, in
+// partial order; lp[t] = logit[t, target] - lse[t] (0 without a target).
+__global__ void logprob_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum, int P,
+                                       int ld, const float* __restrict__ tgt_logit, const int* __restrict__ tgt,
+                                       float* __restrict__ lse, float* __restrict__ lp, int T) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;
+  const float* pm = pmax + (size_t)row * ld;
+  const float* ps = psum + (size_t)row * ld;
+  float m = -INFINITY;
+  for (int p = lane; p < P; p += 32) m = fmaxf(m, pm[p]);
+  m = warp_max(m);
+  float s = 0.f;
+  for (int p = lane; p < P; p += 32) s += ps[p] * __expf(pm[p] - m);
+  s = warp_sum(s);
+  if (lane == 0) {
+    const float l = m + logf(s);
+    lse[row] = l;
+    lp[row] = tgt[row] >= 0 ? tgt_logit[row] - l : 0.f;
+  }
+}
+
+// sums[s] = sum over positions t of sequence s of mask[t] * lp[t] (one block per sequence)
+__global__ void seq_sum_kernel(const float* __restrict__ lp, const uint8_t* __restrict__ mask,
+                               const int* __restrict__ cu, float* __restrict__ sums) {
+  const int s = blockIdx.x;
+  const int a = cu[s], b = cu[s + 1];
+  float acc = 0.f;
+  for (int t = a + threadIdx.x; t < b; t += blockDim.x) acc += mask[t] ? lp[t] : 0.f;
+  __shared__ float red[32];
+  acc = warp_sum(acc);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) sums[s] = v;
+  }
+}
+
+// DPO: z_p = beta ((pi_c - ref_c) - (pi_r - ref_r)), loss = mean_p softplus(-z_p);
+// coeffs = dL/d(sequence logprob sum): chosen -beta sigma(-z)/P, rejected +beta sigma(-z)/P.
+__global__ void dpo_loss_kernel(const float* __restrict__ pi, const float* __restrict__ ref, int npairs,
+                                float beta, float* __restrict__ loss, float* __restrict__ coeffs) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  float acc = 0.f;
+  for (int p = 0; p < npairs; ++p) {
+    const float z = beta * ((pi[2 * p] - ref[2 * p]) - (pi[2 * p + 1] - ref[2 * p + 1]));
+    const float nz = -z;
+    acc += fmaxf(nz, 0.f) + log1pf(__expf(-fabsf(nz)));   // softplus(-z), stable
+    const float sig = 1.f / (1.f + __expf(z));            // sigma(-z)
+    if (coeffs) {
+      coeffs[2 * p] = -beta * sig / (float)npairs;
+      coeffs[2 * p + 1] = beta * sig / (float)npairs;
+    }
+  }
+  if (loss) *loss = acc / (float)npairs;
+}
+
+// ------------------------------------------------------------------ LoRA pieces
+// u_ext [T, 64] bf16 = [bf16(s x A_q^T) | bf16(s x A_v^T) | 0]; A [r, K] bf16, r <= 16.
+// One warp per row; each lane takes 8 contiguous K values per step.
+__global__ void lora_down_kernel(const __nv_bfloat16* __restrict__ x, long long ldx, const __nv_bfloat16* __restrict__ a0,
+                                 const __nv_bfloat16* __restrict__ a1, int r, int K, float s,
+                                 __nv_bfloat16* __restrict__ u_ext, int T) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;
+  float acc[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * ldx);
+  for (int v = lane; v < (K >> 3); v += 32) {
+    const uint4 xv = xr[v];
+    const float xf[8] = {bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y),
+                         bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w)};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int jj = j & 15;
+      const __nv_bfloat16* A = j < 16 ? a0 : a1;
+      if (jj < r && A) {
+        const uint4 av = reinterpret_cast<const uint4*>(A + (size_t)jj * K)[v];
+        acc[j] += xf[0] * bf16lo(av.x) + xf[1] * bf16hi(av.x) + xf[2] * bf16lo(av.y) + xf[3] * bf16hi(av.y) +
+                  xf[4] * bf16lo(av.z) + xf[5] * bf16hi(av.z) + xf[6] * bf16lo(av.w) + xf[7] * bf16hi(av.w);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) acc[j] = warp_sum(acc[j]);
+  // lane j writes column j (0..31); lanes write zeros for columns 32..63
+  float mine = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (lane == j) mine = acc[j];
+  __nv_bfloat16* ur = u_ext + (size_t)row * 64;
+  ur[lane] = __float2bfloat16_rn(s * mine);
+  ur[32 + lane] = __float2bfloat16_rn(0.f);
+}
+
+// du [T, 32] fp32 = s * [dY_q B_q | dY_v B_v] and its bf16 copy in du_ext [T, 64]
+// (columns 32..63 zero).  dY columns are read from the gradient matrix at the given
+// column offsets; B [N, r] bf16.
+__global__ void lora_du_kernel(const __nv_bfloat16* __restrict__ dy, long long ldy, int col_q, int nq,
+                               const __nv_bfloat16* __restrict__ bq, int col_v, int nv,
+                               const __nv_bfloat16* __restrict__ bv, int r, float s, float* __restrict__ du,
+                               __nv_bfloat16* __restrict__ du_ext, int T) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;
+  float acc[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+  for (int side = 0; side < 2; ++side) {
+    const __nv_bfloat16* B = side == 0 ? bq : bv;
+    if (!B) continue;
+    const int n = side == 0 ? nq : nv;
+    const __nv_bfloat16* dr = dy + (size_t)row * ldy + (side == 0 ? col_q : col_v);
+    for (int c = lane; c < n; c += 32) {
+      const float d = bf2f(dr[c]);
+      const __nv_bfloat16* br = B + (size_t)c * r;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < r) acc[side * 16 + j] += d * bf2f(br[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) acc[j] = warp_sum(acc[j]);
+  float mine = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (lane == j) mine = acc[j];
+  du[(size_t)row * 32 + lane] = s * mine;
+  du_ext[(size_t)row * 64 + lane] = __float2bfloat16_rn(s * mine);
+  du_ext[(size_t)row * 64 + 32 + lane] = __float2bfloat16_rn(0.f);
+}
+
+// Partial outer products over a slice of rows:
+//   part[chunk][c][j] = sum_{t in chunk} X[t, c] * U[t, j]     (c < ncols, j < 16)
+// X bf16 [T, ldx]; U given as fp32 [T, ldu] or bf16 [T, ldu].  One thread per column c.
+__global__ void lora_outer_partial_kernel(const __nv_bfloat16* __restrict__ X, long long ldx, int ncols,
+                                          const float* __restrict__ Uf, const __nv_bfloat16* __restrict__ Ub,
+                                          int ldu, int T, int rows_per_chunk, float* __restrict__ part) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int chunk = blockIdx.y;
+  const int t0 = chunk * rows_per_chunk, t1 = min(T, t0 + rows_per_chunk);
+  __shared__ float su[64][16];
+  float acc[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+  for (int tb = t0; tb < t1; tb += 64) {
+    const int nt = min(64, t1 - tb);
+    __syncthreads();
+    for (int e = threadIdx.x; e < 64 * 16; e += blockDim.x) {
+      const int tt = e >> 4, j = e & 15;
+      float v = 0.f;
+      if (tt < nt) v = Uf ? Uf[(size_t)(tb + tt) * ldu + j] : bf2f(Ub[(size_t)(tb + tt) * ldu + j]);
+      su[tt][j] = v;
+    }
+    __syncthreads();
+    if (c < ncols) {
+      for (int tt = 0; tt < nt; ++tt) {
+        const float xv = bf2f(X[(size_t)(tb + tt) * ldx + c]);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] += xv * su[tt][j];
+      }
+    }
+  }
+  if (c < ncols) {
+    float* pp = part + ((size_t)chunk * ncols + c) * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) pp[j] = acc[j];
+  }
+}
+
+// out (+)= sum over chunks, in chunk order.  layout 0: out[c * r + j] (B-shaped [ncols, r]);
+// layout 1: out[j * ncols + c] (A-shaped [r, ncols]).
+__global__ void lora_outer_reduce_kernel(const float* __restrict__ part, int nchunks, int ncols, int r,
+                                         int layout, int accumulate, float* __restrict__ out) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= ncols * r) return;
+  const int c = layout == 0 ? e / r : e % ncols;
+  const int j = layout == 0 ? e % r : e / ncols;
+  float s = 0.f;
+  for (int k = 0; k < nchunks; ++k) s += part[((size_t)k * ncols + c) * 16 + j];
+  out[e] = accumulate ? out[e] + s : s;
+}
+
+// B_ext [N, 64] for the forward extra stage: rows of B_q in columns 0..r-1 for the
+// q rows, rows of B_v in columns 16..16+r-1 for the v rows, zero elsewhere.
+__global__ void build_ext_fwd_kernel(const __nv_bfloat16* __restrict__ bq, int q0, int nq,
+                                     const __nv_bfloat16* __restrict__ bv, int v0, int nv, int r, int N,
+                                     __nv_bfloat16* __restrict__ ext) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= N * 64) return;
+  const int n = e >> 6, c = e & 63;
+  float v = 0.f;
+  if (bq && c < 16 && c < r && n >= q0 && n < q0 + nq) v = bf2f(bq[(size_t)(n - q0) * r + c]);
+  if (bv && c >= 16 && c < 16 + r && n >= v0 && n < v0 + nv) v = bf2f(bv[(size_t)(n - v0) * r + (c - 16)]);
+  ext[e] = __float2bfloat16_rn(v);
+}
+
+// A_ext [K, 64] for the backward extra stage: row k = [A_q[:, k] | A_v[:, k] | 0].
+__global__ void build_ext_bwd_kernel(const __nv_bfloat16* __restrict__ aq, const __nv_bfloat16* __restrict__ av,
+                                     int r, int K, __nv_bfloat16* __restrict__ ext) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= K * 64) return;
+  const int k = e >> 6, c = e & 63;
+  float v = 0.f;
+  if (aq && c < r) v = bf2f(aq[(size_t)c * K + k]);
+  if (av && c >= 16 && c < 16 + r) v = bf2f(av[(size_t)(c - 16) * K + k]);
+  ext[e] = __float2bfloat16_rn(v);
+}
+
+__global__ void cast_f32_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    out[i] = __float2bfloat16_rn(in[i]);
+}
+
+}  // namespace ls

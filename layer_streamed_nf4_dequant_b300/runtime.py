@@ -1,0 +1,271 @@
+"""Host-side plumbing around libls: pinned layer images, workspace, adapters, steps.
+
+PyTorch supplies device memory, pinned host memory and streams; every step of the
+computation runs inside libls.so.  The frozen base is held in pinned host RAM in
+the library's slot layout (one buffer per layer, so each layer read is one
+host-to-device copy), as the layer-streaming design on the Soup pages prescribes
+("The Core Idea: Layer Streaming", Soup: Fine-Tune an 8B Model on a 4 GB GPU).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from concurrent.futures import ThreadPoolExecutor
+from typing import Dict, List, Optional
+
+import numpy as np
+import torch
+
+from ._binding import (LSError, call, check, last_error, lib, ls_config, ls_layer_host, ls_nf4_host, ls_stats_t,
+                       ls_vocab_host)
+
+MATS = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+def make_config(s, max_tokens: int = 0, max_seqs: int = 0, max_seq_len: int = 0, resident: bool = False,
+                cap_bytes: Optional[int] = None, vocab_chunk_rows: int = 0) -> ls_config:
+    """ls_config from a stack shape (anything with the synth.StackConfig fields)."""
+    c = ls_config()
+    c.layers, c.hidden, c.heads, c.kv_heads, c.head_dim = s.layers, s.hidden, s.heads, s.kv_heads, s.head_dim
+    c.inter, c.vocab, c.tied, c.lora_r = s.inter, s.vocab, int(s.tied), s.lora_r
+    c.lora_scale, c.rope_theta, c.eps = s.lora_alpha / s.lora_r, s.rope_theta, s.eps
+    c.max_tokens = max_tokens or s.seq_len * s.nseq
+    c.max_seqs = max_seqs or s.nseq
+    c.max_seq_len = max_seq_len or s.seq_len
+    c.vocab_chunk_rows = vocab_chunk_rows
+    c.resident = int(resident)
+    c.cap_bytes = s.cap_bytes if cap_bytes is None else cap_bytes
+    return c
+
+
+def plan_bytes(cfg: ls_config) -> int:
+    n = C.c_uint64(0)
+    check(lib().ls_plan(C.byref(cfg), C.byref(n)))
+    return n.value
+
+
+def layer_layout(cfg: ls_config):
+    offs = (C.c_uint64 * 16)()
+    nb = C.c_uint64(0)
+    check(lib().ls_layer_layout(C.byref(cfg), offs, C.byref(nb)))
+    return [int(o) for o in offs], nb.value
+
+
+def quantize_host(w: np.ndarray, packed: Optional[np.ndarray] = None, absmax: Optional[np.ndarray] = None,
+                  nthreads: int = 0):
+    """NF4-quantise fp32 W [N, K] with the library's host quantiser."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    if packed is None:
+        packed = np.empty((n, k // 2), np.uint8)
+    if absmax is None:
+        absmax = np.empty((n, k // 64), np.float32)
+    check(lib().nf4_quantize(w.ctypes.data, n, k, packed.ctypes.data, absmax.ctypes.data, nthreads))
+    return packed, absmax
+
+
+def _pinned(nbytes: int) -> torch.Tensor:
+    return torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+
+
+class Stack:
+    """A libls context for one stack shape, with its pinned base, adapters and buffers."""
+
+    def __init__(self, s, max_tokens: int = 0, max_seqs: int = 0, max_seq_len: int = 0, resident: bool = False,
+                 cap_bytes: Optional[int] = None, vocab_chunk_rows: int = 0, device: str = "cuda:0"):
+        self.s = s
+        self.dev = torch.device(device)
+        self.cfg = make_config(s, max_tokens, max_seqs, max_seq_len, resident, cap_bytes, vocab_chunk_rows)
+        self.ws_bytes = plan_bytes(self.cfg)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
+        self.compute = torch.cuda.Stream(self.dev)
+        self.copy = torch.cuda.Stream(self.dev)
+        h = C.c_void_p()
+        check(lib().ls_create(C.byref(self.cfg), self.ws.data_ptr(), self.ws_bytes, self.compute.cuda_stream,
+                              self.copy.cuda_stream, C.byref(h)))
+        self.ctx = h.value
+        self.offs, self.img_bytes = layer_layout(self.cfg)
+        self.images: List[torch.Tensor] = []
+        self.vocab_bufs: Dict[str, torch.Tensor] = {}
+        self.adapters: List[Dict[str, torch.Tensor]] = []
+        self._keep = []
+
+    # ------------------------------------------------------------------ loading
+    def _shape(self, name):
+        s = self.s
+        H, I, nq, nkv = s.hidden, s.inter, s.heads * s.head_dim, s.kv_heads * s.head_dim
+        return {"q": (nq, H), "k": (nkv, H), "v": (nkv, H), "o": (H, nq), "gate": (I, H), "up": (I, H),
+                "down": (H, I)}[name]
+
+    def load_layer_arrays(self, layer: int, weights: Dict[str, np.ndarray], attn_norm: np.ndarray,
+                          mlp_norm: np.ndarray, nthreads: int = 0):
+        """Quantise fp32 weights into a pinned image in slot layout and register it."""
+        img = _pinned(self.img_bytes)
+        buf = img.numpy()
+        for m, name in enumerate(MATS):
+            n, k = self._shape(name)
+            pk = buf[self.offs[m]: self.offs[m] + n * k // 2].reshape(n, k // 2)
+            am = buf[self.offs[7 + m]: self.offs[7 + m] + n * (k // 64) * 4].view(np.float32).reshape(n, k // 64)
+            quantize_host(weights[name], pk, am, nthreads)
+        H = self.s.hidden
+        buf[self.offs[14]: self.offs[14] + 2 * H] = _bf16_bytes(attn_norm)
+        buf[self.offs[15]: self.offs[15] + 2 * H] = _bf16_bytes(mlp_norm)
+        self._register_layer(layer, img)
+
+    def _register_layer(self, layer: int, img: torch.Tensor):
+        base = img.data_ptr()
+        lh = ls_layer_host()
+        for m, name in enumerate(MATS):
+            setattr(lh, name, ls_nf4_host(base + self.offs[m], base + self.offs[7 + m]))
+        lh.attn_norm = base + self.offs[14]
+        lh.mlp_norm = base + self.offs[15]
+        check(lib().load_layer_nf4(self.ctx, layer, C.byref(lh)), self.ctx)
+        while len(self.images) <= layer:
+            self.images.append(None)
+        self.images[layer] = img
+
+    def load_vocab_arrays(self, embed: np.ndarray, lm_head: Optional[np.ndarray], final_norm: np.ndarray,
+                          nthreads: int = 0):
+        V, H = embed.shape
+        ep = _pinned(V * H // 2)
+        ea = _pinned(V * (H // 64) * 4)
+        quantize_host(embed, ep.numpy().reshape(V, H // 2), ea.numpy().view(np.float32).reshape(V, H // 64), nthreads)
+        self.vocab_bufs = {"ep": ep, "ea": ea}
+        vh = ls_vocab_host()
+        vh.embed = ls_nf4_host(ep.data_ptr(), ea.data_ptr())
+        if not self.s.tied:
+            hp = _pinned(V * H // 2)
+            ha = _pinned(V * (H // 64) * 4)
+            quantize_host(lm_head, hp.numpy().reshape(V, H // 2), ha.numpy().view(np.float32).reshape(V, H // 64),
+                          nthreads)
+            self.vocab_bufs.update(hp=hp, ha=ha)
+            vh.lm_head = ls_nf4_host(hp.data_ptr(), ha.data_ptr())
+        fn = _pinned(2 * H)
+        fn.numpy()[:] = _bf16_bytes(final_norm)
+        self.vocab_bufs["fn"] = fn
+        vh.final_norm = fn.data_ptr()
+        check(lib().load_vocab_nf4(self.ctx, C.byref(vh)), self.ctx)
+
+    def load_synthetic(self, synth, seed: int = 0, workers: int = 0):
+        """Draw the base from the shared seeded generators and load it (threads over layers)."""
+        s = self.s
+        workers = workers or min(16, os.cpu_count() or 1)
+
+        def one(layer):
+            w = {n: synth.weight(s, layer, n, seed) for n in MATS}
+            self.load_layer_arrays(layer, w, synth.norm_weight(s, layer, 0, seed),
+                                   synth.norm_weight(s, layer, 1, seed), nthreads=1)
+
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, range(s.layers)))
+        emb = synth.weight(s, -1, "embed", seed)
+        head = None if s.tied else synth.weight(s, -1, "lm_head", seed)
+        self.load_vocab_arrays(emb, head, synth.norm_weight(s, -1, 0, seed))
+
+    # ------------------------------------------------------------------ adapters
+    def set_adapter(self, layer: int, aq, bq, av, bv):
+        """Bind bf16 device LoRA factors (A [r,H], B [N,r]); fp32 grads are allocated here."""
+        d = {"aq": aq, "bq": bq, "av": av, "bv": bv}
+        for k in list(d):
+            d["g" + k] = torch.zeros(d[k].shape, dtype=torch.float32, device=self.dev)
+        check(lib().ls_set_adapter(self.ctx, layer, aq.data_ptr(), bq.data_ptr(), av.data_ptr(), bv.data_ptr(),
+                                   d["gaq"].data_ptr(), d["gbq"].data_ptr(), d["gav"].data_ptr(),
+                                   d["gbv"].data_ptr()), self.ctx)
+        while len(self.adapters) <= layer:
+            self.adapters.append(None)
+        self.adapters[layer] = d
+
+    def set_adapters_synthetic(self, synth, seed: int = 0, zero_b: bool = False):
+        for l in range(self.s.layers):
+            aq, bq = synth.lora_weights(self.s, l, "q", seed, zero_b=zero_b)
+            av, bv = synth.lora_weights(self.s, l, "v", seed, zero_b=zero_b)
+            t = [torch.from_numpy(x).to(torch.bfloat16).to(self.dev) for x in (aq, bq, av, bv)]
+            self.set_adapter(l, *t)
+
+    def grad_numel(self) -> int:
+        s = self.s
+        return s.layers * (2 * s.lora_r * s.hidden + s.lora_r * (s.heads + s.kv_heads) * s.head_dim)
+
+    # ------------------------------------------------------------------ steps
+    def upload_batch(self, tokens: np.ndarray, cu: np.ndarray, mask: np.ndarray):
+        """Device copies of one batch's token ids, sequence offsets and loss mask."""
+        t = torch.from_numpy(np.ascontiguousarray(tokens, np.int32)).to(self.dev)
+        c = torch.from_numpy(np.ascontiguousarray(cu, np.int32)).to(self.dev)
+        m = torch.from_numpy(np.ascontiguousarray(mask, np.uint8)).to(self.dev)
+        return t, c, m
+
+    def fwd(self, tok, cu, mask, adapter_on: bool = True, save: bool = True, sums: Optional[torch.Tensor] = None):
+        nseq = cu.numel() - 1
+        if sums is None:
+            sums = torch.empty(nseq, dtype=torch.float32, device=self.dev)
+        check(lib().stream_step_fwd(self.ctx, tok.data_ptr(), tok.numel(), nseq, cu.data_ptr(), mask.data_ptr(),
+                                    int(adapter_on), int(save), sums.data_ptr()), self.ctx)
+        return sums
+
+    def logprobs(self, T: int):
+        lp = torch.empty(T, dtype=torch.float32, device=self.dev)
+        lse = torch.empty(T, dtype=torch.float32, device=self.dev)
+        check(lib().seq_logprobs(self.ctx, lp.data_ptr(), lse.data_ptr()), self.ctx)
+        return lp, lse
+
+    def bwd(self, coeffs: torch.Tensor):
+        check(lib().stream_step_bwd(self.ctx, coeffs.data_ptr()), self.ctx)
+
+    def dpo_step(self, tok, cu, mask, beta: float, out: Optional[Dict] = None) -> Dict:
+        """Policy pass (adapter on, store kept), reference pass (adapter off), DPO loss, backward."""
+        nseq = cu.numel() - 1
+        o = out if out is not None else {
+            "pi": torch.empty(nseq, dtype=torch.float32, device=self.dev),
+            "ref": torch.empty(nseq, dtype=torch.float32, device=self.dev),
+            "loss": torch.empty(1, dtype=torch.float32, device=self.dev),
+            "coeffs": torch.empty(nseq, dtype=torch.float32, device=self.dev)}
+        self.fwd(tok, cu, mask, True, True, o["pi"])
+        self.fwd(tok, cu, mask, False, False, o["ref"])
+        check(lib().dpo_loss(self.ctx, o["pi"].data_ptr(), o["ref"].data_ptr(), nseq // 2, beta,
+                             o["loss"].data_ptr(), o["coeffs"].data_ptr()), self.ctx)
+        self.bwd(o["coeffs"])
+        return o
+
+    def sft_step(self, tok, cu, mask, count: float, out: Optional[Dict] = None) -> Dict:
+        nseq = cu.numel() - 1
+        o = out if out is not None else {
+            "sums": torch.empty(nseq, dtype=torch.float32, device=self.dev),
+            "loss": torch.empty(1, dtype=torch.float32, device=self.dev),
+            "coeffs": torch.empty(nseq, dtype=torch.float32, device=self.dev)}
+        self.fwd(tok, cu, mask, True, True, o["sums"])
+        check(lib().sft_loss(self.ctx, o["sums"].data_ptr(), nseq, float(count), o["loss"].data_ptr(),
+                             o["coeffs"].data_ptr()), self.ctx)
+        self.bwd(o["coeffs"])
+        return o
+
+    def grads(self, zero_after: bool = False) -> torch.Tensor:
+        flat = torch.empty(self.grad_numel(), dtype=torch.float32, device=self.dev)
+        check(lib().lora_grads(self.ctx, flat.data_ptr(), int(zero_after)), self.ctx)
+        return flat
+
+    def zero_grads(self):
+        check(lib().lora_grads(self.ctx, None, 1), self.ctx)
+
+    def sync(self, timeout_ms: int = 0) -> int:
+        return lib().ls_sync(self.ctx, timeout_ms)
+
+    def stats(self, reset: bool = False) -> Dict:
+        st = ls_stats_t()
+        check(lib().ls_stats(self.ctx, C.byref(st), int(reset)))
+        return st.as_dict()
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            lib().ls_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _bf16_bytes(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16)
+    return t.view(torch.uint8).numpy()

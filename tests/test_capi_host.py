@@ -1,0 +1,88 @@
+"""Host-side checks of the C ABI (no GPU): exports, quantiser, planner, layout."""
+import ctypes as C
+import math
+
+import numpy as np
+import pytest
+
+import layer_streamed_nf4_dequant_b300 as L
+import oracle
+import synth
+
+
+def test_library_exports_every_header_function():
+    lib = L.lib()
+    names = L.header_functions()
+    assert len(names) >= 30
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+@pytest.mark.parametrize("shape", [(3, 64), (17, 256), (64, 896)])
+def test_host_quantizer_bit_exact_vs_oracle(shape):
+    rng = np.random.default_rng(shape[1])
+    w = (rng.standard_normal(shape) * 0.02).astype(np.float32)
+    w[0, :64] = 0.0                                  # zero block
+    w[-1, -64:] = np.tile(oracle.NF4_TABLE, 4) * 3   # exact code points
+    mids = ((oracle.NF4_TABLE[:-1].astype(np.float64) + oracle.NF4_TABLE[1:]) / 2).astype(np.float32)
+    if shape[0] > 1:
+        w[1, :15] = mids
+        w[1, 15] = 1.0
+    pk, am = L.quantize_host(w)
+    codes, absmax = oracle.nf4_quantize(w)
+    np.testing.assert_array_equal(am, absmax)
+    np.testing.assert_array_equal(pk, oracle.nf4_pack(codes))
+
+
+def test_host_quantizer_large_matrix_threads():
+    w = synth.weight(synth.LAYER_896, 0, "gate")    # 4864 x 896
+    pk1, am1 = L.quantize_host(w, nthreads=1)
+    pk8, am8 = L.quantize_host(w, nthreads=8)
+    np.testing.assert_array_equal(pk1, pk8)
+    np.testing.assert_array_equal(am1, am8)
+    codes, absmax = oracle.nf4_quantize(w[:512])
+    np.testing.assert_array_equal(pk1[:512], oracle.nf4_pack(codes))
+
+
+def test_quantizer_rejects_bad_shape():
+    w = np.zeros((2, 65), np.float32)
+    rc = L.lib().nf4_quantize(w.ctypes.data, 2, 65, w.ctypes.data, w.ctypes.data, 1)
+    assert rc == L.LS_ERR_ARG
+
+
+def test_plan_and_preflight_refusal():
+    s32 = synth.QWEN_32B
+    cfg = L.make_config(s32)
+    need = L.plan_bytes(cfg)                     # fits the 4 GiB cap of the 32B workload
+    assert 0 < need <= s32.cap_bytes
+    small = L.make_config(s32, cap_bytes=1 << 30)
+    n = C.c_uint64(0)
+    rc = L.lib().ls_plan(C.byref(small), C.byref(n))
+    assert rc == L.LS_ERR_CAP and n.value == need
+    assert "exceeds the cap" in L.last_error()
+    bad = L.make_config(synth.LLAMA_8B)
+    bad.head_dim = 96
+    assert L.lib().ls_plan(C.byref(bad), C.byref(n)) == L.LS_ERR_ARG
+
+
+def test_layer_layout_sizes():
+    s = synth.LLAMA_8B
+    offs, nbytes = L.layer_layout(L.make_config(s))
+    H, I, nq, nkv = s.hidden, s.inter, s.heads * s.head_dim, s.kv_heads * s.head_dim
+    params = (nq + 2 * nkv) * H + H * nq + 2 * I * H + H * I
+    # packed 0.5 B + absmax 4/64 B per weight, two bf16 norms, 256-byte alignment slack
+    assert abs(nbytes - (params * 0.5625 + 4 * H)) < 16 * 256
+    assert offs == sorted(offs) and offs[0] == 0
+    assert offs[1] - offs[0] == nq * H // 2 and offs[2] - offs[1] == nkv * H // 2
+    assert offs[5] - offs[4] == I * H // 2
+    assert nbytes / 1e6 == pytest.approx(122.7, abs=0.1)
+
+
+def test_rope_table_matches_fp64():
+    maxp, hd, theta = 300, 128, 5e5
+    c = np.empty((maxp, hd // 2), np.float32)
+    s = np.empty_like(c)
+    L.check(L.lib().ls_rope_table(c.ctypes.data, s.ctypes.data, maxp, hd, theta))
+    ang = np.arange(maxp)[:, None] * theta ** (-2.0 * np.arange(hd // 2) / hd)[None, :]
+    np.testing.assert_array_equal(c, np.cos(ang).astype(np.float32))
+    np.testing.assert_array_equal(s, np.sin(ang).astype(np.float32))
