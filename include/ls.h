@@ -197,10 +197,28 @@ typedef struct ls_stats_t {
   uint64_t act_store_bytes;/* activation store                                        */
   int32_t vocab_chunks;
   int32_t vocab_chunk_rows;
+  uint64_t kernel_launches; /* kernels this context enqueued                         */
 } ls_stats_t;
 
 /* Counters since ls_create (or the last reset). */
 int ls_stats(ls_ctx* ctx, ls_stats_t* out, int32_t reset);
+
+/* Kernel classes of the per-launch timing below. */
+enum { LS_K_GEMM_FWD = 0, LS_K_GEMM_DX = 1, LS_K_ATTN_FWD = 2, LS_K_ATTN_BWD = 3, LS_K_OTHER = 4, LS_K_CLASSES = 5 };
+
+typedef struct ls_profile_t {
+  uint64_t launches[LS_K_CLASSES];
+  double ms[LS_K_CLASSES];     /* summed CUDA-event durations on the compute stream       */
+  double flop[LS_K_CLASSES];   /* algorithmic FLOPs (2 M N K per matrix product)          */
+  double bytes[LS_K_CLASSES];  /* algorithmic bytes (operands read once, outputs written) */
+} ls_profile_t;
+
+/* Start (enable = 1, counters reset) or stop (0) timing every kernel this context
+ * launches with a pair of CUDA events on the compute stream (up to 65536 launches). */
+int ls_profile(ls_ctx* ctx, int32_t enable);
+
+/* Wait for the compute stream and total the timed launches by class. */
+int ls_profile_read(ls_ctx* ctx, ls_profile_t* out);
 
 /* Test hook: make every later slot copy on the copy stream first wait host_delay_ms
  * on the host (a host callback), so a bounded ls_sync can be shown to give up.  No

@@ -50,10 +50,22 @@ class ls_vocab_host(C.Structure):
 class ls_stats_t(C.Structure):
     _fields_ = [("layer_reads", C.c_uint64), ("vocab_reads", C.c_uint64), ("h2d_bytes", C.c_uint64),
                 ("slot_reuses", C.c_uint64), ("workspace_bytes", C.c_uint64), ("slot_bytes", C.c_uint64),
-                ("act_store_bytes", C.c_uint64), ("vocab_chunks", C.c_int32), ("vocab_chunk_rows", C.c_int32)]
+                ("act_store_bytes", C.c_uint64), ("vocab_chunks", C.c_int32), ("vocab_chunk_rows", C.c_int32),
+                ("kernel_launches", C.c_uint64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class ls_profile_t(C.Structure):
+    _fields_ = [("launches", C.c_uint64 * 5), ("ms", C.c_double * 5), ("flop", C.c_double * 5),
+                ("bytes", C.c_double * 5)]
+
+    CLASSES = ("gemm_fwd", "gemm_dx", "attn_fwd", "attn_bwd", "other")
+
+    def as_dict(self):
+        return {c: {"launches": int(self.launches[i]), "ms": self.ms[i], "flop": self.flop[i],
+                    "bytes": self.bytes[i]} for i, c in enumerate(self.CLASSES)}
 
 
 P, I32, I64, U64, F32 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_float
@@ -76,6 +88,8 @@ _SIGS = {
     "ls_sync": [P, I32],
     "ls_stats": [P, C.POINTER(ls_stats_t), I32],
     "ls_debug_copy_delay": [P, I32],
+    "ls_profile": [P, I32],
+    "ls_profile_read": [P, C.POINTER(ls_profile_t)],
     "lsk_nf4_dequant": [P, P, I64, I32, P, P],
     "lsk_nf4_gemm": [I32, P, I64, I32, P, P, I32, I32, P, P, I32, I32, P, I64, P, I64, I32, I32, P],
     "lsk_rmsnorm_fwd": [P, P, P, P, I32, I32, F32, P],

@@ -2,7 +2,7 @@
 //
 // Inline-PTX wrappers for mbarrier, TMA (cp.async.bulk.tensor), and the 5th-gen
 // tensor core (tcgen05: TMEM alloc, MMA, commit, TMEM load).  Every spin-wait is
-// bounded: on timeout it raises the device error flag and returns false, so a
+// bounded in time (2 s): on timeout it raises the device error flag and returns false, so a
 // kernel that loses a handshake ends instead of hanging the GPU.
 #pragma once
 #include <cuda.h>
@@ -22,8 +22,15 @@ __device__ int g_device_error = 0;   // one definition: the library is one trans
 
 __device__ __forceinline__ void raise_error(int code) { atomicCAS(&g_device_error, 0, code); }
 
-// About 2^24 polls (well under a minute even at ~1 us each) before a wait gives up.
-constexpr long long kWaitLimit = 1LL << 24;
+// A wait gives up after this much wall-clock time (device %globaltimer, ns).  Real
+// waits in these kernels last microseconds to milliseconds.
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -48,10 +55,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Bounded wait for the phase with the given parity; false (and the error flag) on timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (long long i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  raise_error(DEV_WAIT_TIMEOUT);
-  return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      raise_error(DEV_WAIT_TIMEOUT);
+      return false;
+    }
+  }
 }
 // Arrive on `bar` once all of this thread's earlier cp.async copies have landed.
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {

@@ -155,6 +155,13 @@ struct ls_ctx {
 
   ls_stats_t st{};
   int copy_delay_ms = 0;
+
+  // per-launch CUDA-event timing on the compute stream (ls_profile)
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_ev;
+  std::vector<int> prof_cls;
+  std::vector<double> prof_flop, prof_bytes;
+  size_t prof_used = 0;
 };
 
 namespace {
@@ -179,6 +186,52 @@ int fail(ls_ctx* c, int code, const std::string& m) {
     cudaError_t e_ = cudaGetLastError();                                                      \
     if (e_ != cudaSuccess) return fail(c, LS_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e_)); \
   } while (0)
+
+constexpr size_t kProfMax = 1 << 16;
+
+inline void pbeg(ls_ctx* c) {
+  if (c->prof_on && c->prof_used < kProfMax) cudaEventRecord(c->prof_ev[2 * c->prof_used], c->cs);
+}
+inline void pend(ls_ctx* c, int cls, double flop, double bytes) {
+  c->st.kernel_launches++;
+  if (c->prof_on && c->prof_used < kProfMax) {
+    cudaEventRecord(c->prof_ev[2 * c->prof_used + 1], c->cs);
+    c->prof_cls[c->prof_used] = cls;
+    c->prof_flop[c->prof_used] = flop;
+    c->prof_bytes[c->prof_used] = bytes;
+    ++c->prof_used;
+  }
+}
+
+// Time one enqueue (nk kernels) on the compute stream as class `cls`.
+#define TIMED(cls, flop, bytes, nk, ...)                                                      \
+  do {                                                                                        \
+    pbeg(c);                                                                                  \
+    __VA_ARGS__;                                                                              \
+    cudaError_t e_ = cudaGetLastError();                                                      \
+    if (e_ != cudaSuccess) return fail(c, LS_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e_)); \
+    pend(c, cls, flop, bytes);                                                                \
+    c->st.kernel_launches += (nk) - 1;                                                        \
+  } while (0)
+
+#define GEMM_T(cls, flop, bytes, call)                                                        \
+  do {                                                                                        \
+    pbeg(c);                                                                                  \
+    cudaError_t ge_ = (call);                                                                 \
+    if (ge_ != cudaSuccess) return fail(c, LS_ERR_CUDA, std::string("gemm: ") + cudaGetErrorString(ge_)); \
+    pend(c, cls, flop, bytes);                                                                \
+  } while (0)
+
+// Algorithmic cost of one NF4 matrix product: 2 M N K flops (+ the LoRA stage);
+// bytes = activation read once + NF4 weight (0.5625 B per weight) + output (+ residual).
+inline double gemm_flop(int mode, int M, int Nw, int Kw, int ext_k) {
+  const double Nout = mode == ls::GEMM_FWD ? Nw : Kw;
+  return 2.0 * M * (double)Nw * Kw + 2.0 * M * Nout * ext_k;
+}
+inline double gemm_bytes(int mode, int M, int Nw, int Kw, int out_bytes, bool residual) {
+  const double Nout = mode == ls::GEMM_FWD ? Nw : Kw, Kred = mode == ls::GEMM_FWD ? Kw : Nw;
+  return 2.0 * M * Kred + 0.5625 * (double)Nw * Kw + (double)M * Nout * (out_bytes + (residual ? 2 : 0));
+}
 
 int check_cfg(const ls_config* cfg, std::string& why) {
   if (!cfg) { why = "null config"; return LS_ERR_ARG; }
@@ -605,47 +658,60 @@ LayerW layer_ptrs(const ls_ctx* c, uint8_t* img) {
   return w;
 }
 
+inline double attn_flop(const ls_ctx* c, int T, int nseq) {
+  const double Ls = (double)T / nseq;   // host view: equal sequence lengths
+  return 4.0 * c->hd * c->nh * nseq * Ls * (Ls + 1) / 2;
+}
+
 // Forward of one decoder layer up to (recompute == true) the MLP input projections,
 // or to the layer output x_out.
 int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16* x_out, int T, int nseq,
                   const int32_t* cu, bool adapter, bool recompute) {
   cudaStream_t st = c->cs;
-  const int H = c->H;
-  ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(x_in, w.w1, c->n1, c->rstd1, T, H, c->cfg.eps);
-  CKL();
+  const int H = c->H, I = c->I;
+  const double TH = (double)T * H;
+  TIMED(LS_K_OTHER, 0, 4 * TH, 1,
+        ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(x_in, w.w1, c->n1, c->rstd1, T, H, c->cfg.eps));
   const ls_ctx::Ad& a = c->ad[layer];
   const bool use = adapter && a.on;
   if (use) {
-    ls::lora_down_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->n1, H, a.aq, a.av, c->r, H, c->cfg.lora_scale, c->u_ext, T);
-    CKL();
+    TIMED(LS_K_OTHER, 2.0 * T * 2 * c->r * H, 2 * TH, 1,
+          ls::lora_down_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->n1, H, a.aq, a.av, c->r, H, c->cfg.lora_scale,
+                                                            c->u_ext, T));
     const int n = c->nqkv * 64;
-    ls::build_ext_fwd_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.bq, 0, c->nq, a.bv, c->nq + c->nkvd, c->nkvd, c->r,
-                                                              c->nqkv, c->ext_fwd);
-    CKL();
+    TIMED(LS_K_OTHER, 0, 2.0 * n, 1,
+          ls::build_ext_fwd_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.bq, 0, c->nq, a.bv, c->nq + c->nkvd, c->nkvd,
+                                                                    c->r, c->nqkv, c->ext_fwd));
   }
-  CK(gemm(ls::GEMM_FWD, c->n1, H, T, w.pqkv, w.aqkv, c->nqkv, H, c->u_ext, c->ext_fwd, use ? 32 : 0, ls::EPI_BF16,
-          c->qkv, c->nqkv, nullptr, 0, st));
+  const int ek = use ? 32 : 0;
+  GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, c->nqkv, H, ek), gemm_bytes(0, T, c->nqkv, H, 2, false),
+         gemm(ls::GEMM_FWD, c->n1, H, T, w.pqkv, w.aqkv, c->nqkv, H, c->u_ext, c->ext_fwd, ek, ls::EPI_BF16, c->qkv,
+              c->nqkv, nullptr, 0, st));
   {
     const long long n = (long long)T * (c->nh + c->nkv) * (c->hd / 2);
-    ls::rope_fwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->qkv, c->nqkv, c->pos, c->rope_cos, c->rope_sin, T,
-                                                       c->nh + c->nkv, c->hd);
-    CKL();
+    TIMED(LS_K_OTHER, 0, 4.0 * n * 2, 1,
+          ls::rope_fwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->qkv, c->nqkv, c->pos, c->rope_cos, c->rope_sin, T,
+                                                              c->nh + c->nkv, c->hd));
   }
-  CK(attn_fwd(c->hd, c->qkv, c->nqkv, cu, nseq, c->maxlen, c->nh, c->nkv, c->attn_o, c->nq, c->lse_attn, T, st));
-  CK(gemm(ls::GEMM_FWD, c->attn_o, c->nq, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->x1, H, x_in,
-          H, st));
-  ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->x1, w.w2, c->n2, c->rstd2, T, H, c->cfg.eps);
-  CKL();
-  CK(gemm(ls::GEMM_FWD, c->n2, H, T, w.pgu, w.agu, 2 * c->I, H, nullptr, nullptr, 0, ls::EPI_BF16, c->gu, 2 * c->I,
-          nullptr, 0, st));
+  GEMM_T(LS_K_ATTN_FWD, attn_flop(c, T, nseq), 2.0 * T * (c->nqkv + c->nq),
+         attn_fwd(c->hd, c->qkv, c->nqkv, cu, nseq, c->maxlen, c->nh, c->nkv, c->attn_o, c->nq, c->lse_attn, T, st));
+  GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, H, c->nq, 0), gemm_bytes(0, T, H, c->nq, 2, true),
+         gemm(ls::GEMM_FWD, c->attn_o, c->nq, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->x1, H,
+              x_in, H, st));
+  TIMED(LS_K_OTHER, 0, 4 * TH, 1,
+        ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->x1, w.w2, c->n2, c->rstd2, T, H, c->cfg.eps));
+  GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, 2 * I, H, 0), gemm_bytes(0, T, 2 * I, H, 2, false),
+         gemm(ls::GEMM_FWD, c->n2, H, T, w.pgu, w.agu, 2 * I, H, nullptr, nullptr, 0, ls::EPI_BF16, c->gu, 2 * I,
+              nullptr, 0, st));
   if (recompute) return LS_OK;
   {
-    const long long n = (long long)T * (c->I / 8);
-    ls::swiglu_fwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->gu, c->hbuf, T, c->I);
-    CKL();
+    const long long n = (long long)T * (I / 8);
+    TIMED(LS_K_OTHER, 0, 6.0 * T * I, 1,
+          ls::swiglu_fwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->gu, c->hbuf, T, I));
   }
-  CK(gemm(ls::GEMM_FWD, c->hbuf, c->I, T, w.pd, w.ad, H, c->I, nullptr, nullptr, 0, ls::EPI_BF16, x_out, H, c->x1, H,
-          st));
+  GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, H, I, 0), gemm_bytes(0, T, H, I, 2, true),
+         gemm(ls::GEMM_FWD, c->hbuf, I, T, w.pd, w.ad, H, I, nullptr, nullptr, 0, ls::EPI_BF16, x_out, H, c->x1, H,
+              st));
   return LS_OK;
 }
 
@@ -654,51 +720,66 @@ int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16*
 int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int T, int nseq, const int32_t* cu) {
   cudaStream_t st = c->cs;
   const int H = c->H, I = c->I;
+  const double TH = (double)T * H;
   const ls_ctx::Ad& a = c->ad[layer];
   int rc = layer_forward(c, w, layer, x_in, nullptr, T, nseq, cu, true, true);
   if (rc) return rc;
   // MLP
-  CK(gemm(ls::GEMM_DX, c->gx_bf, H, T, w.pd, w.ad, H, I, nullptr, nullptr, 0, ls::EPI_F32, c->dh, I, nullptr, 0, st));
+  GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, H, I, 0), gemm_bytes(1, T, H, I, 4, false),
+         gemm(ls::GEMM_DX, c->gx_bf, H, T, w.pd, w.ad, H, I, nullptr, nullptr, 0, ls::EPI_F32, c->dh, I, nullptr, 0,
+              st));
   {
     const long long n = (long long)T * (I / 4);
-    ls::swiglu_bwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->dh, c->gu, c->dgu, T, I);
-    CKL();
+    TIMED(LS_K_OTHER, 0, 12.0 * T * I, 1,
+          ls::swiglu_bwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->dh, c->gu, c->dgu, T, I));
   }
-  CK(gemm(ls::GEMM_DX, c->dgu, 2 * I, T, w.pgu, w.agu, 2 * I, H, nullptr, nullptr, 0, ls::EPI_F32, c->dn, H, nullptr,
-          0, st));
-  ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, c->x1, c->rstd2, w.w2, c->gx, c->gx_bf, T, H, 1);
-  CKL();
+  GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, 2 * I, H, 0), gemm_bytes(1, T, 2 * I, H, 4, false),
+         gemm(ls::GEMM_DX, c->dgu, 2 * I, T, w.pgu, w.agu, 2 * I, H, nullptr, nullptr, 0, ls::EPI_F32, c->dn, H,
+              nullptr, 0, st));
+  TIMED(LS_K_OTHER, 0, 16 * TH, 1,
+        ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, c->x1, c->rstd2, w.w2, c->gx, c->gx_bf, T, H, 1));
   // attention
-  CK(gemm(ls::GEMM_DX, c->gx_bf, H, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->do_bf, c->nq,
-          nullptr, 0, st));
-  CK(attn_bwd(c->hd, c->qkv, c->nqkv, c->do_bf, c->attn_o, c->nq, c->lse_attn, cu, nseq, c->maxlen, c->nh, c->nkv,
-              c->Dattn, c->dqkv_f, c->nqkv, T, st));
+  GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, H, c->nq, 0), gemm_bytes(1, T, H, c->nq, 2, false),
+         gemm(ls::GEMM_DX, c->gx_bf, H, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->do_bf, c->nq,
+              nullptr, 0, st));
+  GEMM_T(LS_K_ATTN_BWD, 2 * attn_flop(c, T, nseq), 2.0 * T * (c->nqkv + 2 * c->nq) + 4.0 * T * c->nqkv,
+         attn_bwd(c->hd, c->qkv, c->nqkv, c->do_bf, c->attn_o, c->nq, c->lse_attn, cu, nseq, c->maxlen, c->nh,
+                  c->nkv, c->Dattn, c->dqkv_f, c->nqkv, T, st));
+  c->st.kernel_launches += 2;
   {
     const long long n = (long long)T * c->nqkv;
-    ls::rope_bwd_cast_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->dqkv_f, c->dqkv_bf, c->nqkv, c->pos, c->rope_cos,
-                                                            c->rope_sin, T, c->nh + c->nkv, c->hd, c->nqkv);
-    CKL();
+    TIMED(LS_K_OTHER, 0, 6.0 * n, 1,
+          ls::rope_bwd_cast_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->dqkv_f, c->dqkv_bf, c->nqkv, c->pos,
+                                                                  c->rope_cos, c->rope_sin, T, c->nh + c->nkv, c->hd,
+                                                                  c->nqkv));
   }
   const bool use = a.on;
   if (use) {
     const float s = c->cfg.lora_scale;
-    ls::lora_du_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dqkv_bf, c->nqkv, 0, c->nq, a.bq, c->nq + c->nkvd, c->nkvd,
-                                                   a.bv, c->r, s, c->du, c->du_ext, T);
-    CKL();
+    TIMED(LS_K_OTHER, 2.0 * T * (c->nq + c->nkvd) * c->r, 2.0 * T * (c->nq + c->nkvd), 1,
+          ls::lora_du_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dqkv_bf, c->nqkv, 0, c->nq, a.bq, c->nq + c->nkvd,
+                                                         c->nkvd, a.bv, c->r, s, c->du, c->du_ext, T));
     // dB = dY^T u ;  dA = (s du)^T x
-    CK(lora_outer(c->dqkv_bf, c->nqkv, c->nq, nullptr, c->u_ext, 64, c->r, T, 0, 1, c->lora_part, 128, a.gbq, st));
-    CK(lora_outer(c->dqkv_bf + c->nq + c->nkvd, c->nqkv, c->nkvd, nullptr, c->u_ext + 16, 64, c->r, T, 0, 1,
-                  c->lora_part, 128, a.gbv, st));
-    CK(lora_outer(c->n1, H, H, c->du, nullptr, 32, c->r, T, 1, 1, c->lora_part, 128, a.gaq, st));
-    CK(lora_outer(c->n1, H, H, c->du + 16, nullptr, 32, c->r, T, 1, 1, c->lora_part, 128, a.gav, st));
+    GEMM_T(LS_K_OTHER, 2.0 * T * c->nq * c->r, 2.0 * T * c->nq,
+           lora_outer(c->dqkv_bf, c->nqkv, c->nq, nullptr, c->u_ext, 64, c->r, T, 0, 1, c->lora_part, 128, a.gbq, st));
+    GEMM_T(LS_K_OTHER, 2.0 * T * c->nkvd * c->r, 2.0 * T * c->nkvd,
+           lora_outer(c->dqkv_bf + c->nq + c->nkvd, c->nqkv, c->nkvd, nullptr, c->u_ext + 16, 64, c->r, T, 0, 1,
+                      c->lora_part, 128, a.gbv, st));
+    GEMM_T(LS_K_OTHER, 2.0 * TH * c->r, 2 * TH,
+           lora_outer(c->n1, H, H, c->du, nullptr, 32, c->r, T, 1, 1, c->lora_part, 128, a.gaq, st));
+    GEMM_T(LS_K_OTHER, 2.0 * TH * c->r, 2 * TH,
+           lora_outer(c->n1, H, H, c->du + 16, nullptr, 32, c->r, T, 1, 1, c->lora_part, 128, a.gav, st));
+    c->st.kernel_launches += 4;
     const int n = H * 64;
-    ls::build_ext_bwd_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.aq, a.av, c->r, H, c->ext_bwd);
-    CKL();
+    TIMED(LS_K_OTHER, 0, 2.0 * n, 1,
+          ls::build_ext_bwd_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.aq, a.av, c->r, H, c->ext_bwd));
   }
-  CK(gemm(ls::GEMM_DX, c->dqkv_bf, c->nqkv, T, w.pqkv, w.aqkv, c->nqkv, H, c->du_ext, c->ext_bwd, use ? 32 : 0,
-          ls::EPI_F32, c->dn, H, nullptr, 0, st));
-  ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, x_in, c->rstd1, w.w1, c->gx, c->gx_bf, T, H, 1);
-  CKL();
+  const int ek = use ? 32 : 0;
+  GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, c->nqkv, H, ek), gemm_bytes(1, T, c->nqkv, H, 4, false),
+         gemm(ls::GEMM_DX, c->dqkv_bf, c->nqkv, T, w.pqkv, w.aqkv, c->nqkv, H, c->du_ext, c->ext_bwd, ek, ls::EPI_F32,
+              c->dn, H, nullptr, 0, st));
+  TIMED(LS_K_OTHER, 0, 16 * TH, 1,
+        ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, x_in, c->rstd1, w.w1, c->gx, c->gx_bf, T, H, 1));
   return LS_OK;
 }
 
@@ -810,6 +891,8 @@ int ls_destroy(ls_ctx* c) {
     if (c->ev_ready[s]) cudaEventDestroy(c->ev_ready[s]);
     if (c->ev_free[s]) cudaEventDestroy(c->ev_free[s]);
   }
+  for (auto& e : c->prof_ev)
+    if (e) cudaEventDestroy(e);
   delete c;
   return LS_OK;
 }
@@ -927,14 +1010,14 @@ int stream_step_fwd(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t nseq,
   cudaStream_t st = c->cs;
   const int H = c->H;
   const bool save = save_acts != 0;
-  ls::seq_setup_kernel<<<(T + 255) / 256, 256, 0, st>>>(d_tokens, d_cu, nseq, nullptr, nullptr, c->pos, c->tgt,
-                                                       nullptr, T);
-  CKL();
+  TIMED(LS_K_OTHER, 0, 12.0 * T, 1,
+        ls::seq_setup_kernel<<<(T + 255) / 256, 256, 0, st>>>(d_tokens, d_cu, nseq, nullptr, nullptr, c->pos, c->tgt,
+                                                             nullptr, T));
   bf16* x0 = save ? c->acts : c->xping;
   {
     const long long n = (long long)T * (H / 8);
-    ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, st>>>(d_tokens, c->emb_p, c->emb_a, x0, T, H);
-    CKL();
+    TIMED(LS_K_OTHER, 0, (0.5625 + 2.0) * T * H, 1,
+          ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, st>>>(d_tokens, c->emb_p, c->emb_a, x0, T, H));
   }
   bf16* hf = save ? c->hf_save : c->hf_tmp;
   float* rstdf = save ? c->rstdf_save : c->rstdf_tmp;
@@ -953,8 +1036,8 @@ int stream_step_fwd(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t nseq,
     const int ch = item - c->L;
     if (ch == 0) {
       const bf16* xL = save ? c->acts + (size_t)c->L * (size_t)c->Tmax * H : c->xping + (size_t)(c->L & 1) * TH;
-      ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(xL, c->wf, hf, rstdf, T, H, c->cfg.eps);
-      CKL();
+      TIMED(LS_K_OTHER, 0, 4.0 * T * H, 1,
+            ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(xL, c->wf, hf, rstdf, T, H, c->cfg.eps));
     }
     const int v0 = ch * c->vrows;
     const int n = std::min(c->vrows, c->V - v0);
@@ -971,17 +1054,15 @@ int stream_step_fwd(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t nseq,
     g.g.vocab_off = v0;
     g.g.part_max = c->pmax; g.g.part_sum = c->psum; g.g.part_ld = c->P;
     g.g.tgt_logit = c->tgt_logit;
-    CK(ls::launch_nf4_gemm(g, st));
+    GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, n, H, 0), gemm_bytes(0, T, n, H, 0, false) + 8.0 * T * (n / 128),
+           ls::launch_nf4_gemm(g, st));
     return LS_OK;
   });
   if (rc) return rc;
-  ls::logprob_combine_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->pmax, c->psum, c->P, c->P, c->tgt_logit, c->tgt, lse,
-                                                         c->lp, T);
-  CKL();
-  if (d_sums) {
-    ls::seq_sum_kernel<<<nseq, 256, 0, st>>>(c->lp, d_mask, d_cu, d_sums);
-    CKL();
-  }
+  TIMED(LS_K_OTHER, 0, 8.0 * T * c->P, 1,
+        ls::logprob_combine_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->pmax, c->psum, c->P, c->P, c->tgt_logit, c->tgt,
+                                                               lse, c->lp, T));
+  if (d_sums) TIMED(LS_K_OTHER, 0, 5.0 * T, 1, ls::seq_sum_kernel<<<nseq, 256, 0, st>>>(c->lp, d_mask, d_cu, d_sums));
   c->last_T = T;
   c->last_lse = lse;
   if (save) {
@@ -1005,8 +1086,7 @@ int dpo_loss(ls_ctx* c, const float* d_pi, const float* d_ref, int32_t npairs, f
   int rc = sticky(c);
   if (rc) return rc;
   if (!d_pi || !d_ref || npairs < 1) return fail(c, LS_ERR_ARG, "dpo_loss: bad arguments");
-  ls::dpo_loss_kernel<<<1, 32, 0, c->cs>>>(d_pi, d_ref, npairs, beta, d_loss, d_coeffs);
-  CKL();
+  TIMED(LS_K_OTHER, 0, 16.0 * npairs, 1, ls::dpo_loss_kernel<<<1, 32, 0, c->cs>>>(d_pi, d_ref, npairs, beta, d_loss, d_coeffs));
   return LS_OK;
 }
 
@@ -1029,8 +1109,7 @@ int sft_loss(ls_ctx* c, const float* d_sums, int32_t nseq, float count, float* d
   int rc = sticky(c);
   if (rc) return rc;
   if (!d_sums || nseq < 1 || !(count > 0.f)) return fail(c, LS_ERR_ARG, "sft_loss: bad arguments");
-  ls::sft_loss_kernel<<<1, 32, 0, c->cs>>>(d_sums, nseq, count, d_loss, d_coeffs);
-  CKL();
+  TIMED(LS_K_OTHER, 0, 8.0 * nseq, 1, ls::sft_loss_kernel<<<1, 32, 0, c->cs>>>(d_sums, nseq, count, d_loss, d_coeffs));
   return LS_OK;
 }
 
@@ -1042,9 +1121,9 @@ int stream_step_bwd(ls_ctx* c, const float* d_coeffs) {
   cudaStream_t st = c->cs;
   const int T = c->s_T, nseq = c->s_nseq, H = c->H;
   const int32_t* cu = c->s_cu;
-  ls::seq_setup_kernel<<<(T + 255) / 256, 256, 0, st>>>(c->s_tokens, cu, nseq, c->s_mask, d_coeffs, c->pos, c->tgt,
-                                                       c->coef, T);
-  CKL();
+  TIMED(LS_K_OTHER, 0, 17.0 * T, 1,
+        ls::seq_setup_kernel<<<(T + 255) / 256, 256, 0, st>>>(c->s_tokens, cu, nseq, c->s_mask, d_coeffs, c->pos,
+                                                             c->tgt, c->coef, T));
   std::vector<int> items;
   for (int v = c->nvch - 1; v >= 0; --v) items.push_back(c->L + v);
   for (int l = c->L - 1; l >= 0; --l) items.push_back(l);
@@ -1067,14 +1146,16 @@ int stream_step_bwd(ls_ctx* c, const float* d_coeffs) {
       g.g.out = c->dlogits; g.g.ldo = n;
       g.g.targets = c->tgt; g.g.vocab_off = v0;
       g.g.lse = c->lse_save; g.g.coef = c->coef;
-      CK(ls::launch_nf4_gemm(g, st));
-      CK(gemm(ls::GEMM_DX, c->dlogits, n, T, img, wa, n, H, nullptr, nullptr, 0,
-              first_chunk ? ls::EPI_F32 : ls::EPI_F32_ACC, c->dhf, H, nullptr, 0, st));
+      GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, n, H, 0), gemm_bytes(0, T, n, H, 2, false), ls::launch_nf4_gemm(g, st));
+      const int epi = first_chunk ? ls::EPI_F32 : ls::EPI_F32_ACC;
+      GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, n, H, 0), gemm_bytes(1, T, n, H, first_chunk ? 4 : 8, false),
+             gemm(ls::GEMM_DX, c->dlogits, n, T, img, wa, n, H, nullptr, nullptr, 0, epi, c->dhf, H, nullptr, 0, st));
       first_chunk = false;
       if (ch == 0) {
         const bf16* xL = c->acts + (size_t)c->L * (size_t)c->Tmax * H;
-        ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dhf, xL, c->rstdf_save, c->wf, c->gx, c->gx_bf, T, H, 0);
-        CKL();
+        TIMED(LS_K_OTHER, 0, 12.0 * T * H, 1,
+              ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dhf, xL, c->rstdf_save, c->wf, c->gx, c->gx_bf,
+                                                                 T, H, 0));
       }
       return LS_OK;
     }
@@ -1144,6 +1225,41 @@ int ls_stats(ls_ctx* c, ls_stats_t* out, int32_t reset) {
   *out = c->st;
   if (reset) {
     c->st.layer_reads = c->st.vocab_reads = c->st.h2d_bytes = c->st.slot_reuses = 0;
+    c->st.kernel_launches = 0;
+  }
+  return LS_OK;
+}
+
+int ls_profile(ls_ctx* c, int32_t enable) {
+  if (!c) return set_thread_err(LS_ERR_ARG, "null context");
+  if (enable) {
+    if (c->prof_ev.empty()) {
+      c->prof_ev.resize(2 * kProfMax);
+      for (auto& e : c->prof_ev) CK(cudaEventCreate(&e));
+      c->prof_cls.resize(kProfMax);
+      c->prof_flop.resize(kProfMax);
+      c->prof_bytes.resize(kProfMax);
+    }
+    c->prof_used = 0;
+    c->prof_on = true;
+  } else {
+    c->prof_on = false;
+  }
+  return LS_OK;
+}
+
+int ls_profile_read(ls_ctx* c, ls_profile_t* out) {
+  if (!c || !out) return set_thread_err(LS_ERR_ARG, "ls_profile_read: null argument");
+  memset(out, 0, sizeof(*out));
+  CK(cudaStreamSynchronize(c->cs));
+  for (size_t i = 0; i < c->prof_used; ++i) {
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, c->prof_ev[2 * i], c->prof_ev[2 * i + 1]));
+    const int k = c->prof_cls[i];
+    out->launches[k] += 1;
+    out->ms[k] += ms;
+    out->flop[k] += c->prof_flop[i];
+    out->bytes[k] += c->prof_bytes[i];
   }
   return LS_OK;
 }

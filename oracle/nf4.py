@@ -19,6 +19,9 @@ Readings taken where the pages are silent:
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 BLOCK = 64
@@ -61,17 +64,31 @@ def nf4_quantize(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     blocks = w.reshape(n, k // BLOCK, BLOCK)
     absmax = np.abs(blocks).max(axis=2).astype(np.float32)
     codes = np.empty((n, k // BLOCK, BLOCK), np.uint8)
-    # Work in row chunks to bound the [.., 16] distance tensor.
-    step = max(1, (1 << 22) // max(1, k))
-    for r0 in range(0, n, step):
-        b = blocks[r0:r0 + step]
-        a = absmax[r0:r0 + step, :, None]
+
+    def rows(r0, r1):
         with np.errstate(invalid="ignore", divide="ignore"):
-            x = (b / a).astype(np.float32)                      # fp32 quotient
-        d = np.abs(x[..., None] - NF4_TABLE).astype(np.float32)  # fp32 distances
-        c = np.argmin(d, axis=-1).astype(np.uint8)               # first minimum
-        c[np.broadcast_to(a == 0, c.shape)] = 7
-        codes[r0:r0 + step] = c
+            x = blocks[r0:r1] / absmax[r0:r1, :, None]          # fp32 quotient
+        # argmin_j |x - q_j| as a running minimum over j; strict '<' keeps the lower index on ties
+        best = np.abs(x - NF4_TABLE[0])
+        c = np.zeros(x.shape, np.uint8)
+        d = np.empty_like(x)
+        better = np.empty(x.shape, bool)
+        for j in range(1, 16):
+            np.subtract(x, NF4_TABLE[j], out=d)
+            np.abs(d, out=d)
+            np.less(d, best, out=better)
+            np.copyto(best, d, where=better)
+            np.copyto(c, np.uint8(j), where=better)
+        c[np.broadcast_to(absmax[r0:r1, :, None] == 0, c.shape)] = 7
+        codes[r0:r1] = c
+
+    step = max(1, (1 << 20) // k)
+    spans = [(r0, min(n, r0 + step)) for r0 in range(0, n, step)]
+    if len(spans) > 1:
+        with ThreadPoolExecutor(min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(lambda sp: rows(*sp), spans))
+    else:
+        rows(0, n)
     return codes.reshape(n, k), absmax
 
 
