@@ -68,7 +68,7 @@ typedef struct ls_config {
   int32_t max_seq_len;     /* longest sequence (RoPE table rows); 0 = max_tokens      */
   int32_t vocab_chunk_rows;/* rows of the vocabulary head per streamed chunk; 0 = auto */
   int32_t resident;        /* 1: keep every layer on the device (test/reference mode) */
-  int32_t reserved;
+  int32_t dpo_shared_read; /* 1: size the forward for stream_step_fwd_dpo (2 x max_tokens rows) */
   uint64_t cap_bytes;      /* device-memory cap for the workspace; 0 = none           */
 } ls_config;
 
@@ -155,9 +155,24 @@ int stream_step_fwd(ls_ctx* ctx, const int32_t* d_tokens, int32_t T, int32_t nse
                     const int32_t* d_seq_offsets, const uint8_t* d_loss_mask, int32_t adapter_on,
                     int32_t save_acts, float* d_seq_logprob_sums);
 
+/* Shared-read DPO forward: the policy pass (adapter on, activation store kept for
+ * stream_step_bwd) and the reference pass (adapter off) over the same T tokens in
+ * ONE sweep of the streamed layers.  Each layer is copied to its slot once and
+ * serves both passes, which run as one batch of 2T rows (rows 0..T-1 with the
+ * adapter, rows T..2T-1 without), so a DPO step reads every layer twice (forward,
+ * backward) instead of three times.  The reference logprobs still come from the
+ * same streamed base with the adapter off, as in the two-pass form (Show HN:
+ * Fine-tune an 8B model on a 4 GB laptop GPU, opening paragraph); every row is
+ * computed by the same row-independent kernels.  Writes the policy and reference
+ * sequence sums (fp32 [nseq] each; the mask selects positions as in
+ * stream_step_fwd).  Needs cfg.dpo_shared_read = 1 (LS_ERR_STATE otherwise).
+ * Afterwards seq_logprobs returns 2T values: policy rows, then reference rows. */
+int stream_step_fwd_dpo(ls_ctx* ctx, const int32_t* d_tokens, int32_t T, int32_t nseq, const int32_t* d_seq_offsets,
+                        const uint8_t* d_loss_mask, float* d_pi_sums, float* d_ref_sums);
+
 /* Per-token logprob log p(token[t+1] | tokens <= t) and log-sum-exp of the last
- * forward pass (fp32 [T] each; 0 logprob at a sequence's last position).  Either
- * output may be NULL. */
+ * forward pass (fp32 [T] each, [2T] after stream_step_fwd_dpo; 0 logprob at a
+ * sequence's last position).  Either output may be NULL. */
 int seq_logprobs(ls_ctx* ctx, float* d_token_logprobs, float* d_token_lse);
 
 /* DPO loss over npairs (chosen, rejected) sequence pairs laid out pairwise:
@@ -219,6 +234,14 @@ int ls_profile(ls_ctx* ctx, int32_t enable);
 
 /* Wait for the compute stream and total the timed launches by class. */
 int ls_profile_read(ls_ctx* ctx, ls_profile_t* out);
+
+/* Copy entry `layer` of the activation store of the last forward pass run with
+ * save_acts = 1 into d_out (bf16 [T, H], caller-owned device memory), on the compute
+ * stream: layer 0 is the embedding output (the input of decoder layer 0), layer l
+ * the input of decoder layer l, layer L the output of the last decoder layer.  An
+ * inspection hook (layer-by-layer checks against a reference implementation); a
+ * training step never needs it.  LS_ERR_STATE without a saved forward. */
+int ls_read_activation(ls_ctx* ctx, int32_t layer, uint16_t* d_out);
 
 /* Test hook: make every later slot copy on the copy stream first wait host_delay_ms
  * on the host (a host callback), so a bounded ls_sync can be shown to give up.  No

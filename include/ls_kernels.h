@@ -85,12 +85,14 @@ int lsk_swiglu_bwd(const float* dh, const uint16_t* gu, uint16_t* dgu, int32_t T
 /* LoRA down-projection for the forward extra stage: u_ext bf16 [T, 64] =
  * [bf16(s x A_q^T) | bf16(s x A_v^T) | 0]; x bf16 [T, ldx], A bf16 [r, K] (either
  * may be NULL), r <= 16 (Soup: Fine-Tune an 8B Model on a 4 GB GPU, soup.yaml
- * listing: r 16 on q_proj, v_proj). */
+ * listing: r 16 on q_proj, v_proj).  K a multiple of 16, ldx even. */
 int lsk_lora_down(const uint16_t* x, int64_t ldx, const uint16_t* a_q, const uint16_t* a_v, int32_t r,
                   int32_t K, float s, uint16_t* u_ext, int32_t T, void* stream);
 
 /* du fp32 [T, 32] = s [dY_q B_q | dY_v B_v] (dY columns at col_q / col_v of dy
- * [T, ldy]) and its bf16 copy du_ext [T, 64] (columns 32..63 zero). */
+ * [T, ldy]) and its bf16 copy du_ext [T, 64] (columns 32..63 zero).  ldy, col_q and
+ * col_v even; nq, nv multiples of 16.  Both down-projections run on the tensor cores
+ * (mma.sync, fp32 accumulation) with a fixed-order reduction over K. */
 int lsk_lora_du(const uint16_t* dy, int64_t ldy, int32_t col_q, int32_t nq, const uint16_t* b_q,
                 int32_t col_v, int32_t nv, const uint16_t* b_v, int32_t r, float s, float* du, uint16_t* du_ext,
                 int32_t T, void* stream);
@@ -98,6 +100,7 @@ int lsk_lora_du(const uint16_t* dy, int64_t ldy, int32_t col_q, int32_t nq, cons
 /* Deterministic outer product over tokens: out (+)= X^T U with X bf16 [T, ldx]
  * (ncols columns) and U (fp32 u_f32 or bf16 u_bf16, [T, ldu], first r columns).
  * layout 0: out [ncols, r] (dB shape); layout 1: out [r, ncols] (dA shape).
+ * X rows must be 16-byte aligned (X 16-byte aligned, ldx and ncols multiples of 8).
  * scratch fp32 of nchunks * ncols * 16 floats, nchunks = ceil(T / rows_per_chunk). */
 int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* u_f32, const uint16_t* u_bf16,
                    int32_t ldu, int32_t r, int32_t T, int32_t layout, int32_t accumulate, float* scratch,

@@ -30,7 +30,7 @@ class ls_config(C.Structure):
                 ("head_dim", C.c_int32), ("inter", C.c_int32), ("vocab", C.c_int32), ("tied", C.c_int32),
                 ("lora_r", C.c_int32), ("lora_scale", C.c_float), ("rope_theta", C.c_float), ("eps", C.c_float),
                 ("max_tokens", C.c_int32), ("max_seqs", C.c_int32), ("max_seq_len", C.c_int32),
-                ("vocab_chunk_rows", C.c_int32), ("resident", C.c_int32), ("reserved", C.c_int32),
+                ("vocab_chunk_rows", C.c_int32), ("resident", C.c_int32), ("dpo_shared_read", C.c_int32),
                 ("cap_bytes", C.c_uint64)]
 
 
@@ -80,6 +80,7 @@ _SIGS = {
     "load_vocab_nf4": [P, C.POINTER(ls_vocab_host)],
     "ls_set_adapter": [P, I32, P, P, P, P, P, P, P, P],
     "stream_step_fwd": [P, P, I32, I32, P, P, I32, I32, P],
+    "stream_step_fwd_dpo": [P, P, I32, I32, P, P, P, P],
     "seq_logprobs": [P, P, P],
     "dpo_loss": [P, P, P, I32, F32, P, P],
     "sft_loss": [P, P, I32, F32, P, P],
@@ -88,6 +89,7 @@ _SIGS = {
     "ls_sync": [P, I32],
     "ls_stats": [P, C.POINTER(ls_stats_t), I32],
     "ls_debug_copy_delay": [P, I32],
+    "ls_read_activation": [P, I32, P],
     "ls_profile": [P, I32],
     "ls_profile_read": [P, C.POINTER(ls_profile_t)],
     "lsk_nf4_dequant": [P, P, I64, I32, P, P],

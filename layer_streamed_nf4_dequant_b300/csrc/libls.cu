@@ -142,6 +142,8 @@ struct ls_ctx {
   bf16 *hf_save, *hf_tmp, *dlogits;
   float *rstdf_save, *rstdf_tmp, *pmax, *psum, *tgt_logit, *lse_save, *lse_tmp, *lp, *coef, *dhf, *loss_tmp;
   int32_t *tgt, *pos;
+  int32_t *tok2 = nullptr, *cu2 = nullptr;   // shared-read DPO forward: doubled batch
+  int Tf = 0;                                 // forward row capacity (2 max_tokens with shared read)
   int P = 0;
   size_t lora_part_floats = 0;
 
@@ -315,6 +317,8 @@ Planned lay_out(const ls_config& k, ls_ctx* c) {
   Planned p;
   const LayerLayout ll = layer_layout(k);
   const size_t T = k.max_tokens, H = k.hidden, I = k.inter;
+  // forward-pass buffers hold 2T rows when the policy and reference passes share a sweep
+  const size_t Tf = k.dpo_shared_read ? 2 * T : T;
   const size_t nq = (size_t)k.heads * k.head_dim, nkvd = (size_t)k.kv_heads * k.head_dim, nqkv = nq + 2 * nkvd;
   const int maxlen = k.max_seq_len > 0 ? k.max_seq_len : k.max_tokens;
   size_t slot = ll.bytes;
@@ -342,20 +346,20 @@ Planned lay_out(const ls_config& k, ls_ctx* c) {
   const size_t act0 = b.off;
   bf16* acts = b.take<bf16>((size_t)(k.layers + 1) * T * H);
   p.act_bytes = b.off - act0;
-  bf16* xping = b.take<bf16>(2 * T * H);
+  bf16* xping = b.take<bf16>(2 * Tf * H);
   // forward layer scratch
-  bf16* n1 = b.take<bf16>(T * H);
-  bf16* qkv = b.take<bf16>(T * nqkv);
-  bf16* ao = b.take<bf16>(T * nq);
-  bf16* x1 = b.take<bf16>(T * H);
-  bf16* n2 = b.take<bf16>(T * H);
-  bf16* gu = b.take<bf16>(T * 2 * I);
-  bf16* hb = b.take<bf16>(T * I);
-  bf16* uext = b.take<bf16>(T * 64);
+  bf16* n1 = b.take<bf16>(Tf * H);
+  bf16* qkv = b.take<bf16>(Tf * nqkv);
+  bf16* ao = b.take<bf16>(Tf * nq);
+  bf16* x1 = b.take<bf16>(Tf * H);
+  bf16* n2 = b.take<bf16>(Tf * H);
+  bf16* gu = b.take<bf16>(Tf * 2 * I);
+  bf16* hb = b.take<bf16>(Tf * I);
+  bf16* uext = b.take<bf16>(Tf * 64);
   bf16* extf = b.take<bf16>(nqkv * 64);
-  float* rstd1 = b.take<float>(T);
-  float* rstd2 = b.take<float>(T);
-  float* lsea = b.take<float>((size_t)k.heads * T);
+  float* rstd1 = b.take<float>(Tf);
+  float* rstd2 = b.take<float>(Tf);
+  float* lsea = b.take<float>((size_t)k.heads * Tf);
   // backward
   float* gx = b.take<float>(T * H);
   bf16* gxb = b.take<bf16>(T * H);
@@ -380,20 +384,22 @@ Planned lay_out(const ls_config& k, ls_ctx* c) {
   b.off = std::max(u1.off, u2.off);
   // vocabulary / loss
   bf16* hfs = b.take<bf16>(T * H);
-  bf16* hft = b.take<bf16>(T * H);
+  bf16* hft = b.take<bf16>(Tf * H);
   float* rfs = b.take<float>(T);
-  float* rft = b.take<float>(T);
-  float* pmax = b.take<float>(T * (size_t)p.P);
-  float* psum = b.take<float>(T * (size_t)p.P);
-  float* tl = b.take<float>(T);
+  float* rft = b.take<float>(Tf);
+  float* pmax = b.take<float>(Tf * (size_t)p.P);
+  float* psum = b.take<float>(Tf * (size_t)p.P);
+  float* tl = b.take<float>(Tf);
   float* lses = b.take<float>(T);
-  float* lset = b.take<float>(T);
-  float* lp = b.take<float>(T);
+  float* lset = b.take<float>(Tf);
+  float* lp = b.take<float>(Tf);
   float* coef = b.take<float>(T);
   float* dhf = b.take<float>(T * H);
   float* losst = b.take<float>(64);
-  int32_t* tgt = b.take<int32_t>(T);
-  int32_t* pos = b.take<int32_t>(T);
+  int32_t* tgt = b.take<int32_t>(Tf);
+  int32_t* pos = b.take<int32_t>(Tf);
+  int32_t* tok2 = k.dpo_shared_read ? b.take<int32_t>(Tf) : nullptr;
+  int32_t* cu2 = k.dpo_shared_read ? b.take<int32_t>(2 * (size_t)k.max_seqs + 1) : nullptr;
   p.total = align_up(b.off, 256);
 
   if (c) {
@@ -417,6 +423,7 @@ Planned lay_out(const ls_config& k, ls_ctx* c) {
     c->hf_save = hfs; c->hf_tmp = hft; c->rstdf_save = rfs; c->rstdf_tmp = rft; c->pmax = pmax; c->psum = psum;
     c->tgt_logit = tl; c->lse_save = lses; c->lse_tmp = lset; c->lp = lp; c->coef = coef; c->dhf = dhf;
     c->loss_tmp = losst; c->tgt = tgt; c->pos = pos; c->P = p.P;
+    c->tok2 = tok2; c->cu2 = cu2; c->Tf = (int)Tf;
     c->vrows = vrows; c->nvch = nvch; c->vch_abs_off = abs_off;
   }
   return p;
@@ -514,9 +521,25 @@ cudaError_t lora_outer(const bf16* X, long long ldx, int ncols, const float* Uf,
                        int layout, int accumulate, float* scratch, int rows_per_chunk, float* out, cudaStream_t st) {
   const int nch = (T + rows_per_chunk - 1) / rows_per_chunk;
   dim3 g1((ncols + 127) / 128, nch);
-  ls::lora_outer_partial_kernel<<<g1, 128, 0, st>>>(X, ldx, ncols, Uf, Ub, ldu, T, rows_per_chunk, scratch);
+  ls::lora_outer_partial_kernel<<<g1, 256, 0, st>>>(X, ldx, ncols, Uf, Ub, ldu, T, rows_per_chunk, scratch);
   const int n = ncols * r;
   ls::lora_outer_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(scratch, nch, ncols, r, layout, accumulate, out);
+  return cudaGetLastError();
+}
+
+// LoRA down-projection u_ext = [bf16(s x A_q^T) | bf16(s x A_v^T) | 0].
+cudaError_t lora_down(const bf16* x, long long ldx, const bf16* aq, const bf16* av, int r, int K, float s,
+                      bf16* u_ext, int T, cudaStream_t st) {
+  ls::LoraProjHalf h0{aq, (long long)K, 0, K, 0}, h1{av, (long long)K, 0, K, 0};
+  ls::lora_proj_kernel<<<(T + 15) / 16, 256, 0, st>>>(x, ldx, T, h0, h1, r, s, nullptr, u_ext);
+  return cudaGetLastError();
+}
+
+// du = s [dY_q B_q | dY_v B_v] (fp32 [T, 32]) and its bf16 extra-stage copy du_ext [T, 64].
+cudaError_t lora_du(const bf16* dy, long long ldy, int col_q, int nq, const bf16* bq, int col_v, int nv,
+                    const bf16* bv, int r, float s, float* du, bf16* du_ext, int T, cudaStream_t st) {
+  ls::LoraProjHalf h0{bq, 0, col_q, nq, 1}, h1{bv, 0, col_v, nv, 1};
+  ls::lora_proj_kernel<<<(T + 15) / 16, 256, 0, st>>>(dy, ldy, T, h0, h1, r, s, du, du_ext);
   return cudaGetLastError();
 }
 
@@ -666,7 +689,9 @@ inline double attn_flop(const ls_ctx* c, int T, int nseq) {
 // Forward of one decoder layer up to (recompute == true) the MLP input projections,
 // or to the layer output x_out.
 int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16* x_out, int T, int nseq,
-                  const int32_t* cu, bool adapter, bool recompute) {
+                  const int32_t* cu, bool adapter, bool recompute, int lora_rows = -1) {
+  // rows [0, lora_rows) take the adapter; the extra stage reads zero u rows beyond them
+  if (lora_rows < 0) lora_rows = T;
   cudaStream_t st = c->cs;
   const int H = c->H, I = c->I;
   const double TH = (double)T * H;
@@ -675,9 +700,8 @@ int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16*
   const ls_ctx::Ad& a = c->ad[layer];
   const bool use = adapter && a.on;
   if (use) {
-    TIMED(LS_K_OTHER, 2.0 * T * 2 * c->r * H, 2 * TH, 1,
-          ls::lora_down_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->n1, H, a.aq, a.av, c->r, H, c->cfg.lora_scale,
-                                                            c->u_ext, T));
+    TIMED(LS_K_OTHER, 2.0 * lora_rows * 2 * c->r * H, 2.0 * lora_rows * H, 1,
+          lora_down(c->n1, H, a.aq, a.av, c->r, H, c->cfg.lora_scale, c->u_ext, lora_rows, st));
     const int n = c->nqkv * 64;
     TIMED(LS_K_OTHER, 0, 2.0 * n, 1,
           ls::build_ext_fwd_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.bq, 0, c->nq, a.bv, c->nq + c->nkvd, c->nkvd,
@@ -757,8 +781,8 @@ int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int 
   if (use) {
     const float s = c->cfg.lora_scale;
     TIMED(LS_K_OTHER, 2.0 * T * (c->nq + c->nkvd) * c->r, 2.0 * T * (c->nq + c->nkvd), 1,
-          ls::lora_du_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dqkv_bf, c->nqkv, 0, c->nq, a.bq, c->nq + c->nkvd,
-                                                         c->nkvd, a.bv, c->r, s, c->du, c->du_ext, T));
+          lora_du(c->dqkv_bf, c->nqkv, 0, c->nq, a.bq, c->nq + c->nkvd, c->nkvd, a.bv, c->r, s, c->du, c->du_ext,
+                  T, st));
     // dB = dY^T u ;  dA = (s du)^T x
     GEMM_T(LS_K_OTHER, 2.0 * T * c->nq * c->r, 2.0 * T * c->nq,
            lora_outer(c->dqkv_bf, c->nqkv, c->nq, nullptr, c->u_ext, 64, c->r, T, 0, 1, c->lora_part, 128, a.gbq, st));
@@ -1072,6 +1096,94 @@ int stream_step_fwd(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t nseq,
   return LS_OK;
 }
 
+int stream_step_fwd_dpo(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t nseq, const int32_t* d_cu,
+                        const uint8_t* d_mask, float* d_pi, float* d_ref) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!c->cfg.dpo_shared_read)
+    return fail(c, LS_ERR_STATE, "stream_step_fwd_dpo: context not planned with dpo_shared_read = 1");
+  if (!d_tokens || !d_cu || !d_mask || !d_pi || !d_ref || T < 1 || T > c->Tmax || nseq < 1 ||
+      nseq > c->cfg.max_seqs)
+    return fail(c, LS_ERR_ARG, "stream_step_fwd_dpo: bad buffers or T/nseq outside the configured bounds");
+  for (int l = 0; l < c->L; ++l)
+    if (!c->hl_ok[l]) return fail(c, LS_ERR_STATE, "stream_step_fwd_dpo: layer " + std::to_string(l) + " not loaded");
+  if (!c->hv_ok) return fail(c, LS_ERR_STATE, "stream_step_fwd_dpo: vocabulary not loaded");
+  cudaStream_t st = c->cs;
+  const int H = c->H, T2 = 2 * T, n2 = 2 * nseq;
+  const size_t TH = (size_t)T * H, T2H = (size_t)T2 * H;
+  TIMED(LS_K_OTHER, 0, 12.0 * T2, 1,
+        ls::pair_setup_kernel<<<(T2 + 255) / 256, 256, 0, st>>>(d_tokens, d_cu, nseq, T, c->tok2, c->cu2));
+  TIMED(LS_K_OTHER, 0, 12.0 * T2, 1,
+        ls::seq_setup_kernel<<<(T2 + 255) / 256, 256, 0, st>>>(c->tok2, c->cu2, n2, nullptr, nullptr, c->pos,
+                                                              c->tgt, nullptr, T2));
+  // the reference rows carry no adapter: their rows of the extra-stage input are zero
+  CK(cudaMemsetAsync(c->u_ext + (size_t)T * 64, 0, (size_t)T * 64 * sizeof(bf16), st));
+  bf16* x0 = c->xping;
+  {
+    const long long n = (long long)T * (H / 8);
+    TIMED(LS_K_OTHER, 0, (0.5625 + 2.0) * T * H, 1,
+          ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, st>>>(d_tokens, c->emb_p, c->emb_a, x0, T, H));
+  }
+  CK(cudaMemcpyAsync(x0 + TH, x0, TH * sizeof(bf16), cudaMemcpyDeviceToDevice, st));
+  CK(cudaMemcpyAsync(c->acts, x0, TH * sizeof(bf16), cudaMemcpyDeviceToDevice, st));
+  std::vector<int> items;
+  for (int l = 0; l < c->L; ++l) items.push_back(l);
+  for (int v = 0; v < c->nvch; ++v) items.push_back(c->L + v);
+  rc = run_items(c, items, [&](int item, uint8_t* img) -> int {
+    if (item < c->L) {
+      const int l = item;
+      const bf16* xin = c->xping + (size_t)(l & 1) * T2H;
+      bf16* xout = c->xping + (size_t)((l + 1) & 1) * T2H;
+      int r2 = layer_forward(c, layer_ptrs(c, img), l, xin, xout, T2, n2, c->cu2, true, false, T);
+      if (r2) return r2;
+      // the policy rows are the activation store entry of the next layer
+      CK(cudaMemcpyAsync(c->acts + (size_t)(l + 1) * (size_t)c->Tmax * H, xout, TH * sizeof(bf16),
+                         cudaMemcpyDeviceToDevice, st));
+      return LS_OK;
+    }
+    const int ch = item - c->L;
+    if (ch == 0) {
+      const bf16* xL = c->xping + (size_t)(c->L & 1) * T2H;
+      TIMED(LS_K_OTHER, 0, 4.0 * T2 * H, 1,
+            ls::rmsnorm_fwd_kernel<<<(T2 + 7) / 8, 256, 0, st>>>(xL, c->wf, c->hf_tmp, c->rstdf_tmp, T2, H,
+                                                                c->cfg.eps));
+    }
+    const int v0 = ch * c->vrows;
+    const int n = std::min(c->vrows, c->V - v0);
+    GemmCall g{};
+    g.mode = ls::GEMM_FWD;
+    g.A = c->hf_tmp;
+    g.lda = H;
+    g.Wp = img;
+    g.force_bn = 256;
+    g.g.M = T2; g.g.Nw = n; g.g.Kw = H; g.g.Nout = n; g.g.Kred = H;
+    g.g.absmax = reinterpret_cast<const float*>(img + c->vch_abs_off);
+    g.g.epi = ls::EPI_LOGPROB;
+    g.g.targets = c->tgt;
+    g.g.vocab_off = v0;
+    g.g.part_max = c->pmax; g.g.part_sum = c->psum; g.g.part_ld = c->P;
+    g.g.tgt_logit = c->tgt_logit;
+    GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T2, n, H, 0), gemm_bytes(0, T2, n, H, 0, false) + 8.0 * T2 * (n / 128),
+           ls::launch_nf4_gemm(g, st));
+    return LS_OK;
+  });
+  if (rc) return rc;
+  TIMED(LS_K_OTHER, 0, 8.0 * T2 * c->P, 1,
+        ls::logprob_combine_kernel<<<(T2 + 7) / 8, 256, 0, st>>>(c->pmax, c->psum, c->P, c->P, c->tgt_logit, c->tgt,
+                                                                c->lse_tmp, c->lp, T2));
+  TIMED(LS_K_OTHER, 0, 5.0 * T, 1, ls::seq_sum_kernel<<<nseq, 256, 0, st>>>(c->lp, d_mask, d_cu, d_pi));
+  TIMED(LS_K_OTHER, 0, 5.0 * T, 1, ls::seq_sum_kernel<<<nseq, 256, 0, st>>>(c->lp + T, d_mask, d_cu, d_ref));
+  // what the backward reads of the policy pass
+  CK(cudaMemcpyAsync(c->hf_save, c->hf_tmp, TH * sizeof(bf16), cudaMemcpyDeviceToDevice, st));
+  CK(cudaMemcpyAsync(c->rstdf_save, c->rstdf_tmp, (size_t)T * 4, cudaMemcpyDeviceToDevice, st));
+  CK(cudaMemcpyAsync(c->lse_save, c->lse_tmp, (size_t)T * 4, cudaMemcpyDeviceToDevice, st));
+  c->last_T = T2;
+  c->last_lse = c->lse_tmp;
+  c->saved = true;
+  c->s_tokens = d_tokens; c->s_cu = d_cu; c->s_mask = d_mask; c->s_T = T; c->s_nseq = nseq;
+  return LS_OK;
+}
+
 int seq_logprobs(ls_ctx* c, float* d_lp, float* d_lse) {
   int rc = sticky(c);
   if (rc) return rc;
@@ -1264,6 +1376,16 @@ int ls_profile_read(ls_ctx* c, ls_profile_t* out) {
   return LS_OK;
 }
 
+int ls_read_activation(ls_ctx* c, int32_t layer, uint16_t* d_out) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!c->saved) return fail(c, LS_ERR_STATE, "ls_read_activation: no forward pass with save_acts=1");
+  if (!d_out || layer < 0 || layer > c->L) return fail(c, LS_ERR_ARG, "ls_read_activation: bad layer or null output");
+  const size_t n = (size_t)c->s_T * c->H;
+  CK(cudaMemcpyAsync(d_out, c->acts + (size_t)layer * (size_t)c->Tmax * c->H, n * 2, cudaMemcpyDeviceToDevice, c->cs));
+  return LS_OK;
+}
+
 int ls_debug_copy_delay(ls_ctx* c, int32_t ms) {
   if (!c) return set_thread_err(LS_ERR_ARG, "null context");
   c->copy_delay_ms = ms > 0 ? ms : 0;
@@ -1413,32 +1535,29 @@ int lsk_lora_down(const uint16_t* x, int64_t ldx, const uint16_t* aq, const uint
                   float sc, uint16_t* u_ext, int32_t T, void* s) {
   if (!x || !u_ext || r < 1 || r > 16 || K <= 0 || K % 8 || ldx < K || ldx % 8 || T < 0)
     return set_thread_err(LS_ERR_ARG, "lsk_lora_down: bad args");
+  if (K % 16) return set_thread_err(LS_ERR_ARG, "lsk_lora_down: K must be a multiple of 16");
   if (T == 0) return LS_OK;
-  ls::lora_down_kernel<<<(T + 7) / 8, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(x), ldx,
-                                                          reinterpret_cast<const bf16*>(aq),
-                                                          reinterpret_cast<const bf16*>(av), r, K, sc,
-                                                          reinterpret_cast<bf16*>(u_ext), T);
-  KLAUNCH();
+  KCK(lora_down(reinterpret_cast<const bf16*>(x), ldx, reinterpret_cast<const bf16*>(aq),
+                reinterpret_cast<const bf16*>(av), r, K, sc, reinterpret_cast<bf16*>(u_ext), T, STREAM(s)));
   return LS_OK;
 }
 
 int lsk_lora_du(const uint16_t* dy, int64_t ldy, int32_t col_q, int32_t nq, const uint16_t* bq, int32_t col_v,
                 int32_t nv, const uint16_t* bv, int32_t r, float sc, float* du, uint16_t* du_ext, int32_t T, void* s) {
-  if (!dy || !du || !du_ext || r < 1 || r > 16 || T < 0) return set_thread_err(LS_ERR_ARG, "lsk_lora_du: bad args");
+  if (!dy || !du || !du_ext || r < 1 || r > 16 || T < 0 || ldy % 2 || col_q % 2 || col_v % 2 ||
+      (bq && (nq < 16 || nq % 16)) || (bv && (nv < 16 || nv % 16)))
+    return set_thread_err(LS_ERR_ARG, "lsk_lora_du: bad args (even pitch/offsets, widths multiples of 16)");
   if (T == 0) return LS_OK;
-  ls::lora_du_kernel<<<(T + 7) / 8, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(dy), ldy, col_q, nq,
-                                                        reinterpret_cast<const bf16*>(bq), col_v, nv,
-                                                        reinterpret_cast<const bf16*>(bv), r, sc, du,
-                                                        reinterpret_cast<bf16*>(du_ext), T);
-  KLAUNCH();
+  KCK(lora_du(reinterpret_cast<const bf16*>(dy), ldy, col_q, nq, reinterpret_cast<const bf16*>(bq), col_v, nv,
+              reinterpret_cast<const bf16*>(bv), r, sc, du, reinterpret_cast<bf16*>(du_ext), T, STREAM(s)));
   return LS_OK;
 }
 
 int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* uf, const uint16_t* ub, int32_t ldu,
                    int32_t r, int32_t T, int32_t layout, int32_t accumulate, float* scratch, int32_t rpc, float* out,
                    void* s) {
-  if (!X || (!uf && !ub) || !scratch || !out || r < 1 || r > 16 || ncols < 1 || T < 1 || rpc < 1 ||
-      (layout != 0 && layout != 1))
+  if (!X || (!uf && !ub) || !scratch || !out || r < 1 || r > 16 || ncols < 1 || ncols % 8 || ldx % 8 ||
+      (reinterpret_cast<uintptr_t>(X) & 15) || T < 1 || rpc < 1 || (layout != 0 && layout != 1))
     return set_thread_err(LS_ERR_ARG, "lsk_lora_outer: bad args");
   KCK(lora_outer(reinterpret_cast<const bf16*>(X), ldx, ncols, uf, reinterpret_cast<const bf16*>(ub), ldu, r, T,
                  layout, accumulate, scratch, rpc, out, STREAM(s)));

@@ -246,6 +246,15 @@ __global__ void seq_setup_kernel(const int* __restrict__ tokens, const int* __re
   if (coef) coef[t] = (seq_coef && mask && mask[t] && t + 1 < b) ? seq_coef[s] : 0.f;
 }
 
+// Doubled batch of the shared-read DPO forward: tok2 = [tok; tok] and sequence offsets
+// cu2 = [cu; T + cu[1..nseq]] (the reference copy of every sequence follows the policy copies).
+__global__ void pair_setup_kernel(const int* __restrict__ tokens, const int* __restrict__ cu, int nseq, int T,
+                                  int* __restrict__ tok2, int* __restrict__ cu2) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < 2 * T) tok2[i] = tokens[i < T ? i : i - T];
+  if (i <= 2 * nseq) cu2[i] = i <= nseq ? cu[i] : T + cu[i - nseq];
+}
+
 // lse[t] = log sum_v exp(logit) from per-column-group (max, sum-exp) partials, in
 // partial order; lp[t] = logit[t, target] - lse[t] (0 without a target).
 __global__ void logprob_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum, int P,
@@ -307,117 +316,153 @@ __global__ void dpo_loss_kernel(const float* __restrict__ pi, const float* __res
 }
 
 // ------------------------------------------------------------------ LoRA pieces
-// u_ext [T, 64] bf16 = [bf16(s x A_q^T) | bf16(s x A_v^T) | 0]; A [r, K] bf16, r <= 16.
-// One warp per row; each lane takes 8 contiguous K values per step.
-__global__ void lora_down_kernel(const __nv_bfloat16* __restrict__ x, long long ldx, const __nv_bfloat16* __restrict__ a0,
-                                 const __nv_bfloat16* __restrict__ a1, int r, int K, float s,
-                                 __nv_bfloat16* __restrict__ u_ext, int T) {
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= T) return;
-  float acc[32];
+// Rank-r projections of the LoRA branch (Soup's soup.yaml listing: r 16 on q_proj and
+// v_proj), as one small contraction with N = 2 x 16 output columns:
+//   out[t, 16 h + j] = sum_k X[t, xcol_h + k] * W_h[j, k]      (h = 0, 1; j < r, else 0)
+// Forward down-projection: X = normed input, W_h = A_q / A_v  [r, K]   (row-major)
+// Backward du:             X = dY (q / v columns), W_h = B_q^T / B_v^T (B [N, r], read transposed)
+// Results: out_f32 [T, 32] = s * sum (optional) and out_ext [T, 64] = bf16(s * sum) with
+// columns 32..63 zero (the extra reduction stage of the fused NF4 GEMM).
+// Tensor cores through mma.sync m16n8k16 (bf16 in, fp32 accumulate).  One block = 16
+// rows; its 8 warps split K evenly and are summed in warp order, so the result does not
+// depend on scheduling.
+struct LoraProjHalf {
+  const __nv_bfloat16* w;   // null: this half is absent (columns stay zero)
+  long long ldw;            // row pitch of W_h when not transposed
+  int xcol, K, trans;
+};
+
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t lora_w_pair(const LoraProjHalf& h, int n, int k, int r) {
+  if (n >= r) return 0u;
+  if (!h.trans) return *reinterpret_cast<const uint32_t*>(h.w + (size_t)n * h.ldw + k);
+  const uint16_t* w = reinterpret_cast<const uint16_t*>(h.w);
+  return (uint32_t)w[(size_t)k * r + n] | ((uint32_t)w[(size_t)(k + 1) * r + n] << 16);
+}
+
+__global__ void __launch_bounds__(256) lora_proj_kernel(const __nv_bfloat16* __restrict__ X, long long ldx, int T,
+                                                        LoraProjHalf h0, LoraProjHalf h1, int r, float s,
+                                                        float* __restrict__ out_f32,
+                                                        __nv_bfloat16* __restrict__ out_ext) {
+  __shared__ float red[8][16][33];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, cq = lane & 3;
+  const int r0 = blockIdx.x * 16;
+  const bool ok0 = r0 + g < T, ok1 = r0 + g + 8 < T;
+  const __nv_bfloat16* x0 = X + (size_t)(ok0 ? r0 + g : 0) * ldx;
+  const __nv_bfloat16* x1 = X + (size_t)(ok1 ? r0 + g + 8 : 0) * ldx;
+  float acc[2][2][4];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * ldx);
-  for (int v = lane; v < (K >> 3); v += 32) {
-    const uint4 xv = xr[v];
-    const float xf[8] = {bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y),
-                         bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w)};
+  for (int i = 0; i < 16; ++i) (&acc[0][0][0])[i] = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int jj = j & 15;
-      const __nv_bfloat16* A = j < 16 ? a0 : a1;
-      if (jj < r && A) {
-        const uint4 av = reinterpret_cast<const uint4*>(A + (size_t)jj * K)[v];
-        acc[j] += xf[0] * bf16lo(av.x) + xf[1] * bf16hi(av.x) + xf[2] * bf16lo(av.y) + xf[3] * bf16hi(av.y) +
-                  xf[4] * bf16lo(av.z) + xf[5] * bf16hi(av.z) + xf[6] * bf16lo(av.w) + xf[7] * bf16hi(av.w);
+  for (int hh = 0; hh < 2; ++hh) {
+    const LoraProjHalf& h = hh ? h1 : h0;
+    if (!h.w) continue;
+    const int ksteps = h.K >> 4;
+    const int per = (ksteps + 7) >> 3;
+    const int kb = warp * per, ke = min(ksteps, kb + per);
+#pragma unroll 4
+    for (int ks = kb; ks < ke; ++ks) {
+      const int k0 = ks << 4;
+      const int xc = h.xcol + k0 + 2 * cq;
+      uint32_t a[4];
+      a[0] = ok0 ? *reinterpret_cast<const uint32_t*>(x0 + xc) : 0u;
+      a[1] = ok1 ? *reinterpret_cast<const uint32_t*>(x1 + xc) : 0u;
+      a[2] = ok0 ? *reinterpret_cast<const uint32_t*>(x0 + xc + 8) : 0u;
+      a[3] = ok1 ? *reinterpret_cast<const uint32_t*>(x1 + xc + 8) : 0u;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int n = nt * 8 + g;
+        const uint32_t b0 = lora_w_pair(h, n, k0 + 2 * cq, r);
+        const uint32_t b1 = lora_w_pair(h, n, k0 + 8 + 2 * cq, r);
+        mma_16816_bf16(acc[hh][nt], a, b0, b1);
       }
     }
   }
 #pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j] = warp_sum(acc[j]);
-  // lane j writes column j (0..31); lanes write zeros for columns 32..63
-  float mine = 0.f;
+  for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-  for (int j = 0; j < 32; ++j)
-    if (lane == j) mine = acc[j];
-  __nv_bfloat16* ur = u_ext + (size_t)row * 64;
-  ur[lane] = __float2bfloat16_rn(s * mine);
-  ur[32 + lane] = __float2bfloat16_rn(0.f);
-}
-
-// du [T, 32] fp32 = s * [dY_q B_q | dY_v B_v] and its bf16 copy in du_ext [T, 64]
-// (columns 32..63 zero).  dY columns are read from the gradient matrix at the given
-// column offsets; B [N, r] bf16.
-__global__ void lora_du_kernel(const __nv_bfloat16* __restrict__ dy, long long ldy, int col_q, int nq,
-                               const __nv_bfloat16* __restrict__ bq, int col_v, int nv,
-                               const __nv_bfloat16* __restrict__ bv, int r, float s, float* __restrict__ du,
-                               __nv_bfloat16* __restrict__ du_ext, int T) {
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= T) return;
-  float acc[32];
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = hh * 16 + nt * 8 + 2 * cq;
+      red[warp][g][col] = acc[hh][nt][0];
+      red[warp][g][col + 1] = acc[hh][nt][1];
+      red[warp][g + 8][col] = acc[hh][nt][2];
+      red[warp][g + 8][col + 1] = acc[hh][nt][3];
+    }
+  __syncthreads();
+  for (int e = threadIdx.x; e < 16 * 32; e += 256) {
+    const int row = e >> 5, j = e & 31;
+    float v = 0.f;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-  for (int side = 0; side < 2; ++side) {
-    const __nv_bfloat16* B = side == 0 ? bq : bv;
-    if (!B) continue;
-    const int n = side == 0 ? nq : nv;
-    const __nv_bfloat16* dr = dy + (size_t)row * ldy + (side == 0 ? col_q : col_v);
-    for (int c = lane; c < n; c += 32) {
-      const float d = bf2f(dr[c]);
-      const __nv_bfloat16* br = B + (size_t)c * r;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j < r) acc[side * 16 + j] += d * bf2f(br[j]);
+    for (int w = 0; w < 8; ++w) v += red[w][row][j];
+    const int t = r0 + row;
+    if (t < T) {
+      const float sv = s * v;
+      if (out_f32) out_f32[(size_t)t * 32 + j] = sv;
+      if (out_ext) {
+        out_ext[(size_t)t * 64 + j] = __float2bfloat16_rn(sv);
+        out_ext[(size_t)t * 64 + 32 + j] = __float2bfloat16_rn(0.f);
+      }
     }
   }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) acc[j] = warp_sum(acc[j]);
-  float mine = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    if (lane == j) mine = acc[j];
-  du[(size_t)row * 32 + lane] = s * mine;
-  du_ext[(size_t)row * 64 + lane] = __float2bfloat16_rn(s * mine);
-  du_ext[(size_t)row * 64 + 32 + lane] = __float2bfloat16_rn(0.f);
 }
 
-// Partial outer products over a slice of rows:
+// Partial outer products over a slice of rows (the LoRA weight gradients dB = dY^T u
+// and dA = du^T x, reduced over tokens without atomics):
 //   part[chunk][c][j] = sum_{t in chunk} X[t, c] * U[t, j]     (c < ncols, j < 16)
-// X bf16 [T, ldx]; U given as fp32 [T, ldu] or bf16 [T, ldu].  One thread per column c.
-__global__ void lora_outer_partial_kernel(const __nv_bfloat16* __restrict__ X, long long ldx, int ncols,
-                                          const float* __restrict__ Uf, const __nv_bfloat16* __restrict__ Ub,
-                                          int ldu, int T, int rows_per_chunk, float* __restrict__ part) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+// X bf16 [T, ldx] (16-byte aligned rows, ncols % 8 == 0); U fp32 or bf16 [T, ldu].
+// A block takes 128 columns of one chunk; 32-row tiles of X and U are staged in shared
+// memory with 16-byte loads; thread (c, j-half) accumulates 8 sums in row order.
+__global__ void __launch_bounds__(256) lora_outer_partial_kernel(const __nv_bfloat16* __restrict__ X, long long ldx,
+                                                                 int ncols, const float* __restrict__ Uf,
+                                                                 const __nv_bfloat16* __restrict__ Ub, int ldu, int T,
+                                                                 int rows_per_chunk, float* __restrict__ part) {
+  __shared__ __align__(16) __nv_bfloat16 xs[32][128];
+  __shared__ __align__(16) float us[32][16];
+  const int c0 = blockIdx.x * 128;
   const int chunk = blockIdx.y;
   const int t0 = chunk * rows_per_chunk, t1 = min(T, t0 + rows_per_chunk);
-  __shared__ float su[64][16];
-  float acc[16];
+  const int cl = threadIdx.x & 127, jh = threadIdx.x >> 7;
+  float acc[8];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-  for (int tb = t0; tb < t1; tb += 64) {
-    const int nt = min(64, t1 - tb);
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+  for (int tb = t0; tb < t1; tb += 32) {
+    const int nt = min(32, t1 - tb);
     __syncthreads();
-    for (int e = threadIdx.x; e < 64 * 16; e += blockDim.x) {
+    for (int e = threadIdx.x; e < 32 * 16; e += 256) {
+      const int tt = e >> 4, v = e & 15;
+      const int col = c0 + v * 8;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (tt < nt && col < ncols) val = *reinterpret_cast<const uint4*>(X + (size_t)(tb + tt) * ldx + col);
+      *reinterpret_cast<uint4*>(&xs[tt][v * 8]) = val;
+    }
+    for (int e = threadIdx.x; e < 32 * 16; e += 256) {
       const int tt = e >> 4, j = e & 15;
       float v = 0.f;
       if (tt < nt) v = Uf ? Uf[(size_t)(tb + tt) * ldu + j] : bf2f(Ub[(size_t)(tb + tt) * ldu + j]);
-      su[tt][j] = v;
+      us[tt][j] = v;
     }
     __syncthreads();
-    if (c < ncols) {
-      for (int tt = 0; tt < nt; ++tt) {
-        const float xv = bf2f(X[(size_t)(tb + tt) * ldx + c]);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] += xv * su[tt][j];
-      }
+#pragma unroll 8
+    for (int tt = 0; tt < 32; ++tt) {
+      const float xv = bf2f(xs[tt][cl]);
+      const float4 ua = *reinterpret_cast<const float4*>(&us[tt][jh * 8]);
+      const float4 ub = *reinterpret_cast<const float4*>(&us[tt][jh * 8 + 4]);
+      acc[0] += xv * ua.x; acc[1] += xv * ua.y; acc[2] += xv * ua.z; acc[3] += xv * ua.w;
+      acc[4] += xv * ub.x; acc[5] += xv * ub.y; acc[6] += xv * ub.z; acc[7] += xv * ub.w;
     }
   }
+  const int c = c0 + cl;
   if (c < ncols) {
-    float* pp = part + ((size_t)chunk * ncols + c) * 16;
+    float* pp = part + ((size_t)chunk * ncols + c) * 16 + jh * 8;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) pp[j] = acc[j];
+    for (int j = 0; j < 8; ++j) pp[j] = acc[j];
   }
 }
 

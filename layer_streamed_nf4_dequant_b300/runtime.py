@@ -23,7 +23,7 @@ MATS = ("q", "k", "v", "o", "gate", "up", "down")
 
 
 def make_config(s, max_tokens: int = 0, max_seqs: int = 0, max_seq_len: int = 0, resident: bool = False,
-                cap_bytes: Optional[int] = None, vocab_chunk_rows: int = 0) -> ls_config:
+                cap_bytes: Optional[int] = None, vocab_chunk_rows: int = 0, dpo_shared_read: bool = False) -> ls_config:
     """ls_config from a stack shape (anything with the synth.StackConfig fields)."""
     c = ls_config()
     c.layers, c.hidden, c.heads, c.kv_heads, c.head_dim = s.layers, s.hidden, s.heads, s.kv_heads, s.head_dim
@@ -34,6 +34,7 @@ def make_config(s, max_tokens: int = 0, max_seqs: int = 0, max_seq_len: int = 0,
     c.max_seq_len = max_seq_len or s.seq_len
     c.vocab_chunk_rows = vocab_chunk_rows
     c.resident = int(resident)
+    c.dpo_shared_read = int(dpo_shared_read)
     c.cap_bytes = s.cap_bytes if cap_bytes is None else cap_bytes
     return c
 
@@ -72,10 +73,22 @@ class Stack:
     """A libls context for one stack shape, with its pinned base, adapters and buffers."""
 
     def __init__(self, s, max_tokens: int = 0, max_seqs: int = 0, max_seq_len: int = 0, resident: bool = False,
-                 cap_bytes: Optional[int] = None, vocab_chunk_rows: int = 0, device: str = "cuda:0"):
+                 cap_bytes: Optional[int] = None, vocab_chunk_rows: int = 0, device: str = "cuda:0",
+                 dpo_shared_read: Optional[bool] = None):
+        """dpo_shared_read: run DPO's policy and reference forward in one sweep of the
+        streamed layers (None: whenever the workload is DPO and the larger forward
+        workspace fits the device cap)."""
         self.s = s
         self.dev = torch.device(device)
-        self.cfg = make_config(s, max_tokens, max_seqs, max_seq_len, resident, cap_bytes, vocab_chunk_rows)
+        if dpo_shared_read is None:
+            dpo_shared_read = False
+            if getattr(s, "method", "sft") == "dpo":
+                trial = make_config(s, max_tokens, max_seqs, max_seq_len, resident, cap_bytes, vocab_chunk_rows, True)
+                n = C.c_uint64(0)
+                dpo_shared_read = lib().ls_plan(C.byref(trial), C.byref(n)) == 0
+        self.shared_read = bool(dpo_shared_read)
+        self.cfg = make_config(s, max_tokens, max_seqs, max_seq_len, resident, cap_bytes, vocab_chunk_rows,
+                               self.shared_read)
         self.ws_bytes = plan_bytes(self.cfg)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
         self.compute = torch.cuda.Stream(self.dev)
@@ -162,6 +175,21 @@ class Stack:
         head = None if s.tied else synth.weight(s, -1, "lm_head", seed)
         self.load_vocab_arrays(emb, head, synth.norm_weight(s, -1, 0, seed))
 
+    def adopt_base(self, other: "Stack"):
+        """Register another Stack's pinned host base (same shape) instead of loading a copy."""
+        if other.img_bytes != self.img_bytes or other.s.layers != self.s.layers:
+            raise ValueError("adopt_base: stack shapes differ")
+        for layer, img in enumerate(other.images):
+            self._register_layer(layer, img)
+        vb = other.vocab_bufs
+        vh = ls_vocab_host()
+        vh.embed = ls_nf4_host(vb["ep"].data_ptr(), vb["ea"].data_ptr())
+        if not self.s.tied:
+            vh.lm_head = ls_nf4_host(vb["hp"].data_ptr(), vb["ha"].data_ptr())
+        vh.final_norm = vb["fn"].data_ptr()
+        check(lib().load_vocab_nf4(self.ctx, C.byref(vh)), self.ctx)
+        self.vocab_bufs = dict(vb)
+
     # ------------------------------------------------------------------ adapters
     def set_adapter(self, layer: int, aq, bq, av, bv):
         """Bind bf16 device LoRA factors (A [r,H], B [N,r]); fp32 grads are allocated here."""
@@ -196,31 +224,51 @@ class Stack:
 
     def fwd(self, tok, cu, mask, adapter_on: bool = True, save: bool = True, sums: Optional[torch.Tensor] = None):
         nseq = cu.numel() - 1
+        self._last_rows = tok.numel()
         if sums is None:
             sums = torch.empty(nseq, dtype=torch.float32, device=self.dev)
         check(lib().stream_step_fwd(self.ctx, tok.data_ptr(), tok.numel(), nseq, cu.data_ptr(), mask.data_ptr(),
                                     int(adapter_on), int(save), sums.data_ptr()), self.ctx)
         return sums
 
-    def logprobs(self, T: int):
+    def logprobs(self, T: int = 0):
+        """Per-token logprobs and log-sum-exp of the last forward (2T rows after a
+        shared-read DPO forward: policy, then reference)."""
+        T = getattr(self, "_last_rows", T) or T
         lp = torch.empty(T, dtype=torch.float32, device=self.dev)
         lse = torch.empty(T, dtype=torch.float32, device=self.dev)
         check(lib().seq_logprobs(self.ctx, lp.data_ptr(), lse.data_ptr()), self.ctx)
         return lp, lse
 
+    def activation(self, layer: int, T: int) -> torch.Tensor:
+        """Entry `layer` (0..L) of the activation store of the last saved forward, bf16 [T, H]."""
+        out = torch.empty((T, self.s.hidden), dtype=torch.bfloat16, device=self.dev)
+        check(lib().ls_read_activation(self.ctx, layer, out.data_ptr()), self.ctx)
+        return out
+
     def bwd(self, coeffs: torch.Tensor):
         check(lib().stream_step_bwd(self.ctx, coeffs.data_ptr()), self.ctx)
 
+    def fwd_dpo(self, tok, cu, mask, pi: torch.Tensor, ref: torch.Tensor):
+        """Policy and reference forward in one sweep (needs a shared-read context)."""
+        check(lib().stream_step_fwd_dpo(self.ctx, tok.data_ptr(), tok.numel(), cu.numel() - 1, cu.data_ptr(),
+                                        mask.data_ptr(), pi.data_ptr(), ref.data_ptr()), self.ctx)
+        self._last_rows = 2 * tok.numel()
+
     def dpo_step(self, tok, cu, mask, beta: float, out: Optional[Dict] = None) -> Dict:
-        """Policy pass (adapter on, store kept), reference pass (adapter off), DPO loss, backward."""
+        """Policy pass (adapter on, store kept) and reference pass (adapter off) -- one
+        shared sweep of the layers, or two -- then the DPO loss and the backward."""
         nseq = cu.numel() - 1
         o = out if out is not None else {
             "pi": torch.empty(nseq, dtype=torch.float32, device=self.dev),
             "ref": torch.empty(nseq, dtype=torch.float32, device=self.dev),
             "loss": torch.empty(1, dtype=torch.float32, device=self.dev),
             "coeffs": torch.empty(nseq, dtype=torch.float32, device=self.dev)}
-        self.fwd(tok, cu, mask, True, True, o["pi"])
-        self.fwd(tok, cu, mask, False, False, o["ref"])
+        if self.shared_read:
+            self.fwd_dpo(tok, cu, mask, o["pi"], o["ref"])
+        else:
+            self.fwd(tok, cu, mask, True, True, o["pi"])
+            self.fwd(tok, cu, mask, False, False, o["ref"])
         check(lib().dpo_loss(self.ctx, o["pi"].data_ptr(), o["ref"].data_ptr(), nseq // 2, beta,
                              o["loss"].data_ptr(), o["coeffs"].data_ptr()), self.ctx)
         self.bwd(o["coeffs"])
@@ -237,6 +285,38 @@ class Stack:
                              o["coeffs"].data_ptr()), self.ctx)
         self.bwd(o["coeffs"])
         return o
+
+    def train_step(self, h_tokens: torch.Tensor, h_cu: torch.Tensor, h_mask: torch.Tensor, method: str,
+                   beta: float = 0.1, h_loss: Optional[torch.Tensor] = None, grads_out: Optional[torch.Tensor] = None,
+                   dev_bufs: Optional[Dict] = None) -> torch.Tensor:
+        """One SFT or DPO step from HOST (preferably pinned) token, offset and mask buffers.
+
+        Copies the batch to the device on the compute stream, runs the streamed step,
+        gathers the LoRA gradients into grads_out (zeroing the bound buffers), and
+        copies the loss back into h_loss (fp32 [1] host).  Waits for the loss before
+        returning it, like a training loop that logs every step.
+        """
+        d = dev_bufs if dev_bufs is not None else {}
+        T, n1 = h_tokens.numel(), h_cu.numel()
+        with torch.cuda.stream(self.compute):
+            if "tok" not in d or d["tok"].numel() != T or d["cu"].numel() != n1:
+                d["tok"] = torch.empty(T, dtype=torch.int32, device=self.dev)
+                d["cu"] = torch.empty(n1, dtype=torch.int32, device=self.dev)
+                d["mask"] = torch.empty(T, dtype=torch.uint8, device=self.dev)
+            d["tok"].copy_(h_tokens, non_blocking=True)
+            d["cu"].copy_(h_cu, non_blocking=True)
+            d["mask"].copy_(h_mask, non_blocking=True)
+            if method == "dpo":
+                o = self.dpo_step(d["tok"], d["cu"], d["mask"], beta, d.get("out"))
+            else:
+                o = self.sft_step(d["tok"], d["cu"], d["mask"], float(h_mask.sum().item()), d.get("out"))
+            d["out"] = o
+            check(lib().lora_grads(self.ctx, grads_out.data_ptr() if grads_out is not None else None, 1), self.ctx)
+            if h_loss is None:
+                h_loss = torch.empty(1, dtype=torch.float32, pin_memory=True)
+            h_loss.copy_(o["loss"], non_blocking=True)
+        self.compute.synchronize()
+        return h_loss
 
     def grads(self, zero_after: bool = False) -> torch.Tensor:
         flat = torch.empty(self.grad_numel(), dtype=torch.float32, device=self.dev)

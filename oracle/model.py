@@ -62,6 +62,28 @@ class pure_fp64:
         ROUND = self._old
 
 
+class accumulate_in:
+    """Context manager: run the oracle's arithmetic in another floating type (fp32).
+
+    Not a second reference: the computation and its bf16 storage points are the same,
+    only the accumulation precision drops.  Tests compare such a run with the fp64 one
+    to measure how far rounding alone moves a result (its conditioning floor) -- the
+    spread any fp32-accumulating implementation may legitimately show.  Weights and
+    adapters must be cast with cast_stack / cast_adapters inside the context.
+    """
+
+    def __init__(self, dtype=torch.float32):
+        self.dtype = dtype
+
+    def __enter__(self):
+        global F64
+        self._old, F64 = F64, self.dtype
+
+    def __exit__(self, *exc):
+        global F64
+        F64 = self._old
+
+
 def t64(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).to(F64)
 
@@ -297,6 +319,19 @@ def build_stack(cfg, seed: int = 0, synth=None) -> StackWeights:
     emb = dequant_weight(synth.weight(cfg, -1, "embed", seed))
     head = emb if cfg.tied else dequant_weight(synth.weight(cfg, -1, "lm_head", seed))
     return StackWeights(layers, emb, head, t64(synth.norm_weight(cfg, -1, 0, seed)))
+
+
+def cast_stack(sw: StackWeights, dtype) -> StackWeights:
+    """The same dequantised base in another floating type (see accumulate_in)."""
+    layers = [LayerWeights(*[getattr(l, f.name).to(dtype) for f in dataclasses.fields(LayerWeights)])
+              for l in sw.layers]
+    head = sw.lm_head.to(dtype)
+    emb = head if sw.embed is sw.lm_head else sw.embed.to(dtype)
+    return StackWeights(layers, emb, head, sw.wf.to(dtype))
+
+
+def cast_adapters(ads: List[Adapter], dtype) -> List[Adapter]:
+    return [Adapter(*[p.detach().to(dtype) for p in a.params()]) for a in ads]
 
 
 def build_adapters(cfg, seed: int = 0, synth=None, zero_b: bool = False) -> List[Adapter]:

@@ -1,0 +1,78 @@
+"""Host-side logic of bench.py (no GPU): the per-step roofline model and the
+max-over-ranks timing of a multi-process run (gloo, world size 2)."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+import synth
+
+
+def test_step_roofline_is_link_bound_for_a_slow_link():
+    s = synth.LLAMA_8B
+    layer_b = 122.7e6
+    r = bench.step_roofline_ms(s, {"slot_bytes_layer": layer_b}, s.tokens, s.nseq, s.seq_len, "dpo",
+                               tflops=1e9, link_gbs=1.0)
+    vocab_b = s.vocab * s.hidden * 0.5625
+    # three sweeps of the layers, three reads of the vocabulary head, all at 1 GB/s
+    want = (3 * s.layers * layer_b + 3 * vocab_b) / 1e9 * 1e3
+    assert r["ms"] == pytest.approx(want, rel=1e-9)
+
+
+def test_step_roofline_shared_read_saves_one_sweep():
+    s = synth.LLAMA_8B
+    layer_b = 122.7e6
+    two = bench.step_roofline_ms(s, {"slot_bytes_layer": layer_b}, s.tokens, s.nseq, s.seq_len, "dpo", 1e9, 1.0)
+    one = bench.step_roofline_ms(s, {"slot_bytes_layer": layer_b}, s.tokens, s.nseq, s.seq_len, "dpo", 1e9, 1.0,
+                                 shared_read=True)
+    vocab_b = s.vocab * s.hidden * 0.5625
+    assert two["ms"] - one["ms"] == pytest.approx((s.layers * layer_b + vocab_b) / 1e9 * 1e3, rel=1e-9)
+    assert one["flop"] == pytest.approx(two["flop"], rel=1e-12)
+
+
+def test_step_roofline_is_tensor_bound_for_an_infinite_link():
+    s = synth.QWEN_3B
+    r = bench.step_roofline_ms(s, {"slot_bytes_layer": 43.4e6}, s.tokens, s.nseq, s.seq_len, "sft",
+                               tflops=1000.0, link_gbs=1e12)
+    assert r["ms"] == pytest.approx(r["flop"] / 1e15 * 1e3, rel=1e-9)
+    # forward 2 T P per layer dominates: the step is at least 4 T P L FLOPs (fwd + dX)
+    assert r["flop"] >= 4 * s.tokens * bench.layer_params(s) * s.layers
+
+
+def test_layer_params_match_the_8b_shape():
+    # q/k/v/o + gate/up/down of one Llama-3.1-8B layer: 218.1M weights
+    assert bench.layer_params(synth.LLAMA_8B) == 218_103_808
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, ws, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(ws))
+    bench.init_dist(ws, "gloo")
+    got = bench.max_over_ranks(10.0 + rank, ws)
+    bench.barrier(ws)
+    q.put((rank, got))
+    torch.distributed.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+    assert all(p.exitcode == 0 for p in procs)
+    res = dict(q.get(timeout=5) for _ in range(2))
+    assert res == {0: 11.0, 1: 11.0}

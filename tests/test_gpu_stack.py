@@ -1,0 +1,387 @@
+"""Whole-step parity of the streamed CUDA path against the oracle, and the method's
+invariants (GPU required).
+
+What the Soup pages fix and these tests check:
+  - a streamed pass equals a resident (non-streamed) pass bit for bit (axbrief.com,
+    "Beyond Memory: The Layer Streaming Breakthrough"; the evermx.com summary's
+    Colab check);
+  - the DPO reference logprobs are the frozen base's: the same streamed weights
+    with the adapter switched off (Show HN: Fine-tune an 8B model on a 4 GB laptop
+    GPU, opening paragraph), so adapter-off = no adapter = B = 0, bit for bit;
+  - at policy = reference the DPO loss is ln 2.
+Against the oracle (normwise relative error max|gpu - oracle| / max|oracle|), stage
+by stage -- the oracle recomputes each decoder layer and the vocabulary head from the
+GPU's own stored input of it: every layer's output <= 1e-2, per-token logprobs and
+log-sum-exp <= 2e-2 absolute, and the loss from those logprobs <= 1e-2 relative.
+The whole step free-running: loss <= 1e-2 relative and LoRA gradients <= 1e-2, or
+twice the spread that rounding alone puts on them where that is larger (measured per
+case by re-running the oracle with fp32 accumulation: at two 8B-wide layers it moves
+the DPO loss by 2.6% and the gradients by 2.0%); free-running logprobs <= 2e-2 on the
+shallow stacks, where that floor is below the bound.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import layer_streamed_nf4_dequant_b300 as L
+import synth
+from oracle import model as om
+
+from gpu_util import DEV, rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL_GRAD = 1e-2
+TOL_LP = 2e-2
+TOL_LOSS = 1e-2
+
+SMALL_DPO = synth.StackConfig("tiny-dpo", layers=3, hidden=256, heads=4, kv_heads=2, head_dim=64, inter=512,
+                              vocab=1024, tied=False, rope_theta=1e4, eps=1e-6, lora_r=16, lora_alpha=32.0,
+                              seq_len=96, nseq=4, prompt_len=40, method="dpo", beta=0.1)
+
+
+def _stack(cfg, resident=False, vocab_chunk_rows=0, zero_b=False, adapters=True, **kw):
+    st = L.Stack(cfg, device="cuda:0", resident=resident, vocab_chunk_rows=vocab_chunk_rows, **kw)
+    st.load_synthetic(synth, 0)
+    if adapters:
+        st.set_adapters_synthetic(synth, 0, zero_b=zero_b)
+    return st
+
+
+def _batch(cfg, seed=0, cu=None):
+    tok = synth.tokens(cfg, seed)
+    if cu is None:
+        cu = synth.seq_offsets(cfg)
+        mask = synth.loss_mask(cfg)
+    else:
+        cu = np.asarray(cu, np.int32)
+        tok = tok[: cu[-1]]
+        mask = np.ones(cu[-1], np.uint8)
+        mask[cu[1:] - 1] = 0
+    return tok, cu, mask
+
+
+def _gpu_step(st, cfg, tok, cu, mask):
+    t, c, m = st.upload_batch(tok, cu, mask)
+    if cfg.method == "dpo":
+        o = st.dpo_step(t, c, m, cfg.beta)
+    else:
+        o = st.sft_step(t, c, m, float(mask.sum()))
+    g = st.grads(zero_after=True)
+    lp_last, lse_last = st.logprobs(len(tok))
+    assert st.sync(300000) == 0, L.last_error(st.ctx)
+    return o, g, lp_last, lse_last
+
+
+def _oracle_step(cfg, tok, cu, mask, zero_b=False):
+    sw = om.build_stack(cfg, 0, synth)
+    ads = om.build_adapters(cfg, 0, synth, zero_b=zero_b)
+    o = om.train_step(tok, cu, mask, sw, ads, cfg)
+    flat = np.concatenate([x.numpy().ravel() for layer in o["grads"] for x in layer])
+    return o, flat
+
+
+# ------------------------------------------------------------------ oracle parity
+
+# (config, vocabulary chunk rows, sequence offsets, free-running logprob check)
+PARITY = [
+    # DPO on a tiny stack, vocabulary split over several streamed chunks
+    (SMALL_DPO, 256, None, True),
+    # SFT, tied vocabulary, three ragged sequences (T = 300 is not a tile multiple)
+    (SMALL_DPO.with_(name="tiny-sft-ragged", method="sft", prompt_len=0, tied=True, nseq=3, seq_len=100),
+     512, [0, 100, 237, 300], True),
+    # two layers at the full Qwen2.5-3B widths, reduced vocabulary, SFT over 512 tokens
+    (synth.small_stack(synth.QWEN_3B, layers=2, vocab=4096, seq_len=512), 0, None, False),
+    # two layers at the full Llama-3.1-8B widths, reduced vocabulary, DPO on one pair
+    (synth.small_stack(synth.LLAMA_8B, layers=2, vocab=8192, seq_len=512, nseq=2, prompt_len=256), 0, None, False),
+]
+
+
+def _teacher_forced(st, cfg, tok, cu, mask, sw, ads, adapter_on):
+    """Run one saved forward on the GPU; recompute every layer and the vocabulary head
+    in the oracle from the GPU's own stored input of that layer.  Returns the worst
+    normwise layer-output error, the worst per-token logprob / log-sum-exp error, the
+    GPU's logprobs and the oracle's teacher-forced logprobs."""
+    t, c, m = st.upload_batch(tok, cu, mask)
+    st.fwd(t, c, m, adapter_on=adapter_on, save=True)
+    lp, lse = st.logprobs(len(tok))
+    acts = [st.activation(l, len(tok)) for l in range(cfg.layers + 1)]
+    assert st.sync(300000) == 0, L.last_error(st.ctx)
+    xs = [om.t64(a.float().cpu().numpy()) for a in acts]
+    emb = sw.embed[torch.from_numpy(tok.astype(np.int64))]
+    worst_layer = rel_err(xs[0].numpy(), emb.numpy())
+    with torch.no_grad():
+        for l in range(cfg.layers):
+            y = om.decoder_layer(xs[l], sw.layers[l], ads[l], cfg, cu, adapter_on)
+            worst_layer = max(worst_layer, rel_err(xs[l + 1].numpy(), y.numpy()))
+        hf = om.rmsnorm(xs[-1], sw.wf, cfg.eps)
+        logits = hf @ sw.lm_head.T
+        lse_o = torch.logsumexp(logits, dim=-1)
+        y = om.targets(tok, cu)
+        lp_o = np.where(y >= 0, logits.numpy()[np.arange(len(tok)), np.maximum(y, 0)] - lse_o.numpy(), 0.0)
+    lp_err = max(np.abs(to_np(lp) - lp_o).max(), np.abs(to_np(lse) - lse_o.numpy()).max())
+    return worst_layer, lp_err, lp, torch.from_numpy(lp_o)
+
+
+def _rounding_floor(cfg, tok, cu, mask, sw, ads, want):
+    """How far the oracle's own step moves when it accumulates in fp32 instead of fp64
+    (same bf16 storage points): the spread rounding alone puts on the free-running
+    loss and gradients.  Returns (relative loss spread, normwise gradient spread)."""
+    with om.accumulate_in(torch.float32):
+        o32 = om.train_step(tok, cu, mask, om.cast_stack(sw, torch.float32), om.cast_adapters(ads, torch.float32),
+                            cfg)
+    l64 = float(want["loss"])
+    g64 = np.concatenate([x.numpy().ravel() for layer in want["grads"] for x in layer])
+    g32 = np.concatenate([x.double().numpy().ravel() for layer in o32["grads"] for x in layer])
+    return abs(float(o32["loss"]) - l64) / abs(l64), rel_err(g32, g64)
+
+
+@pytest.mark.parametrize("cfg,vrows,cu,free_lp", PARITY, ids=[p[0].name for p in PARITY])
+def test_step_matches_oracle(cfg, vrows, cu, free_lp):
+    tok, cu, mask = _batch(cfg, 0, cu)
+    nseq = len(cu) - 1
+    st = _stack(cfg, vocab_chunk_rows=vrows, max_tokens=int(cu[-1]), max_seqs=nseq,
+                max_seq_len=int(np.diff(cu).max()))
+    o, g, _, _ = _gpu_step(st, cfg, tok, cu, mask)
+    sw = om.build_stack(cfg, 0, synth)
+    ads = om.build_adapters(cfg, 0, synth)
+    # 1. stage by stage: every layer and the vocabulary head from the GPU's own input
+    passes = [True, False] if cfg.method == "dpo" else [True]
+    lps, lps_o = {}, {}
+    for on in passes:
+        worst_layer, lp_err, lps[on], lps_o[on] = _teacher_forced(st, cfg, tok, cu, mask, sw, ads, on)
+        assert worst_layer <= TOL_GRAD, (on, worst_layer)
+        assert lp_err <= TOL_LP, (on, lp_err)
+    st.close()
+    # the loss from those logprobs (policy sums, reference sums, DPO / SFT)
+    if cfg.method == "dpo":
+        loss_tf = float(om.dpo_loss(om.seq_sums(lps_o[True], mask, cu), om.seq_sums(lps_o[False], mask, cu),
+                                    cfg.beta))
+    else:
+        loss_tf = float(om.sft_loss(lps_o[True], mask))
+    assert abs(o["loss"].item() - loss_tf) <= TOL_LOSS * abs(loss_tf)
+    # 2. the whole step free-running: bounded by the stated tolerance or, where bf16
+    #    storage rounding alone moves the oracle further, twice that measured spread
+    want = om.train_step(tok, cu, mask, sw, ads, cfg)
+    gflat = np.concatenate([x.numpy().ravel() for layer in want["grads"] for x in layer])
+    floor_loss, floor_grad = _rounding_floor(cfg, tok, cu, mask, sw, ads, want)
+    tol_loss, tol_grad = max(TOL_LOSS, 2 * floor_loss), max(TOL_GRAD, 2 * floor_grad)
+    assert abs(o["loss"].item() - float(want["loss"])) <= tol_loss * abs(float(want["loss"])), (floor_loss,)
+    assert rel_err(to_np(g), gflat) <= tol_grad, (floor_grad,)
+    if free_lp:
+        assert np.abs(to_np(lps[True]) - want["lp"].numpy()).max() <= TOL_LP
+        if cfg.method == "dpo":
+            assert np.abs(to_np(lps[False]) - want["lp_ref"].numpy()).max() <= TOL_LP
+    if cfg.method == "dpo":
+        # a sequence sum adds up to `count` per-token logprobs
+        count = max(int(mask[cu[i]:cu[i + 1]].sum()) for i in range(nseq))
+        assert np.abs(to_np(o["pi"]) - want["pi"].numpy()).max() <= TOL_LP * count
+        assert np.abs(to_np(o["ref"]) - want["ref"].numpy()).max() <= TOL_LP * count
+
+
+# ------------------------------------------------------------------ invariants
+
+def _run_all(st, cfg, tok, cu, mask):
+    o, g, lp_ref, lse_ref = _gpu_step(st, cfg, tok, cu, mask)
+    t, c, m = st.upload_batch(tok, cu, mask)
+    st.fwd(t, c, m, adapter_on=True, save=False)
+    lp_pol, _ = st.logprobs(len(tok))
+    assert st.sync(300000) == 0
+    return {k: v.clone() for k, v in o.items()}, g, lp_ref, lp_pol
+
+
+@pytest.mark.parametrize("vrows", [256, 0])
+def test_streamed_equals_resident_bit_exact(vrows):
+    cfg = SMALL_DPO
+    tok, cu, mask = _batch(cfg)
+    a = _stack(cfg, resident=False, vocab_chunk_rows=vrows)
+    b = _stack(cfg, resident=True, vocab_chunk_rows=vrows)
+    ra = _run_all(a, cfg, tok, cu, mask)
+    rb = _run_all(b, cfg, tok, cu, mask)
+    sa, sb = a.stats(), b.stats()
+    a.close()
+    b.close()
+    for x, y in zip(ra[1:], rb[1:]):
+        assert torch.equal(x, y)
+    for k in ("pi", "ref", "loss", "coeffs"):
+        assert torch.equal(ra[0][k], rb[0][k]), k
+    # the streamed context really streamed (a shared-read DPO step and one more forward
+    # sweep, less the layers still in a slot at each turnaround); the resident one read
+    # each layer once
+    assert sa["layer_reads"] >= 2 * cfg.layers
+    assert sb["layer_reads"] == cfg.layers
+
+
+@pytest.mark.parametrize("cfg", [SMALL_DPO, synth.small_stack(synth.LLAMA_8B, layers=2, vocab=8192, seq_len=512,
+                                                               nseq=2, prompt_len=256)], ids=["tiny", "8b-width"])
+def test_shared_read_dpo_equals_two_passes(cfg):
+    """Policy and reference forward in one sweep of the streamed layers give the same
+    sums, loss and gradients as two separate sweeps, with 2 instead of 3 layer reads."""
+    tok, cu, mask = _batch(cfg)
+    two = _stack(cfg, dpo_shared_read=False)
+    one = L.Stack(cfg, device="cuda:0", dpo_shared_read=True)
+    one.adopt_base(two)
+    one.set_adapters_synthetic(synth, 0)
+    assert one.shared_read and not two.shared_read
+    res, reads = {}, {}
+    for name, st in (("two", two), ("one", one)):
+        st.stats(reset=True)
+        o, g, lp, _ = _gpu_step(st, cfg, tok, cu, mask)
+        reads[name] = st.stats()["layer_reads"]
+        res[name] = ({k: v.clone() for k, v in o.items()}, g, lp)
+    one.close()
+    two.close()
+    (o2, g2, lp2), (o1, g1, lp1) = res["two"], res["one"]
+    T = len(tok)
+    # reference-pass logprobs: the two-pass form leaves them as its last forward
+    assert torch.equal(lp1[T:], lp2)
+    for k in ("pi", "ref", "loss", "coeffs"):
+        assert torch.equal(o1[k], o2[k]), k
+    assert torch.equal(g1, g2)
+    assert reads["two"] >= 3 * cfg.layers - 2 and reads["one"] <= 2 * cfg.layers
+
+
+def test_repeat_step_is_deterministic():
+    cfg = SMALL_DPO
+    tok, cu, mask = _batch(cfg)
+    st = _stack(cfg, vocab_chunk_rows=256)
+    r1 = _run_all(st, cfg, tok, cu, mask)
+    r2 = _run_all(st, cfg, tok, cu, mask)
+    st.close()
+    for x, y in zip(r1[1:], r2[1:]):
+        assert torch.equal(x, y)
+    assert torch.equal(r1[0]["loss"], r2[0]["loss"])
+
+
+def test_adapter_off_equals_base_and_zero_b():
+    cfg = SMALL_DPO
+    tok, cu, mask = _batch(cfg)
+    base = _stack(cfg, adapters=False)
+    zb = _stack(cfg, zero_b=True)
+    on = _stack(cfg)
+    t, c, m = base.upload_batch(tok, cu, mask)
+    base.fwd(t, c, m, adapter_on=True, save=False)
+    lp_base, lse_base = base.logprobs(len(tok))
+    res = {}
+    for name, st in (("zb", zb), ("on", on)):
+        t2, c2, m2 = st.upload_batch(tok, cu, mask)
+        st.fwd(t2, c2, m2, adapter_on=False, save=False)
+        res[name + "_off"] = st.logprobs(len(tok))[0]
+        st.fwd(t2, c2, m2, adapter_on=True, save=False)
+        res[name + "_on"] = st.logprobs(len(tok))[0]
+    for st in (base, zb, on):
+        assert st.sync(60000) == 0
+        st.close()
+    assert torch.equal(res["on_off"], lp_base)      # reference pass = frozen base
+    assert torch.equal(res["zb_off"], lp_base)
+    assert torch.equal(res["zb_on"], lp_base)       # B = 0 adds exact zeros
+    assert not torch.equal(res["on_on"], lp_base)   # a real adapter changes the policy
+
+
+def test_dpo_loss_is_ln2_at_policy_equals_reference():
+    cfg = SMALL_DPO
+    tok, cu, mask = _batch(cfg)
+    st = _stack(cfg, zero_b=True)
+    o, g, _, _ = _gpu_step(st, cfg, tok, cu, mask)
+    st.close()
+    assert torch.equal(o["pi"], o["ref"])
+    assert o["loss"].item() == pytest.approx(math.log(2.0), rel=1e-6)
+    # dL/dB = -beta sigma(0) ... != 0 while dL/dA = 0 exactly (B = 0 blocks it)
+    gn = to_np(g)
+    r, H = cfg.lora_r, cfg.hidden
+    per = 2 * r * H + r * (cfg.n_q + cfg.n_kv)
+    for l in range(cfg.layers):
+        blk = gn[l * per:(l + 1) * per]
+        a_q = blk[: r * H]
+        b_q = blk[r * H: r * H + cfg.n_q * r]
+        assert np.all(a_q == 0.0)
+        assert np.abs(b_q).max() > 0.0
+
+
+def test_sft_loss_counts_and_sequence_sums():
+    cfg = SMALL_DPO.with_(name="tiny-sft", method="sft", prompt_len=0)
+    tok, cu, mask = _batch(cfg)
+    st = _stack(cfg)
+    o, _, lp, _ = _gpu_step(st, cfg, tok, cu, mask)
+    st.close()
+    lpn = to_np(lp)
+    sums = [lpn[cu[i]:cu[i + 1]][mask[cu[i]:cu[i + 1]] > 0].sum() for i in range(cfg.nseq)]
+    assert np.allclose(to_np(o["sums"]), sums, rtol=1e-5, atol=1e-3)
+    assert o["loss"].item() == pytest.approx(-sum(sums) / mask.sum(), rel=1e-5)
+    # last position of every sequence has no target
+    assert np.all(lpn[cu[1:] - 1] == 0.0)
+
+
+def test_bounded_sync_gives_up_on_a_slow_copy():
+    """A host-side delay in the copy path makes ls_sync's time limit run out (no GPU fault)."""
+    cfg = SMALL_DPO
+    tok, cu, mask = _batch(cfg)
+    st = _stack(cfg)
+    t, c, m = st.upload_batch(tok, cu, mask)
+    assert st.sync(60000) == 0
+    L.check(L.lib().ls_debug_copy_delay(st.ctx, 300), st.ctx)
+    st.fwd(t, c, m, adapter_on=True, save=False)
+    assert st.sync(50) == L.LS_ERR_TIMEOUT
+    L.check(L.lib().ls_debug_copy_delay(st.ctx, 0), st.ctx)
+    assert st.sync(120000) == 0
+    st.close()
+
+
+def test_state_errors_are_reported():
+    cfg = SMALL_DPO
+    st = _stack(cfg)
+    coeffs = torch.zeros(cfg.nseq, dtype=torch.float32, device=DEV)
+    rc = L.lib().stream_step_bwd(st.ctx, coeffs.data_ptr())
+    assert rc == L.LS_ERR_STATE
+    assert "no forward" in L.last_error(st.ctx)
+    # errors are sticky on the context
+    assert L.lib().lora_grads(st.ctx, None, 0) == L.LS_ERR_STATE
+    st.close()
+
+
+def test_unpinned_layer_memory_is_refused():
+    cfg = SMALL_DPO
+    st = L.Stack(cfg, device="cuda:0")
+    buf = np.zeros(st.img_bytes, np.uint8)   # pageable host memory
+    lh = L.ls_layer_host()
+    base = buf.ctypes.data
+    for i, n in enumerate(("q", "k", "v", "o", "gate", "up", "down")):
+        setattr(lh, n, L.ls_nf4_host(base + st.offs[i], base + st.offs[7 + i]))
+    lh.attn_norm = base + st.offs[14]
+    lh.mlp_norm = base + st.offs[15]
+    import ctypes as C
+    rc = L.lib().load_layer_nf4(st.ctx, 0, C.byref(lh))
+    assert rc == L.LS_ERR_ARG
+    assert "not pinned" in L.last_error(st.ctx)
+    st.close()
+
+
+# ------------------------------------------------------------------ full sizes
+
+@pytest.mark.slow
+def test_llama8b_full_streamed_equals_resident_and_ln2():
+    """The full 32-layer Llama-3.1-8B-shaped DPO step, in the bench's launch
+    configuration: streamed = resident bit for bit; B = 0 gives ln 2."""
+    cfg = synth.LLAMA_8B
+    tok, cu, mask = _batch(cfg)
+    a = _stack(cfg)
+    ra = _run_all(a, cfg, tok, cu, mask)
+    sa = a.stats()
+    # same Stack, adapters with B = 0
+    a.set_adapters_synthetic(synth, 0, zero_b=True)
+    o0, _, _, _ = _gpu_step(a, cfg, tok, cu, mask)
+    a.set_adapters_synthetic(synth, 0)
+    b = L.Stack(cfg, device="cuda:0", resident=True)
+    b.adopt_base(a)                          # the same pinned host images
+    b.set_adapters_synthetic(synth, 0)
+    rb = _run_all(b, cfg, tok, cu, mask)
+    b.close()
+    a.close()
+    for x, y in zip(ra[1:], rb[1:]):
+        assert torch.equal(x, y)
+    assert torch.equal(ra[0]["loss"], rb[0]["loss"])
+    assert np.isfinite(to_np(ra[1])).all() and np.abs(to_np(ra[1])).max() > 0
+    assert o0["loss"].item() == pytest.approx(math.log(2.0), rel=1e-6)
+    assert sa["layer_reads"] >= 2 * cfg.layers

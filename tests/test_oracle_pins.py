@@ -414,3 +414,23 @@ def test_causality_and_sequence_independence():
     # sequence 1 run alone gives the same logprobs as inside the two-sequence pass
     alone = M.stack_forward(tok[6:], [0, 6], sw, ads, cfg)["lp"].detach().numpy()
     np.testing.assert_array_equal(alone, base[6:])
+
+
+def test_accumulate_in_fp32_computes_the_same_step():
+    """The fp32-accumulation mode (used to measure rounding floors) is the same
+    computation: on a tiny stack without bf16 storage it matches fp64 to fp32 accuracy,
+    and the context restores fp64 afterwards."""
+    cfg = TINY.with_(method="dpo", prompt_len=2)
+    sw, ads = _tiny(cfg)
+    tok, cu, mask = synth.tokens(cfg), synth.seq_offsets(cfg), synth.loss_mask(cfg)
+    with M.pure_fp64():
+        o64 = M.train_step(tok, cu, mask, sw, ads, cfg)
+        with M.accumulate_in(torch.float32):
+            o32 = M.train_step(tok, cu, mask, M.cast_stack(sw, torch.float32),
+                               M.cast_adapters(ads, torch.float32), cfg)
+            assert o32["lp"].dtype == torch.float32
+    assert M.t64(np.zeros(2)).dtype == F64
+    assert float(o32["loss"]) == pytest.approx(float(o64["loss"]), rel=1e-5)
+    g64 = torch.cat([g.ravel() for l in o64["grads"] for g in l])
+    g32 = torch.cat([g.ravel().double() for l in o32["grads"] for g in l])
+    assert float((g32 - g64).abs().max() / g64.abs().max()) < 1e-4
