@@ -406,6 +406,44 @@ def run_gpu_arm(args, s, ws, rank, local):
     return res
 
 
+def gemm_microbench(spec: str, reps: int = 10) -> dict:
+    """One NF4-dequant-fused matrix product through the C ABI (lsk_nf4_gemm), timed with
+    CUDA events after warm-up: spec = "mode,M,N,K[,bn,nacc]" (mode 0: Y = X deq(W)^T,
+    mode 1: dX = dY deq(W); W [N, K] drawn N(0, 0.02) and NF4-quantised on the host)."""
+    import layer_streamed_nf4_dequant_b300 as L
+    f = [int(x) for x in spec.split(",")]
+    mode, M, N, K = f[:4]
+    bn, nacc = (f[4], f[5]) if len(f) >= 6 else (0, 0)
+    dev = torch.device("cuda:0")
+    g = torch.Generator().manual_seed(0)
+    pk, am = L.quantize_host((torch.randn(N, K, generator=g) * 0.02).numpy())
+    p, a = torch.from_numpy(pk).to(dev), torch.from_numpy(am).to(dev)
+    red, outc = (K, N) if mode == 0 else (N, K)
+    x = torch.randn(M, red, device=dev).to(torch.bfloat16)
+    out = torch.empty(M, outc, device=dev, dtype=torch.bfloat16 if mode == 0 else torch.float32)
+    st = torch.cuda.current_stream().cuda_stream
+
+    def run():
+        L.call("lsk_nf4_gemm", mode, x, red, M, p, a, N, K, None, None, 0, 0 if mode == 0 else 1, out, outc, None, 0,
+               bn, nacc, st)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    peaks = read_peaks()
+    tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+    return {"kernel": "nf4_gemm", "mode": mode, "M": M, "N": N, "K": K, "bn": bn, "nacc": nacc,
+            "us": round(us, 2), "tflops": round(tf, 1), "frac_of_burst_peak": round(tf / peaks["bf16_tflops"], 4),
+            "peak_source": peaks["source"]}
+
+
 def cpu_baseline(s, seconds_budget: float = 20.0):
     tok, cu, mask = synth.tokens(s), synth.seq_offsets(s), synth.loss_mask(s)
     _, prep = oracle_sample(s, 0, 0, tok, cu, mask, None)   # warm-up (and weight preparation)
@@ -429,7 +467,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="llama-3.1-8b", choices=sorted(synth.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm", default=None, help="micro-benchmark one NF4 GEMM: mode,M,N,K[,bn,nacc]")
     args = ap.parse_args()
+    if args.gemm:
+        print(json.dumps(gemm_microbench(args.gemm, max(1, args.steps))), flush=True)
+        return
     if args.warmup < 3:
         args.warmup = 3
     s = synth.CONFIGS[args.config]

@@ -83,9 +83,21 @@ static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Pick the tile shape with the fewest tile-waves over 148 SMs, ties to the larger tile.
+// Pick the tile shape.  Each CTA dequantises its BN x 64 weight tile once per k-step
+// and the shared-memory traffic of that dequantisation is what limits the kernel, so
+// above 128 rows two accumulators (BM = 256) always pay: they halve the dequant work
+// per MMA FLOP (measured 1.4-1.5x faster at every 8B-shape product).  Between BN = 128
+// and 256 the fewer-waves tile wins (per-CTA time ~ BN), ties to BN = 256.
 static void choose_tile(int M, int Nout, int& nacc, int& bn) {
   const int sms = 148;
+  if (M > 128) {
+    nacc = 2;
+    const long long mt = (M + 255) / 256;
+    const long long w256 = (mt * ((Nout + 255) / 256) + sms - 1) / sms;
+    const long long w128 = (mt * ((Nout + 127) / 128) + sms - 1) / sms;
+    bn = (w128 * 128 < w256 * 256) ? 128 : 256;
+    return;
+  }
   struct Opt { int nacc, bn, per_sm; } opts[4] = {{2, 256, 1}, {2, 128, 1}, {1, 256, 1}, {1, 128, 2}};
   double best = 1e30;
   for (auto& o : opts) {

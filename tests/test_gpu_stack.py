@@ -385,3 +385,28 @@ def test_llama8b_full_streamed_equals_resident_and_ln2():
     assert np.isfinite(to_np(ra[1])).all() and np.abs(to_np(ra[1])).max() > 0
     assert o0["loss"].item() == pytest.approx(math.log(2.0), rel=1e-6)
     assert sa["layer_reads"] >= 2 * cfg.layers
+
+
+def test_tiny_dpo_step_matches_golden():
+    """The GPU step against the oracle-written fixture of tests/golden/ (same bounds)."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tiny_dpo_step.json")))
+    c = g["config"]
+    cfg = synth.StackConfig("golden-tiny-dpo", **c)
+    tok, cu, mask = _batch(cfg)
+    st = _stack(cfg)
+    o, grads, _, _ = _gpu_step(st, cfg, tok, cu, mask)
+    st.close()
+    assert abs(o["loss"].item() - g["loss"]) <= TOL_LOSS * abs(g["loss"])
+    count = int(mask[: cu[1]].sum())
+    assert np.abs(to_np(o["pi"]) - np.array(g["pi"])).max() <= TOL_LP * count
+    gn = to_np(grads)
+    r, H = cfg.lora_r, cfg.hidden
+    sizes = [r * H, cfg.n_q * r, r * H, cfg.n_kv * r]
+    off = 0
+    for layer in range(cfg.layers):
+        for i, n in enumerate(sizes):
+            norm = np.linalg.norm(gn[off: off + n])
+            assert norm == pytest.approx(g["grad_norms"][layer][i], rel=TOL_GRAD * 5)
+            off += n

@@ -434,3 +434,29 @@ def test_accumulate_in_fp32_computes_the_same_step():
     g64 = torch.cat([g.ravel() for l in o64["grads"] for g in l])
     g32 = torch.cat([g.ravel().double() for l in o32["grads"] for g in l])
     assert float((g32 - g64).abs().max() / g64.abs().max()) < 1e-4
+
+
+# ------------------------------------------------------------------ golden fixtures
+
+GOLDEN = __import__("os").path.join(__import__("os").path.dirname(__file__), "golden")
+
+
+def test_nf4_table_matches_published_fixture():
+    vals = [float(l) for l in open(f"{GOLDEN}/nf4_table.txt") if l.strip() and not l.startswith("#")]
+    np.testing.assert_array_equal(oracle.NF4_TABLE, np.array(vals, np.float32))
+
+
+def test_oracle_reproduces_tiny_dpo_golden():
+    import json
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("make_golden", f"{GOLDEN}/make_golden.py")
+    mg = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mg)
+    want = json.load(open(f"{GOLDEN}/tiny_dpo_step.json"))
+    got = mg.tiny_dpo_step()
+    assert got["config"] == want["config"]
+    assert got["loss"] == pytest.approx(want["loss"], rel=1e-12)
+    np.testing.assert_allclose(got["pi"], want["pi"], rtol=1e-12)
+    np.testing.assert_allclose(got["ref"], want["ref"], rtol=1e-12)
+    np.testing.assert_allclose(got["grad_norms"], want["grad_norms"], rtol=1e-10)
+    np.testing.assert_allclose(got["grad_head"], want["grad_head"], rtol=1e-9, atol=1e-15)
