@@ -106,6 +106,32 @@ int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* u
                    int32_t ldu, int32_t r, int32_t T, int32_t layout, int32_t accumulate, float* scratch,
                    int32_t rows_per_chunk, float* out, void* stream);
 
+/* Size (fp32 elements) of the fixed scratch of lsk_lora_outer_noalloc: 2^21 floats
+ * (8 MiB).  A call needs ceil(T / rows_per_chunk) * ncols * 16 of them. */
+#define LS_OUTER_NOALLOC_SCRATCH_FLOATS 2097152
+
+/* lsk_lora_outer for callers that cannot allocate device memory: the same
+ * deterministic outer product over tokens (same arguments minus `scratch`, same
+ * result bit for bit), with its partial sums kept in a fixed array inside the
+ * library instead of caller scratch.  Meant for code that runs where cudaMalloc is
+ * off limits -- inside a host framework whose memory pool owns all device memory,
+ * or on a path that must not take cudaMalloc's implicit device synchronisation.  The
+ * Soup pages have no counterpart; this is a library-usage convenience.
+ *  - The array (LS_OUTER_NOALLOC_SCRATCH_FLOATS floats) is part of the library image:
+ *    every GPU that loads the library holds it until the process exits.
+ *  - The first call on a device looks the array's device address up (with that
+ *    device current) and caches it; make that first call before any stream capture.
+ *  - Every call on a device shares the one array and it keeps the last call's
+ *    contents; each call writes every element it later reads, so nothing needs
+ *    clearing.  Calls whose kernels overlap on the GPU (e.g. on two streams) race on
+ *    the array: serialise them.
+ *  - Sizes beyond the array (ceil(T / rows_per_chunk) * ncols * 16 floats) return
+ *    LS_ERR_ARG with a message; nothing is launched.  No call allocates or frees
+ *    device memory. */
+int lsk_lora_outer_noalloc(const uint16_t* X, int64_t ldx, int32_t ncols, const float* u_f32, const uint16_t* u_bf16,
+                           int32_t ldu, int32_t r, int32_t T, int32_t layout, int32_t accumulate,
+                           int32_t rows_per_chunk, float* out, void* stream);
+
 /* Extra-stage operands built from the adapter: B_ext [N, 64] (q rows [q0, q0+nq)
  * take B_q in columns 0..r-1, v rows [v0, v0+nv) take B_v in columns 16..16+r-1)
  * and A_ext [K, 64] (row k = [A_q[:, k] | A_v[:, k] | 0]). */

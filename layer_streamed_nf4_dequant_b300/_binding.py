@@ -106,6 +106,7 @@ _SIGS = {
     "lsk_lora_down": [P, I64, P, P, I32, I32, F32, P, I32, P],
     "lsk_lora_du": [P, I64, I32, I32, P, I32, I32, P, I32, F32, P, P, I32, P],
     "lsk_lora_outer": [P, I64, I32, P, P, I32, I32, I32, I32, I32, P, I32, P, P],
+    "lsk_lora_outer_noalloc": [P, I64, I32, P, P, I32, I32, I32, I32, I32, I32, P, P],
     "lsk_build_ext_fwd": [P, I32, I32, P, I32, I32, I32, I32, P, P],
     "lsk_build_ext_bwd": [P, P, I32, I32, P, P],
     "lsk_embed_gather": [P, P, P, P, I32, I32, P],

@@ -16,6 +16,7 @@
 #include <cstdio>
 #include <cstring>
 #include <functional>
+#include <mutex>
 #include <string>
 #include <thread>
 #include <vector>
@@ -1559,6 +1560,55 @@ int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* u
   if (!X || (!uf && !ub) || !scratch || !out || r < 1 || r > 16 || ncols < 1 || ncols % 8 || ldx % 8 ||
       (reinterpret_cast<uintptr_t>(X) & 15) || T < 1 || rpc < 1 || (layout != 0 && layout != 1))
     return set_thread_err(LS_ERR_ARG, "lsk_lora_outer: bad args");
+  KCK(lora_outer(reinterpret_cast<const bf16*>(X), ldx, ncols, uf, reinterpret_cast<const bf16*>(ub), ldu, r, T,
+                 layout, accumulate, scratch, rpc, out, STREAM(s)));
+  return LS_OK;
+}
+
+}  // extern "C"
+
+// Partial sums of lsk_lora_outer_noalloc: a fixed array in the library image (no
+// allocation at run time).  Host code must not use the symbol as an address: its
+// device address comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) float g_outer_noalloc_scratch[LS_OUTER_NOALLOC_SCRATCH_FLOATS];
+
+namespace {
+std::mutex g_noalloc_mu;
+constexpr int kMaxDevices = 256;
+float* g_noalloc_addr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" {
+
+int lsk_lora_outer_noalloc(const uint16_t* X, int64_t ldx, int32_t ncols, const float* uf, const uint16_t* ub,
+                           int32_t ldu, int32_t r, int32_t T, int32_t layout, int32_t accumulate, int32_t rpc,
+                           float* out, void* s) {
+  if (!X || (!uf && !ub) || !out || r < 1 || r > 16 || ncols < 1 || ncols % 8 || ldx % 8 ||
+      (reinterpret_cast<uintptr_t>(X) & 15) || T < 1 || rpc < 1 || (layout != 0 && layout != 1))
+    return set_thread_err(LS_ERR_ARG, "lsk_lora_outer_noalloc: bad args");
+  const long long need = (long long)((T + rpc - 1) / rpc) * ncols * 16;
+  if (need > (long long)LS_OUTER_NOALLOC_SCRATCH_FLOATS) {
+    char b[200];
+    snprintf(b, sizeof b, "lsk_lora_outer_noalloc: needs %lld scratch floats (ceil(T/rows_per_chunk)*ncols*16), "
+             "more than the fixed %d", need, (int)LS_OUTER_NOALLOC_SCRATCH_FLOATS);
+    return set_thread_err(LS_ERR_ARG, b);
+  }
+  int dev = -1;
+  KCK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return set_thread_err(LS_ERR_ARG, "lsk_lora_outer_noalloc: device ordinal out of range");
+  float* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_outer_noalloc_scratch);
+      if (e != cudaSuccess || !p)
+        return set_thread_err(LS_ERR_CUDA, std::string("lsk_lora_outer_noalloc: cudaGetSymbolAddress: ") +
+                                               cudaGetErrorString(e));
+      g_noalloc_addr[dev] = reinterpret_cast<float*>(p);
+    }
+    scratch = g_noalloc_addr[dev];
+  }
   KCK(lora_outer(reinterpret_cast<const bf16*>(X), ldx, ncols, uf, reinterpret_cast<const bf16*>(ub), ldu, r, T,
                  layout, accumulate, scratch, rpc, out, STREAM(s)));
   return LS_OK;
