@@ -176,11 +176,12 @@ def step_roofline_ms(s, stats, T, nseq, seq_len, method, tflops, link_gbs, share
     V, H = s.vocab, s.hidden
     vocab_fwd = 2.0 * T * V * H
     vocab_b = V * H * NF4_BYTES_PER_PARAM
-    sweeps_fwd = [True, False] if method == "dpo" else [True]
+    needs_ref = method in ("dpo", "kto")
+    sweeps_fwd = [True, False] if needs_ref else [True]
     t = 0.0
     pk = tflops * 1e12
     bw = link_gbs * 1e9
-    if method == "dpo" and shared_read:
+    if needs_ref and shared_read:
         t += s.layers * max((2 * f_fwd + lora_f) / pk, layer_b / bw)
         t += max(2 * vocab_fwd / pk, vocab_b / bw)
     else:
@@ -236,13 +237,15 @@ def oracle_sample(s, seed: int, layer: int, T_tokens, cu, mask, prep=None):
         p.grad = None
     xin = x.clone().requires_grad_(True)
     y = om.decoder_layer(xin, lw, ad, s, cu, adapter_on=True)
-    with torch.no_grad():
-        om.decoder_layer(x, lw, ad, s, cu, adapter_on=False)
+    if s.method in ("dpo", "kto"):
+        with torch.no_grad():
+            om.decoder_layer(x, lw, ad, s, cu, adapter_on=False)
     hf = x.clone().requires_grad_(True)
     logits = hf @ head.T
     lse = torch.logsumexp(logits, dim=-1)
-    with torch.no_grad():
-        torch.logsumexp(x @ head.T, dim=-1)
+    if s.method in ("dpo", "kto"):
+        with torch.no_grad():
+            torch.logsumexp(x @ head.T, dim=-1)
     (y.sum() * 1e-3 + lse.sum() * 1e-3).backward()
     dt = time.perf_counter() - t0
     return dt, prep
@@ -286,10 +289,10 @@ def run_gpu_arm(args, s, ws, rank, local):
 
     def step():
         nonlocal out
-        if s.method == "dpo":
-            out = st.dpo_step(tok, cu, mask, s.beta, out)
-        else:
+        if s.method == "sft":
             out = st.sft_step(tok, cu, mask, float(mask_np.sum()), out)
+        else:
+            out = st.pref_step(s.method, tok, cu, mask, out)
         L.check(L.lib().lora_grads(st.ctx, flat.data_ptr(), 1), st.ctx)
 
     for _ in range(args.warmup):
@@ -466,6 +469,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="llama-3.1-8b", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--method", default=None, choices=["sft", "dpo", "simpo", "orpo", "kto"],
+                    help="training method on the config's pairs (default: the config's own)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm", default=None, help="micro-benchmark one NF4 GEMM: mode,M,N,K[,bn,nacc]")
     args = ap.parse_args()
@@ -475,6 +480,8 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     s = synth.CONFIGS[args.config]
+    if args.method and args.method != s.method:
+        s = s.with_(method=args.method, prompt_len=0 if args.method == "sft" else s.prompt_len)
     ws, rank, local = dist_env()
 
     if args.impl == "reference":

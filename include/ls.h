@@ -187,6 +187,30 @@ int dpo_loss(ls_ctx* ctx, const float* d_pi, const float* d_ref, int32_t npairs,
 int sft_loss(ls_ctx* ctx, const float* d_seq_sums, int32_t nseq, float count, float* d_loss,
              float* d_coeffs);
 
+/* Reference-free preference losses over npairs (chosen, rejected) pairs laid out
+ * pairwise, from the policy sequence sums d_pi [2 npairs] of stream_step_fwd; the
+ * response lengths |y| are the counts of selected positions of d_loss_mask in each
+ * sequence (d_seq_offsets [2 npairs + 1]).  The pages list SimPO and ORPO among the
+ * methods run over the streamed base (axbrief.com, "The Architecture of Low-VRAM
+ * Alignment"; evermx.com summary); the formulas are the methods' own:
+ *  SimPO (Meng et al. 2024): loss = mean softplus(-(beta (pi_c/|c| - pi_r/|r|) - gamma));
+ *  ORPO (Hong et al. 2024): loss = mean [ -pi_c/|c| + lambda softplus(-(lo_c - lo_r)) ],
+ *    lo = l - log(1 - e^l) the log odds of the mean logprob l = pi/|y|.
+ * d_loss [1]; d_coeffs [2 npairs] = dL/d(sequence sum) for stream_step_bwd.  Neither
+ * needs a reference pass. */
+int simpo_loss(ls_ctx* ctx, const float* d_pi, const int32_t* d_seq_offsets, const uint8_t* d_loss_mask,
+               int32_t npairs, float beta, float gamma, float* d_loss, float* d_coeffs);
+int orpo_loss(ls_ctx* ctx, const float* d_pi, const int32_t* d_seq_offsets, const uint8_t* d_loss_mask,
+              int32_t npairs, float lambda, float* d_loss, float* d_coeffs);
+
+/* KTO (Ethayarajh et al. 2024; listed on the pages beside DPO) over nseq labelled
+ * sequences: r = pi - ref, reference point z0 = max(0, mean r) (held constant for the
+ * gradient), loss = mean of lambda_d (1 - sigmoid(beta (r - z0))) over desirable and
+ * lambda_u (1 - sigmoid(beta (z0 - r))) over undesirable sequences.  d_desirable
+ * uint8 [nseq] (NULL: pair data, even sequences desirable).  d_coeffs [nseq]. */
+int kto_loss(ls_ctx* ctx, const float* d_pi, const float* d_ref, const uint8_t* d_desirable, int32_t nseq,
+             float beta, float lambda_d, float lambda_u, float* d_loss, float* d_coeffs);
+
 /* Streamed backward of the last saved forward: vocabulary head chunks, then layers
  * L-1..0, each re-streamed and recomputed from its stored input.  d_seq_coeffs
  * [nseq]: dL/d(sequence logprob sum).  LoRA gradients are added (+=) into the bound

@@ -84,6 +84,9 @@ _SIGS = {
     "seq_logprobs": [P, P, P],
     "dpo_loss": [P, P, P, I32, F32, P, P],
     "sft_loss": [P, P, I32, F32, P, P],
+    "simpo_loss": [P, P, P, P, I32, F32, F32, P, P],
+    "orpo_loss": [P, P, P, P, I32, F32, P, P],
+    "kto_loss": [P, P, P, P, I32, F32, F32, F32, P, P],
     "stream_step_bwd": [P, P],
     "lora_grads": [P, P, I32],
     "ls_sync": [P, I32],

@@ -156,7 +156,21 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   d |= (uint64_t)2 << 61;                        // 128-byte swizzle
   return d;
 }
-// Instruction descriptor: bf16 A/B (K-major), fp32 D, M x N tile.
+// Descriptor for an MN-major operand with the 128-byte swizzle: atoms of 64 MN
+// elements (128 B) x 8 K-rows (1 KB), 8-row groups 1024 B apart along K (stride byte
+// offset), 64-element MN blocks `mn_block_bytes` apart (leading byte offset).  Tile
+// base 1024-byte aligned; advancing K by 16 adds 2048 B.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);          // start address
+  d |= (uint64_t)((mn_block_bytes >> 4) & 0x3FFF) << 16;   // leading byte offset: next 64 MN elements
+  d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset: next 8 K-rows
+  d |= (uint64_t)1 << 46;                           // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor: bf16 A/B (K-major), fp32 D, M x N tile.  Bit 16 set = B
+// MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }

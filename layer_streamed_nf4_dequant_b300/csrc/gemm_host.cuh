@@ -83,19 +83,24 @@ static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Pick the tile shape.  Each CTA dequantises its BN x 64 weight tile once per k-step
-// and the shared-memory traffic of that dequantisation is what limits the kernel, so
-// above 128 rows two accumulators (BM = 256) always pay: they halve the dequant work
+// Pick the tile shape.  Each CTA dequantises its BN x 64 weight tile once per k-step,
+// so above 128 rows two accumulators (BM = 256) always pay: they halve the dequant work
 // per MMA FLOP (measured 1.4-1.5x faster at every 8B-shape product).  Between BN = 128
-// and 256 the fewer-waves tile wins (per-CTA time ~ BN), ties to BN = 256.
-static void choose_tile(int M, int Nout, int& nacc, int& bn) {
+// and 256 the tile with the lower (waves x per-CTA time) wins.  Per-CTA time relative
+// to BN = 256, measured on the 8B shapes: forward (register-table dequant, one thread
+// per row, BN = 128 tiles alternate k-steps between two halves of the dequant warps)
+// 0.76; input gradient (shared-memory table dequant) 0.5.  Ties go to BN = 256 for the
+// forward and to BN = 128 for the input gradient (measured).
+static void choose_tile(int mode, int M, int Nout, int& nacc, int& bn) {
   const int sms = 148;
   if (M > 128) {
     nacc = 2;
     const long long mt = (M + 255) / 256;
     const long long w256 = (mt * ((Nout + 255) / 256) + sms - 1) / sms;
     const long long w128 = (mt * ((Nout + 127) / 128) + sms - 1) / sms;
-    bn = (w128 * 128 < w256 * 256) ? 128 : 256;
+    const double t128 = mode == GEMM_FWD ? 0.76 : 0.5;
+    const double c128 = (double)w128 * t128, c256 = (double)w256;
+    bn = (mode == GEMM_FWD ? c128 < c256 - 1e-9 : c128 <= c256 + 1e-9) ? 128 : 256;
     return;
   }
   struct Opt { int nacc, bn, per_sm; } opts[4] = {{2, 256, 1}, {2, 128, 1}, {1, 256, 1}, {1, 128, 2}};
@@ -115,7 +120,7 @@ static void choose_tile(int M, int Nout, int& nacc, int& bn) {
 static cudaError_t launch_nf4_gemm(const GemmCall& c, cudaStream_t st) {
   const GemmArgs& g = c.g;
   int nacc = 0, bn = 0;
-  choose_tile(g.M, g.Nout, nacc, bn);
+  choose_tile(c.mode, g.M, g.Nout, nacc, bn);
   if (c.force_bn) bn = c.force_bn;
   if (c.force_nacc) nacc = c.force_nacc;
   if (c.mode == GEMM_FWD) {

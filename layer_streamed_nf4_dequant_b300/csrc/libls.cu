@@ -1226,6 +1226,41 @@ int sft_loss(ls_ctx* c, const float* d_sums, int32_t nseq, float count, float* d
   return LS_OK;
 }
 
+int simpo_loss(ls_ctx* c, const float* d_pi, const int32_t* d_cu, const uint8_t* d_mask, int32_t npairs, float beta,
+               float gamma, float* d_loss, float* d_coeffs) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!d_pi || !d_cu || !d_mask || npairs < 1) return fail(c, LS_ERR_ARG, "simpo_loss: bad arguments");
+  const int n = 2 * npairs;
+  TIMED(LS_K_OTHER, 0, 16.0 * n, 1,
+        ls::pref_loss_kernel<<<1, 256, n * sizeof(float), c->cs>>>(ls::PREF_SIMPO, d_pi, nullptr, d_cu, d_mask, nullptr,
+                                                                   n, beta, gamma, 0.f, d_loss, d_coeffs));
+  return LS_OK;
+}
+
+int orpo_loss(ls_ctx* c, const float* d_pi, const int32_t* d_cu, const uint8_t* d_mask, int32_t npairs, float lambda,
+              float* d_loss, float* d_coeffs) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!d_pi || !d_cu || !d_mask || npairs < 1) return fail(c, LS_ERR_ARG, "orpo_loss: bad arguments");
+  const int n = 2 * npairs;
+  TIMED(LS_K_OTHER, 0, 16.0 * n, 1,
+        ls::pref_loss_kernel<<<1, 256, n * sizeof(float), c->cs>>>(ls::PREF_ORPO, d_pi, nullptr, d_cu, d_mask, nullptr,
+                                                                   n, 0.f, lambda, 0.f, d_loss, d_coeffs));
+  return LS_OK;
+}
+
+int kto_loss(ls_ctx* c, const float* d_pi, const float* d_ref, const uint8_t* d_des, int32_t nseq, float beta,
+             float lambda_d, float lambda_u, float* d_loss, float* d_coeffs) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!d_pi || !d_ref || nseq < 1) return fail(c, LS_ERR_ARG, "kto_loss: bad arguments");
+  TIMED(LS_K_OTHER, 0, 16.0 * nseq, 1,
+        ls::pref_loss_kernel<<<1, 32, 0, c->cs>>>(ls::PREF_KTO, d_pi, d_ref, nullptr, nullptr, d_des, nseq, beta,
+                                                  lambda_d, lambda_u, d_loss, d_coeffs));
+  return LS_OK;
+}
+
 int stream_step_bwd(ls_ctx* c, const float* d_coeffs) {
   int rc = sticky(c);
   if (rc) return rc;

@@ -16,8 +16,9 @@
 // Pipeline per CTA (one BM x BN output tile, BM = 128 x NACC):
 //   warp 0      TMA producer: activation tile (SW128, K-major) + packed code tile,
 //               and the tile's absmax values by cp.async, into an S-deep ring.
-//   warps 2..9  dequantise codes into a K-major SW128 bf16 tile (transposed in
-//               registers for DX), an SB-deep ring; then run the epilogue.
+//   warps 2..9  dequantise codes into a SW128 bf16 tile, an SB-deep ring (one thread
+//               per 64-code row with register byte tables; K-major for FWD, MN-major
+//               -- W's own orientation -- for DX); then run the epilogue.
 //   warp 1      one thread issues tcgen05.mma (M=128, N=BN, K=16) into TMEM
 //               accumulators, NACC of them sharing each dequantised B tile.
 // Epilogues: bf16 store (+ residual), fp32 store / accumulate, vocabulary
@@ -34,6 +35,13 @@ __device__ __constant__ float kNF4Table[16] = {
     0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
 
 __device__ float g_zero_word[4] = {0.f, 0.f, 0.f, 0.f};
+
+// The same 16 values as compile-time constants (folded into the multiplies).
+__device__ constexpr float kNF4Values[16] = {
+    -1.0f, -0.6961928009986877f, -0.5250730514526367f, -0.39491748809814453f,
+    -0.28444138169288635f, -0.18477343022823334f, -0.09105003625154495f, 0.0f,
+    0.07958029955625534f, 0.16093020814657211f, 0.24611230194568634f, 0.33791524171829224f,
+    0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
 
 enum GemmMode : int { GEMM_FWD = 0, GEMM_DX = 1 };
 enum GemmEpi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_F32_ACC = 2, EPI_LOGPROB = 3, EPI_DLOGITS = 4 };
@@ -67,73 +75,109 @@ struct GemmCfg {
   static constexpr int W_BYTES = BN * 32;
   static constexpr int NDQ_WARPS = 8;
   static constexpr int NDQ = NDQ_WARPS * 32;
+  // dequant: one thread per 64-element row of the B tile (forward: output column;
+  // input gradient: W row x 64-column block); with BN = 128 the two halves of the
+  // dequant warps take alternate k-steps (group g owns B buffer g)
+  static constexpr int FWD_GROUPS = NDQ / BN;
+  static constexpr int FWD_GROUP_WARPS = NDQ_WARPS / FWD_GROUPS;
   static constexpr int THREADS = 64 + NDQ;
   static constexpr int TMEM_COLS = NACC * BN;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_BYTES;
   static constexpr int OFF_W = OFF_B + SB * B_BYTES;
   static constexpr int OFF_ABS = OFF_W + S * W_BYTES;
-  static constexpr int OFF_TAB = OFF_ABS + S * BN * 4;
-  static constexpr int OFF_BAR = OFF_TAB + 64;
+  static constexpr int OFF_BAR = OFF_ABS + S * BN * 4;
   static constexpr int NBAR = 2 * S + 2 * SB + 1;
   static constexpr int OFF_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_SLOT + 16 + 1024;   // + slack to align the base to 1024
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
   static_assert(BN == 128 || BN == 256, "BN");
+  static_assert(FWD_GROUPS == 1 || (FWD_GROUPS == 2 && SB == 2), "forward dequant groups need one B buffer each");
 };
 
 // -------------------------------------------------------------------------- dequantisers
 
-// FWD: B tile row j (output column n0 + j) holds 64 reduction values; unit = (row, 16-byte chunk).
-template <int BN, int NDQ>
-__device__ __forceinline__ void dequant_fwd(const uint8_t* Wt, const float* absS, uint8_t* Bt, int tq,
-                                            const float* tab) {
-#pragma unroll 2
-  for (int u = tq; u < BN * 8; u += NDQ) {
-    const int j = u >> 3, c = u & 7;
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(Wt + j * 32 + c * 4);
-    const float a = absS[j];
-    uint32_t o[4];
+// FWD, register tables: one thread turns one whole B-tile row (64 codes, one absmax a)
+// into bf16.  The 16 possible outputs bf16_rne(q[i] * a) are formed once per row (16
+// fp32 multiplies, the same single multiply and rounding as above, so the result is
+// bit-identical) and split into low-byte / high-byte tables of four registers each;
+// every group of four codes is then looked up with byte permutes (prmt): entries 0..7
+// and 8..15 separately, chosen per byte by the code's top bit.  No shared-memory load
+// sits inside the per-element chain, so the eight dequant warps stay issue-bound
+// instead of waiting on table loads.
+struct Nf4ByteTab {
+  uint32_t lo[4], hi[4];
+};
+
+__device__ __forceinline__ void nf4_byte_tab(float a, Nf4ByteTab& t) {
+  uint32_t p[8];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float e0 = tab[(w >> (8 * b + 4)) & 15] * a;   // element 2b: high nibble
-      const float e1 = tab[(w >> (8 * b)) & 15] * a;       // element 2b+1: low nibble
-      o[b] = pack_bf16x2(e0, e1);
-    }
+  for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(kNF4Values[2 * i] * a, kNF4Values[2 * i + 1] * a);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    t.lo[i] = __byte_perm(p[2 * i], p[2 * i + 1], 0x6420);
+    t.hi[i] = __byte_perm(p[2 * i], p[2 * i + 1], 0x7531);
+  }
+}
+
+// Four codes (16 bits: byte 0 = elements 0 (high nibble) and 1, byte 1 = elements 2, 3)
+// to two bf16x2 words (elements 0,1 and 2,3).
+__device__ __forceinline__ void nf4_lookup4(uint32_t v, const Nf4ByteTab& t, uint32_t& o01, uint32_t& o23) {
+  const uint32_t s7 = v & 0x7777u;
+  const uint32_t la = __byte_perm(t.lo[0], t.lo[1], s7), lb = __byte_perm(t.lo[2], t.lo[3], s7);
+  const uint32_t ha = __byte_perm(t.hi[0], t.hi[1], s7), hb = __byte_perm(t.hi[2], t.hi[3], s7);
+  const uint32_t m = __byte_perm(0x0000FF00u, 0u, (v >> 3) & 0x1111u);   // 0xFF where code >= 8
+  const uint32_t L = (la & ~m) | (lb & m), H = (ha & ~m) | (hb & m);
+  // bytes of L/H are in nibble order: element 1, 0, 3, 2
+  o01 = __byte_perm(L, H, 0x4051);
+  o23 = __byte_perm(L, H, 0x6273);
+}
+
+template <int BN>
+__device__ __forceinline__ void dequant_fwd_row(const uint8_t* Wt, const float* absS, uint8_t* Bt, int j) {
+  // the two 16-byte halves of the row's codes, read in an order that keeps a quarter
+  // warp (rows j..j+7, 32 bytes apart) on distinct banks
+  const int h0 = (j >> 2) & 1;
+  const uint4 first = *reinterpret_cast<const uint4*>(Wt + j * 32 + h0 * 16);
+  const uint4 second = *reinterpret_cast<const uint4*>(Wt + j * 32 + (h0 ^ 1) * 16);
+  const uint4 w0 = h0 ? second : first, w1 = h0 ? first : second;
+  Nf4ByteTab t;
+  nf4_byte_tab(absS[j], t);
+  const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t o[4];
+    nf4_lookup4(cw[c] & 0xFFFFu, t, o[0], o[1]);
+    nf4_lookup4(cw[c] >> 16, t, o[2], o[3]);
     *reinterpret_cast<uint4*>(Bt + j * 128 + ((c ^ (j & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
-// DX: W tile = 64 rows n (reduction) x BN columns k (output).  B tile row k holds the
-// 64 n-values.  Unit = 8 n x 8 k, transposed in registers; the k-row order is rotated
-// by the lane's column group so the 8 lanes of a store phase hit distinct banks.
-template <int BN, int NDQ>
-__device__ __forceinline__ void dequant_dx(const uint8_t* Wt, const float* absS, uint8_t* Bt, int tq,
-                                           const float* tab) {
-  constexpr int KG = BN / 8;
-  for (int u = tq; u < BN; u += NDQ) {
-    const int kg = u % KG, ng = u / KG;
-    uint32_t w[8];
-    float a[8];
+// DX, register tables, MN-major B tile.  For dX = dY . deq(W) the MMA's reduction runs
+// over W's rows n and its output columns are W's columns k, so W's own row-major tile
+// IS the B operand in MN-major form: no transpose.  Thread j dequantises the 64 codes
+// of row n = j % 64, 64-column block kbl = j / 64 (one absmax) with the same byte
+// tables as the forward, and stores them as one 128-byte K-row of the canonical
+// MN-major 128B-swizzled layout: atoms of 64 columns x 8 rows (1 KB), 8 atoms down the
+// 64 rows (8 KB per 64 columns):  offset = kbl*8192 + (n/8)*1024 + (n%8)*128 + chunk.
+template <int BN>
+__device__ __forceinline__ void dequant_dx_row(const uint8_t* Wt, const float* absS, uint8_t* Bt, int j) {
+  const int n = j & 63, kbl = j >> 6;
+  const uint8_t* src = Wt + n * (BN / 2) + kbl * 32;
+  const int h0 = (n >> 1) & 1;   // stagger the two 16-byte halves across neighbouring rows
+  const uint4 first = *reinterpret_cast<const uint4*>(src + h0 * 16);
+  const uint4 second = *reinterpret_cast<const uint4*>(src + (h0 ^ 1) * 16);
+  const uint4 w0 = h0 ? second : first, w1 = h0 ? first : second;
+  Nf4ByteTab t;
+  nf4_byte_tab(absS[n * (BN / 64) + kbl], t);
+  const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  uint8_t* row = Bt + kbl * 8192 + (n >> 3) * 1024 + (n & 7) * 128;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      w[r] = *reinterpret_cast<const uint32_t*>(Wt + (8 * ng + r) * (BN / 2) + kg * 4);
-      a[r] = absS[(8 * ng + r) * (BN / 64) + (kg >> 3)];
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int ip = (i + kg) & 7;
-      const int sh = 8 * (ip >> 1) + ((ip & 1) ? 0 : 4);
-      uint32_t o[4];
-#pragma unroll
-      for (int r = 0; r < 8; r += 2) {
-        const float e0 = tab[(w[r] >> sh) & 15] * a[r];
-        const float e1 = tab[(w[r + 1] >> sh) & 15] * a[r + 1];
-        o[r >> 1] = pack_bf16x2(e0, e1);
-      }
-      const int k = 8 * kg + ip;
-      *reinterpret_cast<uint4*>(Bt + k * 128 + ((ng ^ (k & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
+  for (int c = 0; c < 8; ++c) {
+    uint32_t o[4];
+    nf4_lookup4(cw[c] & 0xFFFFu, t, o[0], o[1]);
+    nf4_lookup4(cw[c] >> 16, t, o[2], o[3]);
+    *reinterpret_cast<uint4*>(row + ((c ^ (n & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -160,7 +204,9 @@ __device__ __forceinline__ void store_bf16_32(__nv_bfloat16* dst, const float (&
 #pragma unroll
     for (int i = 0; i < 4; ++i) d[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
   } else {
-    for (int i = 0; i < nvalid; ++i) dst[i] = __float2bfloat16_rn(f[i]);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nvalid) dst[i] = __float2bfloat16_rn(f[i]);
   }
 }
 
@@ -187,7 +233,6 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
   auto bfull = [&](int s) { return bar0 + (2 * S + s) * 8; };
   auto bempty = [&](int s) { return bar0 + (2 * S + SB + s) * 8; };
   const uint32_t accfull = bar0 + (2 * S + 2 * SB) * 8;
-  float* s_tab = reinterpret_cast<float*>(smem + C::OFF_TAB);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -195,14 +240,13 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
       mbar_init(empty(s), 1);
     }
     for (int s = 0; s < SB; ++s) {
-      mbar_init(bfull(s), C::NDQ_WARPS);
+      mbar_init(bfull(s), C::FWD_GROUP_WARPS);
       mbar_init(bempty(s), 1);
     }
     mbar_init(accfull, 1);
     fence_barrier_init();
     s_abort = 0;
   }
-  if (threadIdx.x < 16) s_tab[threadIdx.x] = kNF4Table[threadIdx.x];
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmW);
@@ -275,12 +319,16 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
         const int nk = it < KB ? 4 : g.ext_k / 16;
         const uint32_t a_base = sb + C::OFF_A + s * C::A_BYTES;
         const uint32_t b_base = sb + C::OFF_B + b * C::B_BYTES;
+        // the input-gradient main loop reads B MN-major (16 reduction rows = two 1 KB
+        // 8-row groups per instruction); the LoRA extra stage is K-major in both modes
+        const bool mn = MODE == GEMM_DX && it < KB;
+        const uint32_t idesc = mn ? IDESC | (1u << 16) : IDESC;
         for (int k = 0; k < nk; ++k) {
-          const uint64_t bd = sw128_kmajor_desc(b_base + k * 32);
+          const uint64_t bd = mn ? sw128_mnmajor_desc(b_base + k * 2048, 8192) : sw128_kmajor_desc(b_base + k * 32);
 #pragma unroll
           for (int a = 0; a < NACC; ++a) {
             const uint64_t ad = sw128_kmajor_desc(a_base + a * 16384 + k * 32);
-            tc_mma_bf16(tmem + a * BN, ad, bd, IDESC, (it > 0 || k > 0) ? 1u : 0u);
+            tc_mma_bf16(tmem + a * BN, ad, bd, idesc, (it > 0 || k > 0) ? 1u : 0u);
           }
         }
         tc_commit(empty(s));
@@ -293,7 +341,11 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
   } else {
     // ------------------------------------------------------------ dequant warps
     const int tq = threadIdx.x - 64;
-    for (int it = 0; it < niter; ++it) {
+    // group grp takes k-steps it = grp, grp + FWD_GROUPS, ...; its threads one row each
+    const int grp = tq / BN;
+    const int step = C::FWD_GROUPS;
+    const int tg = tq - grp * BN;
+    for (int it = grp; it < niter; it += step) {
       const int s = it % S, b = it % SB;
       if (s_abort || !mbar_wait(full(s), (it / S) & 1) || !mbar_wait(bempty(b), ((it / SB) & 1) ^ 1)) {
         s_abort = 1;
@@ -303,10 +355,10 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
       if (it < KB) {
         const uint8_t* Wt = smem + C::OFF_W + s * C::W_BYTES;
         const float* absS = reinterpret_cast<const float*>(smem + C::OFF_ABS + s * BN * 4);
-        if (MODE == GEMM_FWD) dequant_fwd<BN, C::NDQ>(Wt, absS, Bt, tq, s_tab);
-        else dequant_dx<BN, C::NDQ>(Wt, absS, Bt, tq, s_tab);
+        if (MODE == GEMM_FWD) dequant_fwd_row<BN>(Wt, absS, Bt, tg);
+        else dequant_dx_row<BN>(Wt, absS, Bt, tg);
       } else {
-        copy_ext_tile<BN, C::NDQ>(g.ext_b, n0, g.Nout, Bt, tq);
+        copy_ext_tile<BN, BN>(g.ext_b, n0, g.Nout, Bt, tg);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -358,7 +410,9 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
                   }
                 }
               } else {
-                for (int i = 0; i < nvalid; ++i) f[i] += bf2f(rp[i]);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i < nvalid) f[i] += bf2f(rp[i]);
               }
             }
             store_bf16_32(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
@@ -376,7 +430,9 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
                 o4[q] = x;
               }
             } else {
-              for (int i = 0; i < nvalid; ++i) op[i] = (g.epi == EPI_F32_ACC ? op[i] : 0.f) + f[i];
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nvalid) op[i] = (g.epi == EPI_F32_ACC ? op[i] : 0.f) + f[i];
             }
           } else if (g.epi == EPI_LOGPROB) {
             float cm = -INFINITY;

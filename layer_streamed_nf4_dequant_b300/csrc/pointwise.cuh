@@ -315,6 +315,81 @@ __global__ void dpo_loss_kernel(const float* __restrict__ pi, const float* __res
   if (loss) *loss = acc / (float)npairs;
 }
 
+// Other preference losses over (chosen, rejected) pairs or labelled sequences, from
+// per-sequence logprob sums (the pages list ORPO, SimPO and KTO beside DPO; the formulas
+// are the methods' own).  One block: the response lengths |y| come from the loss mask
+// (a fixed-order block reduction per sequence), then thread 0 forms the loss and each
+// sequence's coefficient dL/d(sum) for the streamed backward.
+enum PrefKind : int { PREF_SIMPO = 0, PREF_ORPO = 1, PREF_KTO = 2 };
+
+__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x))); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + __expf(-x)); }
+
+__global__ void pref_loss_kernel(int kind, const float* __restrict__ pi, const float* __restrict__ ref,
+                                 const int* __restrict__ cu, const uint8_t* __restrict__ mask,
+                                 const uint8_t* __restrict__ desirable, int nseq, float beta, float p1, float p2,
+                                 float* __restrict__ loss, float* __restrict__ coeffs) {
+  extern __shared__ float cnt[];   // [nseq]
+  __shared__ float red[32];
+  if (kind != PREF_KTO) {
+    for (int sq = 0; sq < nseq; ++sq) {
+      const int a = cu[sq], b = cu[sq + 1];
+      float c = 0.f;
+      for (int t = a + threadIdx.x; t < b; t += blockDim.x) c += mask[t] ? 1.f : 0.f;
+      c = warp_sum(c);
+      if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        v = warp_sum(v);
+        if (threadIdx.x == 0) cnt[sq] = v;
+      }
+      __syncthreads();
+    }
+  }
+  if (threadIdx.x != 0) return;
+  float acc = 0.f;
+  if (kind == PREF_SIMPO || kind == PREF_ORPO) {
+    const int np = nseq / 2;
+    for (int p = 0; p < np; ++p) {
+      const float nc = cnt[2 * p], nr = cnt[2 * p + 1];
+      const float lc = pi[2 * p] / nc, lr = pi[2 * p + 1] / nr;
+      if (kind == PREF_SIMPO) {   // p1 = gamma
+        const float z = beta * (lc - lr) - p1;
+        acc += softplus_f(-z);
+        const float sg = sigmoid_f(-z);
+        if (coeffs) {
+          coeffs[2 * p] = -sg * beta / nc / (float)np;
+          coeffs[2 * p + 1] = sg * beta / nr / (float)np;
+        }
+      } else {                    // p1 = lambda; log odds = l - log(1 - e^l)
+        const float emc = expm1f(lc), emr = expm1f(lr);
+        const float d = (lc - logf(-emc)) - (lr - logf(-emr));
+        acc += -lc + p1 * softplus_f(-d);
+        const float sg = sigmoid_f(-d);
+        if (coeffs) {             // d log odds / d l = -1 / expm1(l)
+          coeffs[2 * p] = (-1.f + p1 * sg / emc) / nc / (float)np;
+          coeffs[2 * p + 1] = (-p1 * sg / emr) / nr / (float)np;
+        }
+      }
+    }
+    if (loss) *loss = acc / (float)np;
+  } else {                        // KTO: p1 = lambda_d, p2 = lambda_u
+    float z0 = 0.f;
+    for (int sq = 0; sq < nseq; ++sq) z0 += pi[sq] - ref[sq];
+    z0 = fmaxf(z0 / (float)nseq, 0.f);
+    for (int sq = 0; sq < nseq; ++sq) {
+      const float r = pi[sq] - ref[sq];
+      const bool des = desirable ? desirable[sq] != 0 : (sq % 2 == 0);
+      const float lam = des ? p1 : p2;
+      const float sg = sigmoid_f(beta * (des ? r - z0 : z0 - r));
+      acc += lam * (1.f - sg);
+      if (coeffs) coeffs[sq] = (des ? -1.f : 1.f) * lam * beta * sg * (1.f - sg) / (float)nseq;
+    }
+    if (loss) *loss = acc / (float)nseq;
+  }
+}
+
 // ------------------------------------------------------------------ LoRA pieces
 // Rank-r projections of the LoRA branch (Soup's soup.yaml listing: r 16 on q_proj and
 // v_proj), as one small contraction with N = 2 x 16 output columns:

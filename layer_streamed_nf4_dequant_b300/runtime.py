@@ -75,14 +75,14 @@ class Stack:
     def __init__(self, s, max_tokens: int = 0, max_seqs: int = 0, max_seq_len: int = 0, resident: bool = False,
                  cap_bytes: Optional[int] = None, vocab_chunk_rows: int = 0, device: str = "cuda:0",
                  dpo_shared_read: Optional[bool] = None):
-        """dpo_shared_read: run DPO's policy and reference forward in one sweep of the
-        streamed layers (None: whenever the workload is DPO and the larger forward
-        workspace fits the device cap)."""
+        """dpo_shared_read: run the policy and reference forward of DPO / KTO in one
+        sweep of the streamed layers (None: whenever the workload needs a reference
+        pass and the larger forward workspace fits the device cap)."""
         self.s = s
         self.dev = torch.device(device)
         if dpo_shared_read is None:
             dpo_shared_read = False
-            if getattr(s, "method", "sft") == "dpo":
+            if getattr(s, "method", "sft") in ("dpo", "kto"):
                 trial = make_config(s, max_tokens, max_seqs, max_seq_len, resident, cap_bytes, vocab_chunk_rows, True)
                 n = C.c_uint64(0)
                 dpo_shared_read = lib().ls_plan(C.byref(trial), C.byref(n)) == 0
@@ -210,6 +210,23 @@ class Stack:
             t = [torch.from_numpy(x).to(torch.bfloat16).to(self.dev) for x in (aq, bq, av, bv)]
             self.set_adapter(l, *t)
 
+    def export_adapter(self, path: str):
+        """Write the bound LoRA factors with canonical keys (see adapters.py)."""
+        from .adapters import save_adapter
+        ads = [{k: self.adapters[l][k].detach().view(torch.int16).cpu().numpy().view(np.uint16)
+                for k in ("aq", "bq", "av", "bv")} for l in range(self.s.layers)]
+        return save_adapter(path, ads, self.s.lora_r, self.s.lora_alpha)
+
+    def import_adapter(self, path: str):
+        """Bind the LoRA factors of a canonical-key adapter file (refuses mismatched keys)."""
+        from .adapters import load_adapter
+        s = self.s
+        ads = load_adapter(path, s.layers, s.hidden, s.heads * s.head_dim, s.kv_heads * s.head_dim, s.lora_r)
+        for l, ad in enumerate(ads):
+            t = [torch.from_numpy(ad[k].view(np.int16)).view(torch.bfloat16).to(self.dev)
+                 for k in ("aq", "bq", "av", "bv")]
+            self.set_adapter(l, *t)
+
     def grad_numel(self) -> int:
         s = self.s
         return s.layers * (2 * s.lora_r * s.hidden + s.lora_r * (s.heads + s.kv_heads) * s.head_dim)
@@ -274,6 +291,41 @@ class Stack:
         self.bwd(o["coeffs"])
         return o
 
+    def pref_step(self, method: str, tok, cu, mask, out: Optional[Dict] = None) -> Dict:
+        """One preference-optimisation step on (chosen, rejected) pairs: "dpo", "kto"
+        (policy and reference forward), "simpo" or "orpo" (policy forward only), then the
+        loss and the streamed backward.  Hyperparameters come from the stack config."""
+        if method == "dpo":
+            return self.dpo_step(tok, cu, mask, self.s.beta, out)
+        s = self.s
+        nseq = cu.numel() - 1
+        o = out if out is not None else {
+            "pi": torch.empty(nseq, dtype=torch.float32, device=self.dev),
+            "ref": torch.empty(nseq, dtype=torch.float32, device=self.dev),
+            "loss": torch.empty(1, dtype=torch.float32, device=self.dev),
+            "coeffs": torch.empty(nseq, dtype=torch.float32, device=self.dev)}
+        if method in ("simpo", "orpo"):
+            self.fwd(tok, cu, mask, True, True, o["pi"])
+            if method == "simpo":
+                check(lib().simpo_loss(self.ctx, o["pi"].data_ptr(), cu.data_ptr(), mask.data_ptr(), nseq // 2, s.beta,
+                                       s.simpo_gamma, o["loss"].data_ptr(), o["coeffs"].data_ptr()), self.ctx)
+            else:
+                check(lib().orpo_loss(self.ctx, o["pi"].data_ptr(), cu.data_ptr(), mask.data_ptr(), nseq // 2,
+                                      s.orpo_lambda, o["loss"].data_ptr(), o["coeffs"].data_ptr()), self.ctx)
+        elif method == "kto":
+            if self.shared_read:
+                self.fwd_dpo(tok, cu, mask, o["pi"], o["ref"])
+            else:
+                self.fwd(tok, cu, mask, True, True, o["pi"])
+                self.fwd(tok, cu, mask, False, False, o["ref"])
+            check(lib().kto_loss(self.ctx, o["pi"].data_ptr(), o["ref"].data_ptr(), None, nseq, s.beta,
+                                 s.kto_lambda_d, s.kto_lambda_u, o["loss"].data_ptr(), o["coeffs"].data_ptr()),
+                  self.ctx)
+        else:
+            raise ValueError(f"unknown preference method {method!r}")
+        self.bwd(o["coeffs"])
+        return o
+
     def sft_step(self, tok, cu, mask, count: float, out: Optional[Dict] = None) -> Dict:
         nseq = cu.numel() - 1
         o = out if out is not None else {
@@ -289,7 +341,8 @@ class Stack:
     def train_step(self, h_tokens: torch.Tensor, h_cu: torch.Tensor, h_mask: torch.Tensor, method: str,
                    beta: float = 0.1, h_loss: Optional[torch.Tensor] = None, grads_out: Optional[torch.Tensor] = None,
                    dev_bufs: Optional[Dict] = None) -> torch.Tensor:
-        """One SFT or DPO step from HOST (preferably pinned) token, offset and mask buffers.
+        """One SFT or preference step (dpo, kto, simpo, orpo) from HOST (preferably
+        pinned) token, offset and mask buffers.
 
         Copies the batch to the device on the compute stream, runs the streamed step,
         gathers the LoRA gradients into grads_out (zeroing the bound buffers), and
@@ -306,10 +359,10 @@ class Stack:
             d["tok"].copy_(h_tokens, non_blocking=True)
             d["cu"].copy_(h_cu, non_blocking=True)
             d["mask"].copy_(h_mask, non_blocking=True)
-            if method == "dpo":
-                o = self.dpo_step(d["tok"], d["cu"], d["mask"], beta, d.get("out"))
-            else:
+            if method == "sft":
                 o = self.sft_step(d["tok"], d["cu"], d["mask"], float(h_mask.sum().item()), d.get("out"))
+            else:
+                o = self.pref_step(method, d["tok"], d["cu"], d["mask"], d.get("out"))
             d["out"] = o
             check(lib().lora_grads(self.ctx, grads_out.data_ptr() if grads_out is not None else None, 1), self.ctx)
             if h_loss is None:

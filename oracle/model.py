@@ -277,9 +277,58 @@ def dpo_loss(pi: torch.Tensor, ref: torch.Tensor, beta: float) -> torch.Tensor:
     return F.softplus(-z).mean()
 
 
+# ---------------------------------------------------------------- other preference losses
+# The pages list ORPO, SimPO and KTO beside DPO as methods run over the streamed base
+# (axbrief.com, "The Architecture of Low-VRAM Alignment"; evermx.com summary) without
+# defining them; these follow the methods' own papers.  All act on per-sequence
+# logprob sums over the response positions, as DPO does.
+
+def seq_counts(mask: np.ndarray, cu) -> torch.Tensor:
+    """Number of response positions (mask = 1) of each sequence."""
+    return torch.tensor([float(mask[int(cu[i]):int(cu[i + 1])].sum()) for i in range(len(cu) - 1)],
+                        dtype=torch.float64)
+
+
+def simpo_loss(pi: torch.Tensor, counts: torch.Tensor, beta: float, gamma: float) -> torch.Tensor:
+    """SimPO (Meng, Xia, Chen 2024): mean over pairs of
+    -log sigmoid(beta pi_c / |c| - beta pi_r / |r| - gamma); no reference model."""
+    avg = pi / counts.to(pi.dtype)
+    z = beta * (avg[0::2] - avg[1::2]) - gamma
+    return F.softplus(-z).mean()
+
+
+def orpo_loss(pi: torch.Tensor, counts: torch.Tensor, lam: float) -> torch.Tensor:
+    """ORPO (Hong, Lee, Thorne 2024): mean over pairs of the chosen response's mean NLL
+    plus lam * -log sigmoid(log odds(c) - log odds(r)), where odds(y) = P / (1 - P) and
+    P = exp(mean logprob of y); no reference model."""
+    avg = pi / counts.to(pi.dtype)
+    log_odds = avg - torch.log1p(-torch.exp(avg))
+    nll = -avg[0::2]
+    return (nll + lam * F.softplus(-(log_odds[0::2] - log_odds[1::2]))).mean()
+
+
+def kto_loss(pi: torch.Tensor, ref: torch.Tensor, desirable: torch.Tensor, beta: float, lam_d: float,
+             lam_u: float) -> torch.Tensor:
+    """KTO (Ethayarajh et al. 2024): r = pi - ref per sequence, reference point
+    z0 = max(0, mean r over the batch) taken without gradient; loss = mean of
+    lam_d (1 - sigmoid(beta (r - z0))) on desirable sequences and
+    lam_u (1 - sigmoid(beta (z0 - r))) on undesirable ones."""
+    r = pi - ref
+    z0 = torch.clamp(r.detach().mean(), min=0.0)
+    d = desirable.to(torch.bool)
+    v = torch.where(d, lam_d * torch.sigmoid(beta * (r - z0)), lam_u * torch.sigmoid(beta * (z0 - r)))
+    lam = torch.where(d, torch.full_like(r, lam_d), torch.full_like(r, lam_u))
+    return (lam - v).mean()
+
+
+def pair_desirable(nseq: int) -> torch.Tensor:
+    """KTO labels for (chosen, rejected) pair data: chosen desirable, rejected not."""
+    return torch.tensor([1 - (i % 2) for i in range(nseq)], dtype=torch.uint8)
+
+
 def train_step(tokens: np.ndarray, cu, mask: np.ndarray, sw: StackWeights,
                adapters: List[Adapter], cfg, method: Optional[str] = None) -> Dict:
-    """One SFT or DPO step: loss, logprobs and the LoRA gradients (fp64).
+    """One SFT, DPO, SimPO, ORPO or KTO step: loss, logprobs and the LoRA gradients (fp64).
 
     The base is frozen; gradients are taken for A and B of every layer only.
     """
@@ -292,12 +341,24 @@ def train_step(tokens: np.ndarray, cu, mask: np.ndarray, sw: StackWeights,
     out = dict(lp=pol["lp"].detach(), lse=pol["lse"].detach())
     if method == "sft":
         loss = sft_loss(pol["lp"], mask)
+    elif method in ("simpo", "orpo"):
+        pi = seq_sums(pol["lp"], mask, cu)
+        counts = seq_counts(mask, cu)
+        if method == "simpo":
+            loss = simpo_loss(pi, counts, cfg.beta, getattr(cfg, "simpo_gamma", 1.0))
+        else:
+            loss = orpo_loss(pi, counts, getattr(cfg, "orpo_lambda", 0.1))
+        out.update(pi=pi.detach())
     else:
         with torch.no_grad():
             ref = stack_forward(tokens, cu, sw, adapters, cfg, adapter_on=False)
         pi = seq_sums(pol["lp"], mask, cu)
         rs = seq_sums(ref["lp"], mask, cu)
-        loss = dpo_loss(pi, rs, cfg.beta)
+        if method == "kto":
+            loss = kto_loss(pi, rs, pair_desirable(len(cu) - 1), cfg.beta, getattr(cfg, "kto_lambda_d", 1.0),
+                            getattr(cfg, "kto_lambda_u", 1.0))
+        else:
+            loss = dpo_loss(pi, rs, cfg.beta)
         out.update(lp_ref=ref["lp"], pi=pi.detach(), ref=rs)
     loss.backward()
     out["loss"] = loss.detach()

@@ -37,8 +37,12 @@ class StackConfig:
     seq_len: int = 512            # tokens per sequence
     nseq: int = 1                 # sequences per pass
     prompt_len: int = 0           # DPO: shared prompt length (0 = SFT)
-    method: str = "sft"           # "sft" | "dpo"
+    method: str = "sft"           # "sft" | "dpo" | "simpo" | "orpo" | "kto"
     beta: float = 0.1
+    simpo_gamma: float = 1.0      # SimPO target margin
+    orpo_lambda: float = 0.1      # ORPO odds-ratio weight
+    kto_lambda_d: float = 1.0     # KTO weights of desirable / undesirable sequences
+    kto_lambda_u: float = 1.0
     cap_bytes: int = 0            # device cap (0 = none)
 
     @property
@@ -156,12 +160,12 @@ def lora_weights(cfg: StackConfig, layer: int, proj: str, seed: int = 0,
 def tokens(cfg: StackConfig, seed: int = 0) -> np.ndarray:
     """Token ids for one pass, int32 [T]; uniform over the vocabulary.
 
-    DPO: sequences come in (chosen, rejected) pairs that share their first
-    prompt_len tokens.
+    Preference methods: sequences come in (chosen, rejected) pairs that share their
+    first prompt_len tokens.
     """
     g = _rng(seed, 5)
     t = g.integers(0, cfg.vocab, size=(cfg.nseq, cfg.seq_len), dtype=np.int64)
-    if cfg.method == "dpo" and cfg.prompt_len > 0:
+    if cfg.method != "sft" and cfg.prompt_len > 0:
         for p in range(0, cfg.nseq, 2):
             t[p + 1, :cfg.prompt_len] = t[p, :cfg.prompt_len]
     return t.reshape(-1).astype(np.int32)
@@ -175,11 +179,11 @@ def seq_offsets(cfg: StackConfig) -> np.ndarray:
 def loss_mask(cfg: StackConfig) -> np.ndarray:
     """uint8 [T]: 1 where position t's prediction of token t+1 counts.
 
-    SFT: every position but the last of each sequence.  DPO: only predictions of
-    response tokens (positions prompt_len-1 .. seq_len-2 of each sequence).
+    SFT: every position but the last of each sequence.  Preference methods: only
+    predictions of response tokens (positions prompt_len-1 .. seq_len-2 of each sequence).
     """
     m = np.zeros((cfg.nseq, cfg.seq_len), np.uint8)
-    lo = cfg.prompt_len - 1 if cfg.method == "dpo" and cfg.prompt_len > 0 else 0
+    lo = cfg.prompt_len - 1 if cfg.method != "sft" and cfg.prompt_len > 0 else 0
     m[:, lo: cfg.seq_len - 1] = 1
     return m.reshape(-1)
 

@@ -410,3 +410,30 @@ def test_tiny_dpo_step_matches_golden():
             norm = np.linalg.norm(gn[off: off + n])
             assert norm == pytest.approx(g["grad_norms"][layer][i], rel=TOL_GRAD * 5)
             off += n
+
+
+def test_adapter_export_import_round_trip(tmp_path):
+    """An adapter written with canonical keys and read back into a fresh context gives
+    the same policy logprobs bit for bit, and they differ from the base's (so the
+    import is not a silent no-op)."""
+    cfg = SMALL_DPO
+    tok, cu, mask = _batch(cfg)
+    a = _stack(cfg)
+    path = str(tmp_path / "adapter.safetensors")
+    keys = a.export_adapter(path)
+    assert len(keys) == 4 * cfg.layers and not any(".inner." in k for k in keys)
+    b = L.Stack(cfg, device="cuda:0")
+    b.adopt_base(a)
+    base = L.Stack(cfg, device="cuda:0")
+    base.adopt_base(a)
+    b.import_adapter(path)
+    lps = []
+    for st in (a, b, base):
+        t, c, m = st.upload_batch(tok, cu, mask)
+        st.fwd(t, c, m, adapter_on=True, save=False)
+        lps.append(st.logprobs(len(tok))[0])
+        assert st.sync(60000) == 0
+    for st in (b, base, a):
+        st.close()
+    assert torch.equal(lps[0], lps[1])
+    assert not torch.equal(lps[1], lps[2])

@@ -460,3 +460,97 @@ def test_oracle_reproduces_tiny_dpo_golden():
     np.testing.assert_allclose(got["ref"], want["ref"], rtol=1e-12)
     np.testing.assert_allclose(got["grad_norms"], want["grad_norms"], rtol=1e-10)
     np.testing.assert_allclose(got["grad_head"], want["grad_head"], rtol=1e-9, atol=1e-15)
+
+
+# ------------------------------------------------------------------ SimPO, ORPO, KTO
+
+def test_simpo_closed_forms():
+    counts = torch.tensor([4.0, 8.0], dtype=F64)
+    # equal average logprobs and no margin: -log sigmoid(0) = ln 2
+    pi = torch.tensor([-8.0, -16.0], dtype=F64, requires_grad=True)
+    L = M.simpo_loss(pi, counts, beta=2.0, gamma=0.0)
+    assert float(L.detach()) == pytest.approx(math.log(2.0), rel=1e-15)
+    L.backward()
+    # dL/dpi_c = -sigma(-z) beta / |c|, dL/dpi_r = +sigma(-z) beta / |r|, sigma(0) = 1/2
+    np.testing.assert_allclose(pi.grad.numpy(), [-0.5 * 2.0 / 4, 0.5 * 2.0 / 8], rtol=1e-15)
+    # the margin gamma shifts the logit: z = -gamma
+    L2 = M.simpo_loss(pi.detach(), counts, beta=2.0, gamma=1.5)
+    assert float(L2) == pytest.approx(math.log1p(math.exp(1.5)), rel=1e-14)
+    # length normalisation: doubling a sequence's sum and its length changes nothing
+    a = M.simpo_loss(torch.tensor([-3.0, -5.0], dtype=F64), torch.tensor([3.0, 5.0], dtype=F64), 1.0, 0.2)
+    b = M.simpo_loss(torch.tensor([-6.0, -5.0], dtype=F64), torch.tensor([6.0, 5.0], dtype=F64), 1.0, 0.2)
+    assert float(a) == pytest.approx(float(b), rel=1e-15)
+
+
+def test_orpo_closed_forms():
+    counts = torch.tensor([2.0, 2.0], dtype=F64)
+    pi = torch.tensor([-1.0, -3.0], dtype=F64)
+    # lambda = 0: the chosen response's mean NLL
+    assert float(M.orpo_loss(pi, counts, 0.0)) == pytest.approx(0.5, rel=1e-15)
+    # log odds against log(P / (1 - P)) computed directly
+    lc, lr = -0.5, -1.5
+    odds = lambda l: math.log(math.exp(l) / (1 - math.exp(l)))
+    want = 0.5 + 0.1 * math.log1p(math.exp(-(odds(lc) - odds(lr))))
+    assert float(M.orpo_loss(pi, counts, 0.1)) == pytest.approx(want, rel=1e-13)
+    # equal responses: odds-ratio term = ln 2
+    eq = M.orpo_loss(torch.tensor([-2.0, -2.0], dtype=F64), counts, 1.0)
+    assert float(eq) == pytest.approx(1.0 + math.log(2.0), rel=1e-14)
+
+
+def test_kto_closed_forms_and_reference_point():
+    d = torch.tensor([1, 0], dtype=torch.uint8)
+    # policy = reference: r = 0, z0 = 0, sigma(0) = 1/2 -> loss = mean(lambda / 2)
+    z = torch.zeros(2, dtype=F64)
+    pi = torch.zeros(2, dtype=F64, requires_grad=True)
+    L = M.kto_loss(pi, z, d, beta=0.1, lam_d=1.0, lam_u=3.0)
+    assert float(L.detach()) == pytest.approx((0.5 + 1.5) / 2, rel=1e-15)
+    L.backward()
+    # dL/dpi = -lam_d beta s(1-s) / n for desirable, +lam_u beta s(1-s) / n for undesirable
+    np.testing.assert_allclose(pi.grad.numpy(), [-1.0 * 0.1 * 0.25 / 2, 3.0 * 0.1 * 0.25 / 2], rtol=1e-15)
+    # the reference point is clamped at zero and carries no gradient
+    pi2 = torch.tensor([-4.0, -2.0], dtype=F64, requires_grad=True)
+    L2 = M.kto_loss(pi2, z, d, beta=1.0, lam_d=1.0, lam_u=1.0)
+    want = ((1 - 1 / (1 + math.exp(4.0))) + (1 - 1 / (1 + math.exp(-2.0)))) / 2
+    assert float(L2.detach()) == pytest.approx(want, rel=1e-14)
+    L2.backward()
+    s1 = 1 / (1 + math.exp(4.0))
+    s2 = 1 / (1 + math.exp(-2.0))
+    np.testing.assert_allclose(pi2.grad.numpy(), [-s1 * (1 - s1) / 2, s2 * (1 - s2) / 2], rtol=1e-13)
+
+
+@pytest.mark.parametrize("method", ["simpo", "orpo", "kto"])
+def test_preference_grads_finite_differences(method):
+    cfg = TINY.with_(method=method, prompt_len=2, beta=0.5, simpo_gamma=0.3, orpo_lambda=0.5)
+    sw, ads = _tiny(cfg)
+    tok, cu, mask = synth.tokens(cfg), synth.seq_offsets(cfg), synth.loss_mask(cfg)
+    with M.pure_fp64():
+        out = M.train_step(tok, cu, mask, sw, ads, cfg)
+
+        def loss_at():
+            with torch.no_grad():
+                pi = M.seq_sums(M.stack_forward(tok, cu, sw, ads, cfg, True)["lp"], mask, cu)
+                n = M.seq_counts(mask, cu)
+                if method == "simpo":
+                    return float(M.simpo_loss(pi, n, cfg.beta, cfg.simpo_gamma))
+                if method == "orpo":
+                    return float(M.orpo_loss(pi, n, cfg.orpo_lambda))
+                ref = M.seq_sums(M.stack_forward(tok, cu, sw, ads, cfg, False)["lp"], mask, cu)
+                return float(M.kto_loss(pi, ref, M.pair_desirable(len(cu) - 1), cfg.beta, 1.0, 1.0))
+
+        assert float(out["loss"]) == pytest.approx(loss_at(), rel=1e-12)
+        rng = np.random.default_rng(11)
+        h = 1e-6
+        for li in range(cfg.layers):
+            for pi_, p in enumerate(ads[li].params()):
+                g = out["grads"][li][pi_]
+                for _ in range(2):
+                    idx = tuple(int(rng.integers(0, s)) for s in p.shape)
+                    old = p.data[idx].item()
+                    p.data[idx] = old + h
+                    lp_ = loss_at()
+                    p.data[idx] = old - h
+                    lm_ = loss_at()
+                    p.data[idx] = old
+                    fd = (lp_ - lm_) / (2 * h)
+                    scale = float(g.abs().max()) + 1e-12
+                    assert abs(fd - float(g[idx])) <= 1e-6 * scale + 1e-9, (li, pi_, idx, fd, float(g[idx]))
