@@ -7,7 +7,7 @@ NF4 base held in pinned host RAM and LoRA r=16 on q_proj/v_proj, trained with DP
 responses, so each pass carries 2 x 512 tokens.  One step = policy forward (adapter
 on, activation store kept) and reference forward (same streamed base, adapter off)
 in one shared sweep of the layers, DPO loss, streamed backward, LoRA gradient
-gather.  Weights and tokens are seeded
+gather, AdamW step on the adapters (fp32 master weights).  Weights and tokens are seeded
 synthetic draws (N(0, 0.02) base, N(0, 0.01) adapters, uniform tokens).
 
 Prints ONE JSON line (rank 0).  value = policy tokens per second with the batch
@@ -287,15 +287,22 @@ def run_gpu_arm(args, s, ws, rank, local):
     flat = torch.empty(st.grad_numel(), dtype=torch.float32, device=dev)
     out = None
 
+    st.init_optimizer(lr=1e-4)
+
     def step():
         nonlocal out
         if s.method == "sft":
             out = st.sft_step(tok, cu, mask, float(mask_np.sum()), out)
         else:
             out = st.pref_step(s.method, tok, cu, mask, out)
-        L.check(L.lib().lora_grads(st.ctx, flat.data_ptr(), 1), st.ctx)
+        L.check(L.lib().lora_grads(st.ctx, flat.data_ptr(), 0), st.ctx)
+        st.optimizer_step(zero_grads=True)
 
-    for _ in range(args.warmup):
+    step()
+    if st.sync(600000) != 0:
+        raise RuntimeError(L.last_error(st.ctx))
+    loss_first = float(out["loss"].item())   # the optimizer then keeps training on this one batch
+    for _ in range(args.warmup - 1):
         step()
     if st.sync(600000) != 0:
         raise RuntimeError(L.last_error(st.ctx))
@@ -402,7 +409,7 @@ def run_gpu_arm(args, s, ws, rank, local):
         "profiled_ms_per_step": round(prof_step_ms, 3),
         "kernels_ms_per_step": {k: round(v["ms"] / K, 3) for k, v in p.items()},
         "kernels_share": {k: round(v["ms"] / total_prof_ms, 4) for k, v in p.items()} if total_prof_ms else {},
-        "loss": loss,
+        "loss_first_step": loss_first, "loss": loss,
         "clocks": clk.summary(),
     }
     st.close()

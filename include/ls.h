@@ -221,6 +221,21 @@ int stream_step_bwd(ls_ctx* ctx, const float* d_seq_coeffs);
  * layer in the order A_q, B_q, A_v, B_v, then zero the bound buffers if zero_after. */
 int lora_grads(ls_ctx* ctx, float* d_flat_out, int32_t zero_after);
 
+/* fp32 copy of every bound adapter tensor into d_flat_out, in lora_grads' order (the
+ * optimizer's master weights before its first step). */
+int lora_params(ls_ctx* ctx, float* d_flat_out);
+
+/* AdamW step on every bound adapter (the pages only say the optimizer is picked
+ * automatically, "Beyond Streaming" of Soup: Fine-Tune an 8B Model on a 4 GB GPU; this
+ * is the usual LoRA choice, Loshchilov & Hutter 2019): with g the bound fp32 gradient,
+ *   w = w (1 - lr wd);  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ *   w -= lr (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps)
+ * on fp32 master weights d_master, moments d_m, d_v (caller-owned, lora_grads' flat
+ * order; d_master from lora_params, d_m = d_v = 0 before step t = 1), then writes
+ * bf16(w) into the bound A/B buffers.  zero_grads = 1 clears the gradient buffers. */
+int lora_adamw(ls_ctx* ctx, float* d_master, float* d_m, float* d_v, int32_t step, float lr, float beta1,
+               float beta2, float eps, float weight_decay, int32_t zero_grads);
+
 /* Wait for the context's streams with a host-side time limit (ms; <= 0: no limit).
  * LS_ERR_TIMEOUT when the limit passes first; LS_ERR_DEVICE when a kernel raised
  * the device error flag. */

@@ -89,6 +89,8 @@ _SIGS = {
     "kto_loss": [P, P, P, P, I32, F32, F32, F32, P, P],
     "stream_step_bwd": [P, P],
     "lora_grads": [P, P, I32],
+    "lora_params": [P, P],
+    "lora_adamw": [P, P, P, P, I32, F32, F32, F32, F32, F32, I32],
     "ls_sync": [P, I32],
     "ls_stats": [P, C.POINTER(ls_stats_t), I32],
     "ls_debug_copy_delay": [P, I32],
@@ -97,6 +99,7 @@ _SIGS = {
     "ls_profile_read": [P, C.POINTER(ls_profile_t)],
     "lsk_nf4_dequant": [P, P, I64, I32, P, P],
     "lsk_nf4_gemm": [I32, P, I64, I32, P, P, I32, I32, P, P, I32, I32, P, I64, P, I64, I32, I32, P],
+    "lsk_gemm_cluster_mode": [I32],
     "lsk_rmsnorm_fwd": [P, P, P, P, I32, I32, F32, P],
     "lsk_rmsnorm_bwd": [P, P, P, P, P, P, I32, I32, I32, P],
     "ls_rope_table": [P, P, I32, I32, F32],

@@ -1332,6 +1332,59 @@ int lora_grads(ls_ctx* c, float* d_flat, int32_t zero_after) {
   return LS_OK;
 }
 
+int lora_params(ls_ctx* c, float* d_flat) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!d_flat) return fail(c, LS_ERR_ARG, "lora_params: null output");
+  size_t off = 0;
+  for (int l = 0; l < c->L; ++l) {
+    const ls_ctx::Ad& a = c->ad[l];
+    if (!a.on) continue;
+    const bf16* p4[4] = {a.aq, a.bq, a.av, a.bv};
+    const size_t n4[4] = {(size_t)c->r * c->H, (size_t)c->nq * c->r, (size_t)c->r * c->H, (size_t)c->nkvd * c->r};
+    for (int i = 0; i < 4; ++i) {
+      TIMED(LS_K_OTHER, 0, 6.0 * n4[i], 1,
+            ls::bf16_to_f32_kernel<<<grid1d((long long)n4[i], 256), 256, 0, c->cs>>>(p4[i], d_flat + off,
+                                                                                    (long long)n4[i]));
+      off += n4[i];
+    }
+  }
+  return LS_OK;
+}
+
+int lora_adamw(ls_ctx* c, float* d_master, float* d_m, float* d_v, int32_t step, float lr, float beta1, float beta2,
+               float eps, float wd, int32_t zero_grads) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!d_master || !d_m || !d_v || step < 1) return fail(c, LS_ERR_ARG, "lora_adamw: null state or step < 1");
+  const float bc1 = (float)(1.0 - std::pow((double)beta1, step));
+  const float bc2 = (float)(1.0 - std::pow((double)beta2, step));
+  long long off = 0;
+  for (int l = 0; l < c->L; ++l) {
+    const ls_ctx::Ad& a = c->ad[l];
+    if (!a.on) continue;
+    ls::AdamLayer L{};
+    float* g4[4] = {a.gaq, a.gbq, a.gav, a.gbv};
+    const bf16* p4[4] = {a.aq, a.bq, a.av, a.bv};
+    const long long n4[4] = {(long long)c->r * c->H, (long long)c->nq * c->r, (long long)c->r * c->H,
+                             (long long)c->nkvd * c->r};
+    long long nmax = 0;
+    for (int i = 0; i < 4; ++i) {
+      L.g[i] = g4[i];
+      L.p[i] = const_cast<bf16*>(p4[i]);   // the caller bound these buffers and owns them
+      L.off[i] = off;
+      L.n[i] = n4[i];
+      off += n4[i];
+      nmax = std::max(nmax, n4[i]);
+    }
+    dim3 grid(grid1d(nmax, 256, 148), 4);
+    TIMED(LS_K_OTHER, 0, 22.0 * (n4[0] + n4[1] + n4[2] + n4[3]), 1,
+          ls::adamw_layer_kernel<<<grid, 256, 0, c->cs>>>(L, d_master, d_m, d_v, lr, beta1, beta2, eps, wd, bc1, bc2,
+                                                         zero_grads));
+  }
+  return LS_OK;
+}
+
 int ls_sync(ls_ctx* c, int32_t timeout_ms) {
   if (!c) return set_thread_err(LS_ERR_ARG, "null context");
   cudaEvent_t e[2];
@@ -1468,6 +1521,12 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
            reinterpret_cast<const bf16*>(ext_b), ext_k, epi, out, ldo, reinterpret_cast<const bf16*>(residual), ldr,
            STREAM(s), force_bn, force_nacc));
   return LS_OK;
+}
+
+int lsk_gemm_cluster_mode(int32_t mode) {
+  const int old = ls::gemm_cluster_mode();
+  if (mode >= 0 && mode <= 2) ls::gemm_cluster_mode() = mode;
+  return old;
 }
 
 int lsk_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, float* rstd, int32_t T, int32_t H, float eps,

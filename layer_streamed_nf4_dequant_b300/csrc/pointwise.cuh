@@ -390,6 +390,44 @@ __global__ void pref_loss_kernel(int kind, const float* __restrict__ pi, const f
   }
 }
 
+// ------------------------------------------------------------------ optimizer
+// AdamW on the four adapter tensors of one layer (A_q, B_q, A_v, B_v), in place:
+// fp32 master / first / second moments at flat offsets, bf16 copy for the forward,
+// optional zeroing of the gradient.  bc1 = 1 - beta1^t, bc2 = 1 - beta2^t.
+struct AdamLayer {
+  float* g[4];
+  __nv_bfloat16* p[4];
+  long long off[4], n[4];
+};
+
+__global__ void adamw_layer_kernel(AdamLayer L, float* __restrict__ master, float* __restrict__ m1,
+                                   float* __restrict__ m2, float lr, float beta1, float beta2, float eps, float wd,
+                                   float bc1, float bc2, int zero_grads) {
+  const int tsel = blockIdx.y;
+  const long long n = L.n[tsel];
+  float* g = L.g[tsel];
+  __nv_bfloat16* p = L.p[tsel];
+  const long long off = L.off[tsel];
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const float gi = g[i];
+    float w = master[off + i] * (1.f - lr * wd);
+    const float a = beta1 * m1[off + i] + (1.f - beta1) * gi;
+    const float b = beta2 * m2[off + i] + (1.f - beta2) * gi * gi;
+    w -= lr * (a / bc1) / (sqrtf(b / bc2) + eps);
+    master[off + i] = w;
+    m1[off + i] = a;
+    m2[off + i] = b;
+    p[i] = __float2bfloat16_rn(w);
+    if (zero_grads) g[i] = 0.f;
+  }
+}
+
+// fp32 copy of one bf16 tensor (the optimizer's master weights at start).
+__global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* __restrict__ out, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    out[i] = __bfloat162float(in[i]);
+}
+
 // ------------------------------------------------------------------ LoRA pieces
 // Rank-r projections of the LoRA branch (Soup's soup.yaml listing: r 16 on q_proj and
 // v_proj), as one small contraction with N = 2 x 16 output columns:

@@ -227,6 +227,22 @@ class Stack:
                  for k in ("aq", "bq", "av", "bv")]
             self.set_adapter(l, *t)
 
+    def init_optimizer(self, lr: float = 1e-4, betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0):
+        """AdamW state for the bound adapters: fp32 master (from the bf16 factors) and moments."""
+        n = self.grad_numel()
+        self.opt = {"master": torch.empty(n, dtype=torch.float32, device=self.dev),
+                    "m": torch.zeros(n, dtype=torch.float32, device=self.dev),
+                    "v": torch.zeros(n, dtype=torch.float32, device=self.dev),
+                    "step": 0, "lr": lr, "betas": betas, "eps": eps, "wd": weight_decay}
+        check(lib().lora_params(self.ctx, self.opt["master"].data_ptr()), self.ctx)
+
+    def optimizer_step(self, zero_grads: bool = True):
+        """One AdamW step on every bound adapter from its accumulated gradient."""
+        o = self.opt
+        o["step"] += 1
+        check(lib().lora_adamw(self.ctx, o["master"].data_ptr(), o["m"].data_ptr(), o["v"].data_ptr(), o["step"],
+                               o["lr"], o["betas"][0], o["betas"][1], o["eps"], o["wd"], int(zero_grads)), self.ctx)
+
     def grad_numel(self) -> int:
         s = self.s
         return s.layers * (2 * s.lora_r * s.hidden + s.lora_r * (s.heads + s.kv_heads) * s.head_dim)
@@ -345,7 +361,8 @@ class Stack:
         pinned) token, offset and mask buffers.
 
         Copies the batch to the device on the compute stream, runs the streamed step,
-        gathers the LoRA gradients into grads_out (zeroing the bound buffers), and
+        gathers the LoRA gradients into grads_out, applies the AdamW step when
+        init_optimizer was called (the gradient buffers are cleared either way), and
         copies the loss back into h_loss (fp32 [1] host).  Waits for the loss before
         returning it, like a training loop that logs every step.
         """
@@ -364,7 +381,14 @@ class Stack:
             else:
                 o = self.pref_step(method, d["tok"], d["cu"], d["mask"], d.get("out"))
             d["out"] = o
-            check(lib().lora_grads(self.ctx, grads_out.data_ptr() if grads_out is not None else None, 1), self.ctx)
+            if getattr(self, "opt", None) is not None:
+                # gradients feed the optimizer, which clears them
+                if grads_out is not None:
+                    check(lib().lora_grads(self.ctx, grads_out.data_ptr(), 0), self.ctx)
+                self.optimizer_step(zero_grads=True)
+            else:
+                check(lib().lora_grads(self.ctx, grads_out.data_ptr() if grads_out is not None else None, 1),
+                      self.ctx)
             if h_loss is None:
                 h_loss = torch.empty(1, dtype=torch.float32, pin_memory=True)
             h_loss.copy_(o["loss"], non_blocking=True)

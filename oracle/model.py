@@ -418,3 +418,18 @@ def lora_linear_step(x: np.ndarray, w_deq: np.ndarray, a: np.ndarray, b: np.ndar
     y = linear(X, t64(w_deq), (lora_u(X, A, s), B))
     (y * t64(dy)).sum().backward()
     return dict(y=y.detach(), dx=X.grad, da=A.grad, db=B.grad)
+
+
+# --------------------------------------------------------------------------- optimizer
+
+def adamw_update(p: torch.Tensor, g: torch.Tensor, m: torch.Tensor, v: torch.Tensor, step: int, lr: float,
+                 beta1: float, beta2: float, eps: float, weight_decay: float) -> None:
+    """One AdamW step in place (fp64): decoupled weight decay p -= lr wd p, then the
+    bias-corrected Adam update (Loshchilov & Hutter 2019).  The pages only say the
+    optimizer is picked automatically; this is the usual choice for LoRA."""
+    p.mul_(1.0 - lr * weight_decay)
+    m.mul_(beta1).add_((1.0 - beta1) * g)
+    v.mul_(beta2).add_((1.0 - beta2) * g * g)
+    mh = m / (1.0 - beta1 ** step)
+    vh = v / (1.0 - beta2 ** step)
+    p.sub_(lr * mh / (torch.sqrt(vh) + eps))

@@ -437,3 +437,29 @@ def test_adapter_export_import_round_trip(tmp_path):
         st.close()
     assert torch.equal(lps[0], lps[1])
     assert not torch.equal(lps[1], lps[2])
+
+
+def test_adamw_step_matches_oracle():
+    """Two AdamW steps on the bound adapters from the GPU's own gradients, against the
+    oracle's AdamW applied to the same gradients (fp32 vs fp64); the bf16 factors the
+    forward reads are the rounded master weights."""
+    cfg = SMALL_DPO
+    tok, cu, mask = _batch(cfg)
+    st = _stack(cfg)
+    st.init_optimizer(lr=1e-3, betas=(0.9, 0.99), eps=1e-8, weight_decay=0.1)
+    p = torch.from_numpy(to_np(st.opt["master"]))
+    m = torch.zeros_like(p)
+    v = torch.zeros_like(p)
+    for t in (1, 2):
+        t_, c_, m_ = st.upload_batch(tok, cu, mask)
+        st.dpo_step(t_, c_, m_, cfg.beta)
+        g = st.grads(zero_after=False)
+        st.optimizer_step(zero_grads=True)
+        assert st.sync(60000) == 0, L.last_error(st.ctx)
+        om.adamw_update(p, torch.from_numpy(to_np(g)), m, v, t, 1e-3, 0.9, 0.99, 1e-8, 0.1)
+        assert rel_err(to_np(st.opt["master"]), p.numpy()) <= 1e-5
+        assert float(torch.from_numpy(to_np(st.grads())).abs().max()) == 0.0     # cleared
+    flat_bf16 = torch.cat([st.adapters[l][k].float().ravel() for l in range(cfg.layers)
+                           for k in ("aq", "bq", "av", "bv")])
+    assert torch.equal(flat_bf16, st.opt["master"].to(torch.bfloat16).float())
+    st.close()

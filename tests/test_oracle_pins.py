@@ -554,3 +554,20 @@ def test_preference_grads_finite_differences(method):
                     fd = (lp_ - lm_) / (2 * h)
                     scale = float(g.abs().max()) + 1e-12
                     assert abs(fd - float(g[idx])) <= 1e-6 * scale + 1e-9, (li, pi_, idx, fd, float(g[idx]))
+
+
+def test_adamw_matches_torch_optim():
+    """The oracle's AdamW against torch.optim.AdamW (fp64) over three steps."""
+    rng = np.random.default_rng(5)
+    p0 = torch.from_numpy(rng.normal(size=(7, 5)))
+    grads = [torch.from_numpy(rng.normal(size=(7, 5))) for _ in range(3)]
+    q = p0.clone().requires_grad_(True)
+    opt = torch.optim.AdamW([q], lr=1e-2, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.05)
+    p = p0.clone()
+    m = torch.zeros_like(p)
+    v = torch.zeros_like(p)
+    for t, g in enumerate(grads, start=1):
+        q.grad = g.clone()
+        opt.step()
+        M.adamw_update(p, g, m, v, t, 1e-2, 0.9, 0.999, 1e-8, 0.05)
+        np.testing.assert_allclose(p.numpy(), q.detach().numpy(), rtol=1e-12, atol=1e-15)
