@@ -104,7 +104,7 @@ static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
 // Process-wide switch for the paired-CTA tiles: 0 automatic, 1 never, 2 whenever the
 // tile allows it (a tuning / measurement knob; results are identical either way).
 inline int& gemm_cluster_mode() {
-  static int mode = 0;
+  static int mode = 1;
   return mode;
 }
 
