@@ -280,6 +280,12 @@ def run_gpu_arm(args, s, ws, rank, local):
     st = L.Stack(s, device=str(dev))
     st.load_synthetic(synth, seed=0)
     st.set_adapters_synthetic(synth, seed=0)
+    layer_file = None
+    if args.stream_source == "file":
+        # the NVMe tier: layer images in a file, read through pinned staging buffers
+        layer_file = os.path.join(args.file_dir or tempfile.gettempdir(), f"ls_layers_{os.getpid()}_{rank}.bin")
+        st.write_layer_file(layer_file)
+        st.use_layer_file(layer_file, nbuf=3)
     t_load = time.perf_counter() - t_load
     data_seed = rank  # weak scaling: each replica trains on its own pair
     tok_np, cu_np, mask_np = synth.tokens(s, data_seed), synth.seq_offsets(s), synth.loss_mask(s)
@@ -379,11 +385,17 @@ def run_gpu_arm(args, s, ws, rank, local):
                                                             "kernel_launches", "slot_reuses")}
     roof = step_roofline_ms(s, {"slot_bytes_layer": layer_img}, s.tokens, s.nseq, s.seq_len, s.method,
                             tf_peak, link, st.shared_read)
+    if layer_file:
+        try:
+            os.unlink(layer_file)
+        except OSError:
+            pass
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{s.name} streamed NF4 LoRA {s.method.upper()}", "layers": s.layers,
+        "config": {"workload": f"{s.name} streamed NF4 LoRA {s.method.upper()}"
+                               + (" (layers from file)" if args.stream_source == "file" else ""), "layers": s.layers,
                    "hidden": s.hidden, "heads": s.heads, "kv_heads": s.kv_heads, "inter": s.inter,
                    "vocab": s.vocab, "lora_r": s.lora_r, "tokens_per_pass": s.tokens,
                    "seqs": s.nseq, "seq_len": s.seq_len, "prompt_len": s.prompt_len,
@@ -405,7 +417,10 @@ def run_gpu_arm(args, s, ws, rank, local):
                    "step_roofline_ms": round(roof["ms"], 3), "step_roofline_frac": round(roof["ms"] / step_ms, 4),
                    "step_algorithmic_tflop": round(roof["flop"] / 1e12, 3),
                    "workspace_bytes": int(st.ws_bytes), "peak_device_bytes": int(torch.cuda.max_memory_allocated(dev)),
-                   "load_s": round(t_load, 1)},
+                   "load_s": round(t_load, 1), "source": args.stream_source,
+                   **({"file_gb_per_step": round(stats["file_bytes"] / K / 1e9, 3),
+                       "file_read_gbs": round(stats["file_bytes"] / max(1e-9, stats["file_read_ms"] * 1e-3) / 1e9, 2)}
+                      if args.stream_source == "file" else {})},
         "profiled_ms_per_step": round(prof_step_ms, 3),
         "kernels_ms_per_step": {k: round(v["ms"] / K, 3) for k, v in p.items()},
         "kernels_share": {k: round(v["ms"] / total_prof_ms, 4) for k, v in p.items()} if total_prof_ms else {},
@@ -480,6 +495,9 @@ def main():
                     help="training method on the config's pairs (default: the config's own)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm", default=None, help="micro-benchmark one NF4 GEMM: mode,M,N,K[,bn,nacc]")
+    ap.add_argument("--stream-source", default="ram", choices=["ram", "file"],
+                    help="where the streamed decoder layers live: pinned host RAM, or a file (NVMe tier)")
+    ap.add_argument("--file-dir", default=None, help="directory of the layer file (default: the temp dir)")
     args = ap.parse_args()
     if args.gemm:
         print(json.dumps(gemm_microbench(args.gemm, max(1, args.steps))), flush=True)

@@ -132,6 +132,22 @@ int ls_layer_layout(const ls_config* cfg, uint64_t* offsets16, uint64_t* image_b
  * LS_ERR_ARG.  The layer is copied to a device slot each time a pass needs it. */
 int load_layer_nf4(ls_ctx* ctx, int32_t layer, const ls_layer_host* h_layer);
 
+/* File-backed layers (the pages' `stream_source` tier: the base on NVMe when host RAM
+ * is short; Soup: Fine-Tune an 8B Model on a 4 GB GPU, "The Core Idea: Layer
+ * Streaming" and the soup.yaml listing; evermx.com summary).  The layer's slot image
+ * (ls_layer_layout) starts at byte `offset` of the file at `path`.  Each time a pass
+ * needs the layer it is read on the host (pread; O_DIRECT, bypassing the page cache,
+ * when the file system allows it and offset is 4 KiB-aligned) into the next pinned
+ * staging buffer, then copied to the slot like a RAM-backed layer, one item ahead of
+ * the compute that needs it.  The file must stay unchanged until ls_destroy; results
+ * are bit-identical to the same image held in pinned RAM.  Needs ls_set_staging. */
+int load_layer_file(ls_ctx* ctx, int32_t layer, const char* path, uint64_t offset);
+
+/* Staging for file-backed layers: nbuf (2..16) caller-owned pinned host buffers of
+ * bytes_each (>= the layer image rounded up to 4 KiB, a multiple of 4 KiB), at
+ * h_pinned (4 KiB-aligned, consecutive), kept until ls_destroy. */
+int ls_set_staging(ls_ctx* ctx, void* h_pinned, uint64_t bytes_each, int32_t nbuf);
+
 /* Register the embedding, vocabulary head and final norm (same rules as above).
  * The final-norm weight is copied to the device here. */
 int load_vocab_nf4(ls_ctx* ctx, const ls_vocab_host* h_vocab);
@@ -252,6 +268,8 @@ typedef struct ls_stats_t {
   int32_t vocab_chunks;
   int32_t vocab_chunk_rows;
   uint64_t kernel_launches; /* kernels this context enqueued                         */
+  uint64_t file_bytes;      /* layer-image bytes read from files (load_layer_file)     */
+  double file_read_ms;      /* host time spent in those reads                          */
 } ls_stats_t;
 
 /* Counters since ls_create (or the last reset). */

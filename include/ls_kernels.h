@@ -39,12 +39,6 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
                  int32_t ext_k, int32_t epi, void* out, int64_t ldo, const uint16_t* residual, int64_t ldr,
                  int32_t force_bn, int32_t force_nacc, void* stream);
 
-/* Tuning switch of the fused GEMM (process-wide): 0 automatic, 1 never (default), 2
- * always pair two CTAs of a cluster on one 256 x 256 weight tile (each dequantises
- * half of it into both CTAs' shared memory).  Results are bit-identical either way;
- * the switch exists to measure the two forms.  Returns the previous mode. */
-int lsk_gemm_cluster_mode(int32_t mode);
-
 /* RMSNorm: y = bf16(w * bf16(x * rstd)), rstd = 1/sqrt(mean(x^2) + eps) (fp32).
  * x, y bf16 [T, H] (H % 8 == 0), w bf16 [H], rstd fp32 [T] (may be NULL). */
 int lsk_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, float* rstd, int32_t T, int32_t H,

@@ -51,7 +51,7 @@ class ls_stats_t(C.Structure):
     _fields_ = [("layer_reads", C.c_uint64), ("vocab_reads", C.c_uint64), ("h2d_bytes", C.c_uint64),
                 ("slot_reuses", C.c_uint64), ("workspace_bytes", C.c_uint64), ("slot_bytes", C.c_uint64),
                 ("act_store_bytes", C.c_uint64), ("vocab_chunks", C.c_int32), ("vocab_chunk_rows", C.c_int32),
-                ("kernel_launches", C.c_uint64)]
+                ("kernel_launches", C.c_uint64), ("file_bytes", C.c_uint64), ("file_read_ms", C.c_double)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -78,6 +78,8 @@ _SIGS = {
     "nf4_quantize": [P, I64, I64, P, P, I32],
     "load_layer_nf4": [P, I32, C.POINTER(ls_layer_host)],
     "load_vocab_nf4": [P, C.POINTER(ls_vocab_host)],
+    "load_layer_file": [P, I32, C.c_char_p, U64],
+    "ls_set_staging": [P, P, U64, I32],
     "ls_set_adapter": [P, I32, P, P, P, P, P, P, P, P],
     "stream_step_fwd": [P, P, I32, I32, P, P, I32, I32, P],
     "stream_step_fwd_dpo": [P, P, I32, I32, P, P, P, P],
@@ -99,7 +101,6 @@ _SIGS = {
     "ls_profile_read": [P, C.POINTER(ls_profile_t)],
     "lsk_nf4_dequant": [P, P, I64, I32, P, P],
     "lsk_nf4_gemm": [I32, P, I64, I32, P, P, I32, I32, P, P, I32, I32, P, I64, P, I64, I32, I32, P],
-    "lsk_gemm_cluster_mode": [I32],
     "lsk_rmsnorm_fwd": [P, P, P, P, I32, I32, F32, P],
     "lsk_rmsnorm_bwd": [P, P, P, P, P, P, I32, I32, I32, P],
     "ls_rope_table": [P, P, I32, I32, F32],

@@ -47,10 +47,10 @@ struct GemmCall {
   GemmArgs g;
 };
 
-template <int NACC, int BN, int S, int SB, int MODE, int CL = 1>
+template <int NACC, int BN, int S, int SB, int MODE>
 static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
-  using C = GemmCfg<NACC, BN, S, SB, CL>;
-  auto kern = nf4_gemm_kernel<NACC, BN, S, SB, MODE, CL>;
+  using C = GemmCfg<NACC, BN, S, SB>;
+  auto kern = nf4_gemm_kernel<NACC, BN, S, SB, MODE>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -62,7 +62,6 @@ static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
   if (!make_map_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.A, (uint64_t)g.Kred, (uint64_t)g.M,
                    (uint64_t)c.lda * 2, 64, C::BM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // each CTA loads its share of the weight tile: UNITS rows (FWD) / UNITS columns (DX)
   if (MODE == GEMM_FWD) {
     if (!make_map_2d(&tW, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.Wp, (uint64_t)g.Kw / 2, (uint64_t)g.Nw,
                      (uint64_t)g.Kw / 2, 32, C::UNITS, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -79,33 +78,16 @@ static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
   } else {
     tX = tA;
   }
-  const unsigned mt = (unsigned)((g.M + C::BM - 1) / C::BM);
-  dim3 grid((mt + CL - 1) / CL * CL, (g.Nout + BN - 1) / BN);
-  if (CL == 1) {
-    kern<<<grid, C::THREADS, C::SMEM, st>>>(tA, tW, tX, g);
-    return cudaGetLastError();
-  }
-  // a pair of CTAs along M per cluster (rows past M are zero-filled by TMA, not stored)
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = grid;
-  lc.blockDim = dim3(C::THREADS);
-  lc.dynamicSmemBytes = C::SMEM;
-  lc.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = CL;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  lc.attrs = at;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, kern, tA, tW, tX, g);
-}
-
-// Process-wide switch for the paired-CTA tiles: 0 automatic, 1 never, 2 whenever the
-// tile allows it (a tuning / measurement knob; results are identical either way).
-inline int& gemm_cluster_mode() {
-  static int mode = 1;
-  return mode;
+  // Tile order: consecutive CTAs (one wave) share the operand that is walked slowly.
+  // M-fastest keeps each weight tile in L2 for all row tiles; when the activation
+  // operand is the larger one (long reductions, e.g. the 32B down-projection's dX) the
+  // N-fastest order lets a wave share activation tiles instead.
+  GemmArgs ga = g;
+  ga.n_fast = (double)g.M * g.Kred * 2.0 > (double)g.Nw * g.Kw * 0.5625;
+  const unsigned tm = (unsigned)((g.M + C::BM - 1) / C::BM), tn = (unsigned)((g.Nout + BN - 1) / BN);
+  dim3 grid = ga.n_fast ? dim3(tn, tm) : dim3(tm, tn);
+  kern<<<grid, C::THREADS, C::SMEM, st>>>(tA, tW, tX, ga);
+  return cudaGetLastError();
 }
 
 // Pick the tile shape.  Each CTA dequantises its BN x 64 weight tile once per k-step,
@@ -148,13 +130,6 @@ static cudaError_t launch_nf4_gemm(const GemmCall& c, cudaStream_t st) {
   choose_tile(c.mode, g.M, g.Nout, nacc, bn);
   if (c.force_bn) bn = c.force_bn;
   if (c.force_nacc) nacc = c.force_nacc;
-  // paired CTAs for 256 x 256 tiles when there are at least two row tiles to pair
-  const int cm = gemm_cluster_mode();
-  const bool pair = nacc == 2 && bn == 256 && cm != 1 && (cm == 2 || (g.M + 255) / 256 >= 2);
-  if (pair) {
-    if (c.mode == GEMM_FWD) return launch_cfg<2, 256, 4, 2, GEMM_FWD, 2>(c, st);
-    return launch_cfg<2, 256, 4, 2, GEMM_DX, 2>(c, st);
-  }
   if (c.mode == GEMM_FWD) {
     if (nacc == 2 && bn == 256) return launch_cfg<2, 256, 3, 2, GEMM_FWD>(c, st);
     if (nacc == 2 && bn == 128) return launch_cfg<2, 128, 4, 2, GEMM_FWD>(c, st);

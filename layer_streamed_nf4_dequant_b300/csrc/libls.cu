@@ -16,6 +16,9 @@
 #include <cstdio>
 #include <cstring>
 #include <functional>
+#include <fcntl.h>
+#include <unistd.h>
+#include <cerrno>
 #include <mutex>
 #include <string>
 #include <thread>
@@ -43,6 +46,8 @@ int set_thread_err(int code, const std::string& m) {
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr int kLoraSplitMax = 4;   // K slices of the LoRA projections (workspace scratch)
 
 // ------------------------------------------------------------------ host NF4 quantiser
 // QLoRA's NormalFloat-4 code values (Dettmers et al. 2023, Appendix E).
@@ -120,6 +125,19 @@ struct ls_ctx {
 
   std::vector<ls_layer_host> hl;
   std::vector<char> hl_ok;
+  // file-backed layers (the "NVMe" tier): slot image at byte offset of a file
+  struct FileSrc {
+    int fd = -1;
+    bool direct = false;
+    uint64_t off = 0;
+  };
+  std::vector<FileSrc> lf;
+  std::vector<std::pair<std::string, std::pair<int, int>>> files;   // path -> (O_DIRECT fd, buffered fd)
+  std::vector<uint8_t*> stage;            // caller's pinned staging buffers
+  std::vector<cudaEvent_t> stage_ev;      // H2D copy out of each buffer
+  std::vector<char> stage_used;
+  size_t stage_bytes = 0;
+  int stage_next = 0;
   ls_vocab_host hv{};
   bool hv_ok = false;
   const uint8_t* emb_p = nullptr;   // device-visible pointers to the mapped pinned embedding
@@ -157,6 +175,8 @@ struct ls_ctx {
   const float* last_lse = nullptr;
 
   ls_stats_t st{};
+  double file_ms = 0.0;
+  uint64_t file_bytes = 0;
   int copy_delay_ms = 0;
 
   // per-launch CUDA-event timing on the compute stream (ls_profile)
@@ -373,7 +393,8 @@ Planned lay_out(const ls_config& k, ls_ctx* c) {
   bf16* duext = b.take<bf16>(T * 64);
   bf16* extb = b.take<bf16>(H * 64);
   const int chunks = (int)((T + 127) / 128);
-  const size_t lpf = (size_t)chunks * std::max(nqkv, H) * 16;
+  // LoRA scratch: outer-product partials, and the K-split partials of the projections
+  const size_t lpf = std::max((size_t)chunks * std::max(nqkv, H) * 16, (size_t)kLoraSplitMax * T * 32);
   float* lpart = b.take<float>(lpf);
   // union: layer-backward big buffers / vocabulary dlogits
   const size_t u0 = align_up(b.off, 256);
@@ -528,20 +549,33 @@ cudaError_t lora_outer(const bf16* X, long long ldx, int ncols, const float* Uf,
   return cudaGetLastError();
 }
 
+// LoRA projection: with scratch (>= nsplit * T * 32 floats) K is split over
+// kLoraSplit blocks per 16-row tile and reduced in slice order by a second kernel
+// (more blocks in flight); without it, one block per tile.
+constexpr int kLoraSplit = kLoraSplitMax;
+
+cudaError_t lora_proj(const bf16* X, long long ldx, int T, ls::LoraProjHalf h0, ls::LoraProjHalf h1, int r, float s,
+                      float* out_f32, bf16* out_ext, float* scratch, cudaStream_t st) {
+  const int ns = scratch ? kLoraSplit : 1;
+  ls::lora_proj_kernel<<<dim3((T + 15) / 16, ns), 256, 0, st>>>(X, ldx, T, h0, h1, r, s, out_f32, out_ext, scratch);
+  if (ns > 1)
+    ls::lora_proj_reduce_kernel<<<(T * 32 + 255) / 256, 256, 0, st>>>(scratch, ns, T, s, out_f32, out_ext);
+  return cudaGetLastError();
+}
+
 // LoRA down-projection u_ext = [bf16(s x A_q^T) | bf16(s x A_v^T) | 0].
 cudaError_t lora_down(const bf16* x, long long ldx, const bf16* aq, const bf16* av, int r, int K, float s,
-                      bf16* u_ext, int T, cudaStream_t st) {
+                      bf16* u_ext, int T, cudaStream_t st, float* scratch = nullptr) {
   ls::LoraProjHalf h0{aq, (long long)K, 0, K, 0}, h1{av, (long long)K, 0, K, 0};
-  ls::lora_proj_kernel<<<(T + 15) / 16, 256, 0, st>>>(x, ldx, T, h0, h1, r, s, nullptr, u_ext);
-  return cudaGetLastError();
+  return lora_proj(x, ldx, T, h0, h1, r, s, nullptr, u_ext, scratch, st);
 }
 
 // du = s [dY_q B_q | dY_v B_v] (fp32 [T, 32]) and its bf16 extra-stage copy du_ext [T, 64].
 cudaError_t lora_du(const bf16* dy, long long ldy, int col_q, int nq, const bf16* bq, int col_v, int nv,
-                    const bf16* bv, int r, float s, float* du, bf16* du_ext, int T, cudaStream_t st) {
+                    const bf16* bv, int r, float s, float* du, bf16* du_ext, int T, cudaStream_t st,
+                    float* scratch = nullptr) {
   ls::LoraProjHalf h0{bq, 0, col_q, nq, 1}, h1{bv, 0, col_v, nv, 1};
-  ls::lora_proj_kernel<<<(T + 15) / 16, 256, 0, st>>>(dy, ldy, T, h0, h1, r, s, du, du_ext);
-  return cudaGetLastError();
+  return lora_proj(dy, ldy, T, h0, h1, r, s, du, du_ext, scratch, st);
 }
 
 void CUDART_CB host_sleep(void* p) {
@@ -562,8 +596,55 @@ size_t item_layer_component_bytes(const ls_ctx* c, int m, bool absmax) {
   return absmax ? rows[m] * (cols[m] / 64) * 4 : rows[m] * cols[m] / 2;
 }
 
+// Read a file-backed layer image into the next pinned staging buffer (host, now) and
+// enqueue its copy into the slot.  The buffer is reused only after its previous copy
+// has finished (bounded host wait).  O_DIRECT reads bypass the page cache where the
+// file system allows them; the image is read whole (rounded up to 4 KiB).
+int copy_item_file(ls_ctx* c, int item, uint8_t* img, cudaStream_t st) {
+  if (c->stage.empty()) return fail(c, LS_ERR_STATE, "file-backed layer without staging buffers (ls_set_staging)");
+  const int k = c->stage_next;
+  c->stage_next = (k + 1) % (int)c->stage.size();
+  if (c->stage_used[k]) {
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+      const cudaError_t q = cudaEventQuery(c->stage_ev[k]);
+      if (q == cudaSuccess) break;
+      if (q != cudaErrorNotReady) return fail(c, LS_ERR_CUDA, std::string("staging wait: ") + cudaGetErrorString(q));
+      if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(120))
+        return fail(c, LS_ERR_TIMEOUT, "staging buffer still being copied after 120 s");
+      std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+  }
+  const ls_ctx::FileSrc& f = c->lf[item];
+  const size_t n = c->lay.bytes;
+  const size_t want = f.direct ? align_up(n, 4096) : n;
+  const auto t0 = std::chrono::steady_clock::now();
+  size_t got = 0;
+  while (got < want) {
+    const ssize_t r = pread(f.fd, c->stage[k] + got, want - got, (off_t)(f.off + got));
+    if (r < 0) {
+      if (errno == EINTR) continue;
+      return fail(c, LS_ERR_ARG, std::string("layer file read: ") + strerror(errno));
+    }
+    if (r == 0) {
+      if (got >= n) break;   // the padding past the last image may be missing
+      return fail(c, LS_ERR_ARG, "layer file shorter than its image");
+    }
+    got += (size_t)r;
+  }
+  c->file_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  c->file_bytes += n;
+  CK(cudaMemcpyAsync(img, c->stage[k], n, cudaMemcpyHostToDevice, st));
+  CK(cudaEventRecord(c->stage_ev[k], st));
+  c->stage_used[k] = 1;
+  c->st.layer_reads++;
+  c->st.h2d_bytes += n;
+  return LS_OK;
+}
+
 int copy_item(ls_ctx* c, int item, uint8_t* img, cudaStream_t st) {
   if (c->copy_delay_ms > 0) CK(cudaLaunchHostFunc(st, host_sleep, &c->copy_delay_ms));
+  if (item < c->L && c->lf[item].fd >= 0) return copy_item_file(c, item, img, st);
   if (item < c->L) {
     const ls_layer_host& h = c->hl[item];
     const ls_nf4_host* m7[7] = {&h.q, &h.k, &h.v, &h.o, &h.gate, &h.up, &h.down};
@@ -701,8 +782,8 @@ int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16*
   const ls_ctx::Ad& a = c->ad[layer];
   const bool use = adapter && a.on;
   if (use) {
-    TIMED(LS_K_OTHER, 2.0 * lora_rows * 2 * c->r * H, 2.0 * lora_rows * H, 1,
-          lora_down(c->n1, H, a.aq, a.av, c->r, H, c->cfg.lora_scale, c->u_ext, lora_rows, st));
+    TIMED(LS_K_OTHER, 2.0 * lora_rows * 2 * c->r * H, 2.0 * lora_rows * H, 2,
+          lora_down(c->n1, H, a.aq, a.av, c->r, H, c->cfg.lora_scale, c->u_ext, lora_rows, st, c->lora_part));
     const int n = c->nqkv * 64;
     TIMED(LS_K_OTHER, 0, 2.0 * n, 1,
           ls::build_ext_fwd_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.bq, 0, c->nq, a.bv, c->nq + c->nkvd, c->nkvd,
@@ -781,9 +862,9 @@ int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int 
   const bool use = a.on;
   if (use) {
     const float s = c->cfg.lora_scale;
-    TIMED(LS_K_OTHER, 2.0 * T * (c->nq + c->nkvd) * c->r, 2.0 * T * (c->nq + c->nkvd), 1,
+    TIMED(LS_K_OTHER, 2.0 * T * (c->nq + c->nkvd) * c->r, 2.0 * T * (c->nq + c->nkvd), 2,
           lora_du(c->dqkv_bf, c->nqkv, 0, c->nq, a.bq, c->nq + c->nkvd, c->nkvd, a.bv, c->r, s, c->du, c->du_ext,
-                  T, st));
+                  T, st, c->lora_part));
     // dB = dY^T u ;  dA = (s du)^T x
     GEMM_T(LS_K_OTHER, 2.0 * T * c->nq * c->r, 2.0 * T * c->nq,
            lora_outer(c->dqkv_bf, c->nqkv, c->nq, nullptr, c->u_ext, 64, c->r, T, 0, 1, c->lora_part, 128, a.gbq, st));
@@ -881,6 +962,7 @@ int ls_create(const ls_config* cfg, void* d_workspace, uint64_t ws_bytes, void* 
   Planned p = lay_out(*cfg, c);
   c->hl.assign(c->L, ls_layer_host{});
   c->hl_ok.assign(c->L, 0);
+  c->lf.assign(c->L, ls_ctx::FileSrc{});
   c->ad.assign(c->L, ls_ctx::Ad{});
   c->st.workspace_bytes = p.total;
   c->st.slot_bytes = p.slot_bytes;
@@ -918,6 +1000,12 @@ int ls_destroy(ls_ctx* c) {
   }
   for (auto& e : c->prof_ev)
     if (e) cudaEventDestroy(e);
+  for (auto& e : c->stage_ev)
+    if (e) cudaEventDestroy(e);
+  for (auto& f : c->files) {
+    if (f.second.first >= 0) close(f.second.first);
+    if (f.second.second >= 0) close(f.second.second);
+  }
   delete c;
   return LS_OK;
 }
@@ -969,6 +1057,60 @@ int load_layer_nf4(ls_ctx* c, int32_t layer, const ls_layer_host* h) {
   if ((rc = check_pinned(h->attn_norm, "attn_norm", why)) || (rc = check_pinned(h->mlp_norm, "mlp_norm", why)))
     return set_thread_err(rc, "load_layer_nf4: " + why);
   c->hl[layer] = *h;
+  c->hl_ok[layer] = 1;
+  c->lf[layer] = ls_ctx::FileSrc{};
+  if (c->cfg.resident) c->res_loaded[layer] = 0;
+  for (int s = 0; s < 2; ++s)
+    if (c->slot_item[s] == layer) c->slot_item[s] = -1;
+  return LS_OK;
+}
+
+int ls_set_staging(ls_ctx* c, void* h_pinned, uint64_t bytes_each, int32_t nbuf) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!h_pinned || nbuf < 2 || nbuf > 16 || bytes_each < align_up(c->lay.bytes, 4096) || bytes_each % 4096 ||
+      reinterpret_cast<uintptr_t>(h_pinned) % 4096)
+    return fail(c, LS_ERR_ARG, "ls_set_staging: need 2..16 page-aligned buffers of >= the 4 KiB-rounded layer image");
+  std::string why;
+  if ((rc = check_pinned(h_pinned, "staging", why))) return set_thread_err(rc, "ls_set_staging: " + why);
+  CK(cudaStreamSynchronize(c->cp));
+  for (auto& e : c->stage_ev)
+    if (e) cudaEventDestroy(e);
+  c->stage.clear();
+  c->stage_ev.assign(nbuf, nullptr);
+  c->stage_used.assign(nbuf, 0);
+  for (int i = 0; i < nbuf; ++i) {
+    c->stage.push_back(reinterpret_cast<uint8_t*>(h_pinned) + (size_t)i * bytes_each);
+    CK(cudaEventCreateWithFlags(&c->stage_ev[i], cudaEventDisableTiming));
+  }
+  c->stage_bytes = bytes_each;
+  c->stage_next = 0;
+  return LS_OK;
+}
+
+int load_layer_file(ls_ctx* c, int32_t layer, const char* path, uint64_t offset) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!path || layer < 0 || layer >= c->L) return fail(c, LS_ERR_ARG, "load_layer_file: bad layer or null path");
+  int fdd = -1, fdb = -1;
+  for (auto& f : c->files)
+    if (f.first == path) { fdd = f.second.first; fdb = f.second.second; }
+  if (fdb < 0) {
+    fdb = open(path, O_RDONLY | O_CLOEXEC);
+    if (fdb < 0) return set_thread_err(LS_ERR_ARG, std::string("load_layer_file: ") + path + ": " + strerror(errno));
+#ifdef O_DIRECT
+    fdd = open(path, O_RDONLY | O_CLOEXEC | O_DIRECT);   // -1 where the file system has no direct I/O
+#endif
+    c->files.push_back({path, {fdd, fdb}});
+  }
+  const off_t end = lseek(fdb, 0, SEEK_END);
+  if (end < 0 || (uint64_t)end < offset + c->lay.bytes)
+    return set_thread_err(LS_ERR_ARG, "load_layer_file: file shorter than offset + layer image");
+  ls_ctx::FileSrc f;
+  f.direct = fdd >= 0 && offset % 4096 == 0;
+  f.fd = f.direct ? fdd : fdb;
+  f.off = offset;
+  c->lf[layer] = f;
   c->hl_ok[layer] = 1;
   if (c->cfg.resident) c->res_loaded[layer] = 0;
   for (int s = 0; s < 2; ++s)
@@ -1423,10 +1565,14 @@ int ls_sync(ls_ctx* c, int32_t timeout_ms) {
 
 int ls_stats(ls_ctx* c, ls_stats_t* out, int32_t reset) {
   if (!c || !out) return set_thread_err(LS_ERR_ARG, "ls_stats: null argument");
+  c->st.file_bytes = c->file_bytes;
+  c->st.file_read_ms = c->file_ms;
   *out = c->st;
   if (reset) {
     c->st.layer_reads = c->st.vocab_reads = c->st.h2d_bytes = c->st.slot_reuses = 0;
     c->st.kernel_launches = 0;
+    c->file_bytes = 0;
+    c->file_ms = 0.0;
   }
   return LS_OK;
 }
@@ -1521,12 +1667,6 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
            reinterpret_cast<const bf16*>(ext_b), ext_k, epi, out, ldo, reinterpret_cast<const bf16*>(residual), ldr,
            STREAM(s), force_bn, force_nacc));
   return LS_OK;
-}
-
-int lsk_gemm_cluster_mode(int32_t mode) {
-  const int old = ls::gemm_cluster_mode();
-  if (mode >= 0 && mode <= 2) ls::gemm_cluster_mode() = mode;
-  return old;
 }
 
 int lsk_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, float* rstd, int32_t T, int32_t H, float eps,

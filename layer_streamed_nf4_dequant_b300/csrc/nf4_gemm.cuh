@@ -65,18 +65,15 @@ struct GemmArgs {
   float* tgt_logit;                  // EPI_LOGPROB: [M] logit of the target
   const float* lse;                  // EPI_DLOGITS: [M]
   const float* coef;                 // EPI_DLOGITS: [M] dL/dlogprob per row
+  int n_fast;                        // grid.x walks output-column tiles (CTAs of a wave share A rows)
 };
 
-// CL = 2: a cluster of two CTAs along M shares each dequantised weight tile -- every
-// CTA dequantises half of the BN rows (forward) / columns (input gradient) and stores
-// them into its own and its peer's B buffer, so the pair does the dequant work of one
-// tile for 2 x BM rows of A.
-template <int NACC, int BN, int S, int SB, int CL = 1>
+template <int NACC, int BN, int S, int SB>
 struct GemmCfg {
   static constexpr int BM = 128 * NACC;
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
-  static constexpr int UNITS = BN / CL;          // 64-element rows this CTA dequantises per k-step
+  static constexpr int UNITS = BN;               // 64-element rows dequantised per k-step
   static constexpr int W_BYTES = UNITS * 32;
   static constexpr int ABS_PER_STAGE = UNITS;
   static constexpr int NDQ_WARPS = 8;
@@ -99,7 +96,6 @@ struct GemmCfg {
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(FWD_GROUPS == 1 || (FWD_GROUPS == 2 && SB == 2), "dequant groups need one B buffer each");
-  static_assert(CL == 1 || (CL == 2 && BN == 256), "the CTA pair shares 256-wide tiles");
 };
 
 // -------------------------------------------------------------------------- dequantisers
@@ -141,11 +137,9 @@ __device__ __forceinline__ void nf4_lookup4(uint32_t v, const Nf4ByteTab& t, uin
 }
 
 // One 64-code row: codes at src (32 bytes, 16-byte aligned), one absmax, written as one
-// 128-byte row of the swizzled B tile (dst_off, swizzle phase sw) locally and, with a
-// peer (peer_row != 0), at the same offset of the peer CTA's B buffer.  h0 staggers the
+// 128-byte row of the swizzled B tile (dst_off, swizzle phase sw).  h0 staggers the
 // order of the two 16-byte code reads across neighbouring rows (bank spread).
-__device__ __forceinline__ void dequant_row(const uint8_t* src, float a, int h0, uint8_t* Bt, int dst_off, int sw,
-                                            uint32_t peer_Bt) {
+__device__ __forceinline__ void dequant_row(const uint8_t* src, float a, int h0, uint8_t* Bt, int dst_off, int sw) {
   const uint4 first = *reinterpret_cast<const uint4*>(src + h0 * 16);
   const uint4 second = *reinterpret_cast<const uint4*>(src + (h0 ^ 1) * 16);
   const uint4 w0 = h0 ? second : first, w1 = h0 ? first : second;
@@ -157,19 +151,16 @@ __device__ __forceinline__ void dequant_row(const uint8_t* src, float a, int h0,
     uint32_t o[4];
     nf4_lookup4(cw[c] & 0xFFFFu, t, o[0], o[1]);
     nf4_lookup4(cw[c] >> 16, t, o[2], o[3]);
-    const uint4 v = make_uint4(o[0], o[1], o[2], o[3]);
-    const int off = dst_off + ((c ^ sw) << 4);
-    *reinterpret_cast<uint4*>(Bt + off) = v;
-    if (peer_Bt) st_cluster_v4(peer_Bt + off, v);
+    *reinterpret_cast<uint4*>(Bt + dst_off + ((c ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
 // FWD: unit j = B-tile row base_row + j (output column n0 + base_row + j); its codes
 // are row j of this CTA's W tile (32 bytes per row), K-major SW128 destination.
 __device__ __forceinline__ void dequant_fwd_unit(const uint8_t* Wt, const float* absS, uint8_t* Bt, int j,
-                                                 int base_row, uint32_t peer_Bt) {
+                                                 int base_row) {
   const int jb = base_row + j;
-  dequant_row(Wt + j * 32, absS[j], (j >> 2) & 1, Bt, jb * 128, jb & 7, peer_Bt);
+  dequant_row(Wt + j * 32, absS[j], (j >> 2) & 1, Bt, jb * 128, jb & 7);
 }
 
 // DX, MN-major B tile.  For dX = dY . deq(W) the MMA's reduction runs over W's rows n
@@ -180,24 +171,22 @@ __device__ __forceinline__ void dequant_fwd_unit(const uint8_t* Wt, const float*
 // (1 KB), 8 atoms down the 64 rows (8 KB per 64 columns):
 //   offset = kbl*8192 + (n/8)*1024 + (n%8)*128 + chunk,  kbl = base_kb + j / 64.
 __device__ __forceinline__ void dequant_dx_unit(const uint8_t* Wt, const float* absS, uint8_t* Bt, int j, int wbytes,
-                                                int base_kb, uint32_t peer_Bt) {
+                                                int base_kb) {
   const int n = j & 63, kbl = j >> 6;
-  const int cb = wbytes / 32;   // 64-column blocks in this CTA's W tile
+  const int cb = wbytes / 32;   // 64-column blocks in the W tile
   dequant_row(Wt + n * wbytes + kbl * 32, absS[n * cb + kbl], (n >> 1) & 1, Bt,
-              (base_kb + kbl) * 8192 + (n >> 3) * 1024 + (n & 7) * 128, n & 7, peer_Bt);
+              (base_kb + kbl) * 8192 + (n >> 3) * 1024 + (n & 7) * 128, n & 7);
 }
 
 // LoRA extra stage: B_ext rows [row0, row0 + rows) (K-major, 64 wide) into the B tile.
 __device__ __forceinline__ void copy_ext_rows(const __nv_bfloat16* ext_b, int n0, int Nout, uint8_t* Bt, int row0,
-                                              int rows, int tq, int nthreads, uint32_t peer_Bt) {
+                                              int rows, int tq, int nthreads) {
   for (int u = tq; u < rows * 8; u += nthreads) {
     const int j = row0 + (u >> 3), c = u & 7;
     const int n = n0 + j;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (n < Nout) v = *reinterpret_cast<const uint4*>(ext_b + (size_t)n * 64 + c * 8);
-    const int off = j * 128 + ((c ^ (j & 7)) << 4);
-    *reinterpret_cast<uint4*>(Bt + off) = v;
-    if (peer_Bt) st_cluster_v4(peer_Bt + off, v);
+    *reinterpret_cast<uint4*>(Bt + j * 128 + ((c ^ (j & 7)) << 4)) = v;
   }
 }
 
@@ -220,17 +209,17 @@ __device__ __forceinline__ void store_bf16_32(__nv_bfloat16* dst, const float (&
 
 // -------------------------------------------------------------------------- kernel
 
-template <int NACC, int BN, int S, int SB, int MODE, int CL = 1>
-__global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
+template <int NACC, int BN, int S, int SB, int MODE>
+__global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX, const GemmArgs g) {
-  using C = GemmCfg<NACC, BN, S, SB, CL>;
+  using C = GemmCfg<NACC, BN, S, SB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * C::BM, n0 = blockIdx.y * BN;
+  const int m0 = (g.n_fast ? blockIdx.y : blockIdx.x) * C::BM, n0 = (g.n_fast ? blockIdx.x : blockIdx.y) * BN;
   const int KB = g.Kred / 64;
   const int KBw = g.Kw / 64;
   const int niter = KB + (g.ext_k > 0 ? 1 : 0);
@@ -241,9 +230,6 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
   auto bfull = [&](int s) { return bar0 + (2 * S + s) * 8; };
   auto bempty = [&](int s) { return bar0 + (2 * S + SB + s) * 8; };
   const uint32_t accfull = bar0 + (2 * S + 2 * SB) * 8;
-  // this CTA's share of the weight tile: rows (FWD) / columns (DX) [half0, half0 + UNITS)
-  const uint32_t rank = CL == 2 ? cluster_ctarank() : 0u;
-  const int half0 = (int)rank * C::UNITS;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -251,8 +237,8 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
       mbar_init(empty(s), 1);
     }
     for (int s = 0; s < SB; ++s) {
-      mbar_init(bfull(s), C::FWD_GROUP_WARPS * CL);   // every dequant warp of the pair arrives
-      mbar_init(bempty(s), CL);                       // every MMA issuer of the pair commits
+      mbar_init(bfull(s), C::FWD_GROUP_WARPS);
+      mbar_init(bempty(s), 1);
     }
     mbar_init(accfull, 1);
     fence_barrier_init();
@@ -269,7 +255,6 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CL == 2) cluster_sync_all();   // the peer's barriers exist before anything arrives on them
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
 
@@ -285,8 +270,8 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
           mbar_arrive_expect_tx(full(s), C::A_BYTES + C::W_BYTES);
           tma_load_2d(a_dst, &tmA, it * 64, m0, full(s));
           const uint32_t w_dst = sb + C::OFF_W + s * C::W_BYTES;
-          if (MODE == GEMM_FWD) tma_load_2d(w_dst, &tmW, it * 32, n0 + half0, full(s));
-          else tma_load_2d(w_dst, &tmW, (n0 + half0) / 2, it * 64, full(s));
+          if (MODE == GEMM_FWD) tma_load_2d(w_dst, &tmW, it * 32, n0, full(s));
+          else tma_load_2d(w_dst, &tmW, n0 / 2, it * 64, full(s));
         } else {
           mbar_arrive_expect_tx(full(s), C::A_BYTES);
           tma_load_2d(a_dst, &tmX, 0, m0, full(s));
@@ -296,7 +281,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
         const uint32_t abs_dst = sb + C::OFF_ABS + s * C::ABS_PER_STAGE * 4;
         if (MODE == GEMM_FWD) {
           for (int j = lane; j < C::UNITS; j += 32) {
-            const int n = n0 + half0 + j;
+            const int n = n0 + j;
             const float* src = n < g.Nw ? g.absmax + (size_t)n * KBw + it : g_zero_word;
             cp_async_4(abs_dst + j * 4, src);
           }
@@ -304,7 +289,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
           constexpr int CB = C::UNITS / 64;
           for (int e = lane; e < 64 * CB; e += 32) {
             const int r = e / CB, c = e % CB;
-            const int kb = (n0 + half0) / 64 + c;
+            const int kb = n0 / 64 + c;
             const float* src = kb < KBw ? g.absmax + (size_t)(it * 64 + r) * KBw + kb : g_zero_word;
             cp_async_4(abs_dst + e * 4, src);
           }
@@ -323,8 +308,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
       constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
       for (int it = 0; it < niter; ++it) {
         const int s = it % S, b = it % SB;
-        if (s_abort || !mbar_wait(full(s), (it / S) & 1) ||
-            !(CL == 2 ? mbar_wait_cluster(bfull(b), (it / SB) & 1) : mbar_wait(bfull(b), (it / SB) & 1))) {
+        if (s_abort || !mbar_wait(full(s), (it / S) & 1) || !mbar_wait(bfull(b), (it / SB) & 1)) {
           s_abort = 1;
           break;
         }
@@ -345,8 +329,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
           }
         }
         tc_commit(empty(s));
-        if (CL == 2) tc_commit_multicast(bempty(b), 0x3);   // both CTAs may refill this B buffer
-        else tc_commit(bempty(b));
+        tc_commit(bempty(b));
       }
       tc_commit(accfull);
       mbar_wait(accfull, 0);   // every MMA has retired before TMEM is released
@@ -361,35 +344,22 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
     const int tg = tq - grp * C::UNITS;
     for (int it = grp; it < niter; it += step) {
       const int s = it % S, b = it % SB;
-      if (s_abort || !mbar_wait(full(s), (it / S) & 1) ||
-          !(CL == 2 ? mbar_wait_cluster(bempty(b), ((it / SB) & 1) ^ 1)
-                    : mbar_wait(bempty(b), ((it / SB) & 1) ^ 1))) {
+      if (s_abort || !mbar_wait(full(s), (it / S) & 1) || !mbar_wait(bempty(b), ((it / SB) & 1) ^ 1)) {
         s_abort = 1;
         break;
       }
       uint8_t* Bt = smem + C::OFF_B + b * C::B_BYTES;
-      const uint32_t peer_Bt = CL == 2 ? mapa_shared(sb + C::OFF_B + b * C::B_BYTES, rank ^ 1u) : 0u;
       if (it < KB) {
         const uint8_t* Wt = smem + C::OFF_W + s * C::W_BYTES;
         const float* absS = reinterpret_cast<const float*>(smem + C::OFF_ABS + s * C::ABS_PER_STAGE * 4);
-        if (MODE == GEMM_FWD) dequant_fwd_unit(Wt, absS, Bt, tg, half0, peer_Bt);
-        else dequant_dx_unit(Wt, absS, Bt, tg, C::W_BYTES / 64, half0 / 64, peer_Bt);
+        if (MODE == GEMM_FWD) dequant_fwd_unit(Wt, absS, Bt, tg, 0);
+        else dequant_dx_unit(Wt, absS, Bt, tg, C::W_BYTES / 64, 0);
       } else {
-        copy_ext_rows(g.ext_b, n0, g.Nout, Bt, half0, C::UNITS, tg, C::UNITS, peer_Bt);
+        copy_ext_rows(g.ext_b, n0, g.Nout, Bt, 0, C::UNITS, tg, C::UNITS);
       }
-      if (CL == 2) {
-        // this thread's stores into both B buffers: visible to the tensor cores (async
-        // proxy) and, cluster-wide, before the peer learns of them
-        fence_proxy_async_all();
-        fence_acq_rel_cluster();
-      } else {
-        fence_proxy_async_smem();
-      }
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bfull(b));
-        if (CL == 2) mbar_arrive_remote(mapa_shared(bfull(b), rank ^ 1u));
-      }
+      if (lane == 0) mbar_arrive(bfull(b));
     }
 
     // ------------------------------------------------------------ epilogue
@@ -501,7 +471,6 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB, CL>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (CL == 2) cluster_sync_all();   // no peer store or arrive may target this CTA after it exits
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);

@@ -460,13 +460,18 @@ __device__ __forceinline__ uint32_t lora_w_pair(const LoraProjHalf& h, int n, in
   return (uint32_t)w[(size_t)k * r + n] | ((uint32_t)w[(size_t)(k + 1) * r + n] << 16);
 }
 
+// blockIdx.y / gridDim.y selects a slice of K (fixed split); with gridDim.y > 1 the
+// block writes its unscaled partial sums to part [gridDim.y][T][32] for
+// lora_proj_reduce_kernel instead of the outputs.
 __global__ void __launch_bounds__(256) lora_proj_kernel(const __nv_bfloat16* __restrict__ X, long long ldx, int T,
                                                         LoraProjHalf h0, LoraProjHalf h1, int r, float s,
                                                         float* __restrict__ out_f32,
-                                                        __nv_bfloat16* __restrict__ out_ext) {
+                                                        __nv_bfloat16* __restrict__ out_ext,
+                                                        float* __restrict__ part) {
   __shared__ float red[8][16][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, cq = lane & 3;
   const int r0 = blockIdx.x * 16;
+  const int nsplit = gridDim.y, split = blockIdx.y;
   const bool ok0 = r0 + g < T, ok1 = r0 + g + 8 < T;
   const __nv_bfloat16* x0 = X + (size_t)(ok0 ? r0 + g : 0) * ldx;
   const __nv_bfloat16* x1 = X + (size_t)(ok1 ? r0 + g + 8 : 0) * ldx;
@@ -478,8 +483,8 @@ __global__ void __launch_bounds__(256) lora_proj_kernel(const __nv_bfloat16* __r
     const LoraProjHalf& h = hh ? h1 : h0;
     if (!h.w) continue;
     const int ksteps = h.K >> 4;
-    const int per = (ksteps + 7) >> 3;
-    const int kb = warp * per, ke = min(ksteps, kb + per);
+    const int wper = (ksteps + nsplit * 8 - 1) / (nsplit * 8);   // k-steps per warp
+    const int kb = (split * 8 + warp) * wper, ke = min(ksteps, kb + wper);
 #pragma unroll 4
     for (int ks = kb; ks < ke; ++ks) {
       const int k0 = ks << 4;
@@ -516,6 +521,10 @@ __global__ void __launch_bounds__(256) lora_proj_kernel(const __nv_bfloat16* __r
     for (int w = 0; w < 8; ++w) v += red[w][row][j];
     const int t = r0 + row;
     if (t < T) {
+      if (nsplit > 1) {
+        part[((size_t)split * T + t) * 32 + j] = v;
+        continue;
+      }
       const float sv = s * v;
       if (out_f32) out_f32[(size_t)t * 32 + j] = sv;
       if (out_ext) {
@@ -523,6 +532,22 @@ __global__ void __launch_bounds__(256) lora_proj_kernel(const __nv_bfloat16* __r
         out_ext[(size_t)t * 64 + 32 + j] = __float2bfloat16_rn(0.f);
       }
     }
+  }
+}
+
+// Sum of the K-slice partials in slice order, then the scale and the outputs.
+__global__ void lora_proj_reduce_kernel(const float* __restrict__ part, int nsplit, int T, float s,
+                                        float* __restrict__ out_f32, __nv_bfloat16* __restrict__ out_ext) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= T * 32) return;
+  const int t = e >> 5, j = e & 31;
+  float v = 0.f;
+  for (int k = 0; k < nsplit; ++k) v += part[(size_t)k * T * 32 + e];
+  const float sv = s * v;
+  if (out_f32) out_f32[e] = sv;
+  if (out_ext) {
+    out_ext[(size_t)t * 64 + j] = __float2bfloat16_rn(sv);
+    out_ext[(size_t)t * 64 + 32 + j] = __float2bfloat16_rn(0.f);
   }
 }
 

@@ -190,6 +190,31 @@ class Stack:
         check(lib().load_vocab_nf4(self.ctx, C.byref(vh)), self.ctx)
         self.vocab_bufs = dict(vb)
 
+    # ------------------------------------------------------------------ file-backed layers
+    def layer_file_stride(self) -> int:
+        """Bytes between consecutive layer images in a layer file (4 KiB-aligned)."""
+        return (self.img_bytes + 4095) // 4096 * 4096
+
+    def write_layer_file(self, path: str):
+        """Write every pinned layer image to one file (layer l at l * layer_file_stride())."""
+        stride = self.layer_file_stride()
+        with open(path, "wb") as f:
+            for l, img in enumerate(self.images):
+                f.seek(l * stride)
+                f.write(img.numpy().tobytes())
+            f.truncate(len(self.images) * stride)
+
+    def use_layer_file(self, path: str, nbuf: int = 3, release_ram: bool = True):
+        """Stream every decoder layer from `path` (written by write_layer_file) through
+        `nbuf` pinned staging buffers instead of from pinned RAM images."""
+        stride = self.layer_file_stride()
+        self.staging = torch.empty(nbuf * stride, dtype=torch.uint8, pin_memory=True)
+        check(lib().ls_set_staging(self.ctx, self.staging.data_ptr(), stride, nbuf), self.ctx)
+        for l in range(self.s.layers):
+            check(lib().load_layer_file(self.ctx, l, path.encode(), l * stride), self.ctx)
+        if release_ram:
+            self.images = [None] * self.s.layers
+
     # ------------------------------------------------------------------ adapters
     def set_adapter(self, layer: int, aq, bq, av, bv):
         """Bind bf16 device LoRA factors (A [r,H], B [N,r]); fp32 grads are allocated here."""

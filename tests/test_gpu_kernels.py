@@ -331,51 +331,3 @@ def test_vocab_logprob_fwd_bwd(T, H, V):
     want = (coef[:, None] * (oh - sm)) @ wd.astype(np.float64)
     torch.cuda.synchronize()
     assert rel_err(to_np(dh), want) <= TOL
-
-
-# ------------------------------------------------------------------ paired-CTA tiles
-
-PAIR_CASES = [
-    # (mode, M, N, K): odd row-tile counts pad the pair; ragged N and reduction tails
-    (0, 600, 640, 512),
-    (0, 1024, 6144, 256),
-    (1, 700, 768, 1024),
-    (1, 300, 1024, 640),
-]
-
-
-@pytest.mark.parametrize("mode,M,N,K", PAIR_CASES)
-def test_paired_cta_tiles_match_single_and_oracle(mode, M, N, K):
-    """Two CTAs of a cluster sharing one dequantised 256 x 256 weight tile give the same
-    bits as one CTA per tile, and the oracle's product (with the LoRA extra stage)."""
-    red, outc = (K, N) if mode == 0 else (N, K)
-    x = synth.gaussian((M, red), 50, M, red)
-    w = _w(N, K, seed=51)
-    p, a, _, _ = nf4_dev(w)
-    wd = _oracle_deq(w)
-    xd = bf16_dev(x)
-    ext_a = bf16_dev(synth.gaussian((M, 64), 52, M, std=0.1))
-    ext_b = bf16_dev(synth.gaussian((outc, 64), 53, outc, std=0.1))
-    res = bf16_dev(synth.gaussian((M, outc), 54, M)) if mode == 0 else None
-    outs = []
-    old = L.lib().lsk_gemm_cluster_mode(1)
-    try:
-        for cm in (1, 2):
-            L.lib().lsk_gemm_cluster_mode(cm)
-            if mode == 0:
-                o = torch.empty((M, outc), dtype=torch.bfloat16, device=DEV)
-                k("lsk_nf4_gemm", 0, xd, red, M, p, a, N, K, ext_a, ext_b, 32, 0, o, outc, res, outc, 256, 2)
-            else:
-                o = torch.empty((M, outc), dtype=torch.float32, device=DEV)
-                k("lsk_nf4_gemm", 1, xd, red, M, p, a, N, K, ext_a, ext_b, 32, 1, o, outc, None, 0, 256, 2)
-            outs.append(o)
-        torch.cuda.synchronize()
-    finally:
-        L.lib().lsk_gemm_cluster_mode(old)
-    assert torch.equal(outs[0], outs[1])
-    ea, eb = to_np(ext_a)[:, :32], to_np(ext_b)[:, :32]
-    base = x.astype(np.float64) @ (wd.astype(np.float64).T if mode == 0 else wd.astype(np.float64))
-    want = base + ea @ eb.T
-    if mode == 0:
-        want = want + to_np(res)
-    assert rel_err(to_np(outs[1]), want) <= TOL

@@ -463,3 +463,42 @@ def test_adamw_step_matches_oracle():
                            for k in ("aq", "bq", "av", "bv")])
     assert torch.equal(flat_bf16, st.opt["master"].to(torch.bfloat16).float())
     st.close()
+
+
+def test_file_backed_layers_match_pinned_ram(tmp_path):
+    """Layers streamed from a file through pinned staging buffers give the same step,
+    bit for bit, as the same images held in pinned RAM; every layer read goes through
+    the file."""
+    cfg = SMALL_DPO
+    tok, cu, mask = _batch(cfg)
+    ram = _stack(cfg, vocab_chunk_rows=256)
+    path = str(tmp_path / "layers.bin")
+    ram.write_layer_file(path)
+    disk = L.Stack(cfg, device="cuda:0", vocab_chunk_rows=256)
+    disk.adopt_base(ram)
+    disk.set_adapters_synthetic(synth, 0)
+    disk.use_layer_file(path, nbuf=2)
+    disk.stats(reset=True)
+    r_ram = _run_all(ram, cfg, tok, cu, mask)
+    r_disk = _run_all(disk, cfg, tok, cu, mask)
+    st = disk.stats()
+    ram.close()
+    disk.close()
+    for x, y in zip(r_ram[1:], r_disk[1:]):
+        assert torch.equal(x, y)
+    for k in ("pi", "ref", "loss", "coeffs"):
+        assert torch.equal(r_ram[0][k], r_disk[0][k]), k
+    assert st["layer_reads"] >= 2 * cfg.layers
+    assert st["file_bytes"] == st["layer_reads"] * disk.img_bytes
+
+
+def test_layer_file_errors_are_reported(tmp_path):
+    cfg = SMALL_DPO
+    st = L.Stack(cfg, device="cuda:0")
+    short = tmp_path / "short.bin"
+    short.write_bytes(b"\0" * 1000)
+    import ctypes as C
+    assert L.lib().load_layer_file(st.ctx, 0, str(short).encode(), 0) == L.LS_ERR_ARG
+    assert "shorter" in L.last_error(st.ctx)
+    assert L.lib().load_layer_file(st.ctx, 0, str(tmp_path / "missing.bin").encode(), 0) == L.LS_ERR_ARG
+    st.close()
