@@ -43,6 +43,12 @@ import torch  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "train tokens/s streamed NF4 LoRA (8B shape, SFT+DPO); H2D GB/s; % roofline"
+# DRAM bytes (read + write) per algorithmic byte of the forward NF4 GEMM, from one ncu
+# capture of the 8B gate|up launch (M 2048, N 28672, K 4096: 156.0 MB measured against
+# 200.3 MB algorithmic; output rows partly still in L2 at kernel end).  It scales the
+# class's algorithmic bytes per launch to the reported traffic; set to None whenever the
+# kernel changes until it is captured again.
+GEMM_FWD_TRAFFIC_PER_ALG_BYTE = 156.0 / 200.3
 UNIT = "tokens/s"
 NF4_BYTES_PER_PARAM = 0.5625
 
@@ -408,7 +414,11 @@ def run_gpu_arm(args, s, ws, rank, local):
         "gpu_launches": int(stats_k["kernel_launches"] * K),
         "roofline": {"bound": "tensor", "kernel": f"nf4_gemm ({dom})", "achieved": round(achieved, 2),
                      "peak": tf_peak, "unit": "TFLOP/s", "frac": round(achieved / tf_peak, 4),
-                     "peak_source": f"{peaks['source']} bf16 sustained", "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16 sustained",
+                     "traffic": (round(p[dom]["bytes"] / max(1, p[dom]["launches"]) * GEMM_FWD_TRAFFIC_PER_ALG_BYTE)
+                                 if dom == "gemm_fwd" and GEMM_FWD_TRAFFIC_PER_ALG_BYTE else None),
+                     "traffic_unit": "bytes per launch (ncu-measured DRAM/algorithmic ratio x algorithmic bytes)",
+                     "alg_bytes_per_launch": round(p[dom]["bytes"] / max(1, p[dom]["launches"])),
                      "launches": p[dom]["launches"], "avg_launch_us": round(1e3 * p[dom]["ms"] / max(1, p[dom]["launches"]), 2)},
         "stream": {"h2d_gbs": round(stats_k["h2d_bytes"] / (step_ms * 1e-3) / 1e9, 2),
                    "h2d_peak_gbs": round(link, 2), "h2d_gb_per_step": round(stats_k["h2d_bytes"] / 1e9, 3),
