@@ -65,6 +65,25 @@ __device__ __forceinline__ void load_tile(__nv_bfloat16* dst, const __nv_bfloat1
   }
 }
 
+// Asynchronous variant: 16-byte cp.async per chunk, rows at or past L zero-filled (source
+// size 0, no global read).  The caller commits the group and waits on it.
+template <int HD>
+__device__ __forceinline__ void load_tile_async(__nv_bfloat16* dst, const __nv_bfloat16* src, long long ld, int r0,
+                                                int L, int tid, int nthr) {
+  constexpr int LDS = HD + 8;
+  for (int e = tid; e < 64 * (HD / 8); e += nthr) {
+    const int r = e / (HD / 8), c = e % (HD / 8);
+    const bool ok = r0 + r < L;
+    const __nv_bfloat16* g = ok ? src + (size_t)(r0 + r) * ld + c * 8 : src;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst + r * LDS + c * 8)), "l"(g),
+                 "r"(ok ? 16 : 0)
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -77,9 +96,8 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const __nv_bfloat16* __re
                                                        float* __restrict__ lse, int T) {
   constexpr int LDS = HD + 8;
   extern __shared__ __align__(16) uint8_t attn_smem[];
+  // Q, then two (K, V) buffers: the next key tile is copied while this one computes
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(attn_smem);
-  __nv_bfloat16* sK = sQ + 64 * LDS;
-  __nv_bfloat16* sV = sK + 64 * LDS;
   const int s = blockIdx.z, h = blockIdx.y;
   const int a = cu[s], L = cu[s + 1] - a;
   const int q0 = blockIdx.x * 64;
@@ -89,7 +107,10 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const __nv_bfloat16* __re
   const __nv_bfloat16* Qg = qkv + (size_t)a * ld + (size_t)h * HD;
   const __nv_bfloat16* Kg = qkv + (size_t)a * ld + (size_t)(nh + g) * HD;
   const __nv_bfloat16* Vg = qkv + (size_t)a * ld + (size_t)(nh + nkv + g) * HD;
-  load_tile<HD>(sQ, Qg, ld, q0, L, tid, 128);
+  load_tile_async<HD>(sQ, Qg, ld, q0, L, tid, 128);
+  load_tile_async<HD>(sQ + 64 * LDS, Kg, ld, 0, L, tid, 128);
+  load_tile_async<HD>(sQ + 2 * 64 * LDS, Vg, ld, 0, L, tid, 128);
+  cp_async_commit();
   const float c2 = scale * kLog2e;
   float o[HD / 8][4];
 #pragma unroll
@@ -97,10 +118,18 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const __nv_bfloat16* __re
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   const int row0 = q0 + warp * 16 + (lane >> 2);
   const int kend = min(L, q0 + 64);
-  for (int k0 = 0; k0 < kend; k0 += 64) {
-    __syncthreads();
-    load_tile<HD>(sK, Kg, ld, k0, L, tid, 128);
-    load_tile<HD>(sV, Vg, ld, k0, L, tid, 128);
+  for (int k0 = 0, it = 0; k0 < kend; k0 += 64, ++it) {
+    __nv_bfloat16* sK = sQ + (1 + 2 * (it & 1)) * 64 * LDS;
+    __nv_bfloat16* sV = sK + 64 * LDS;
+    if (k0 + 64 < kend) {
+      __nv_bfloat16* nK = sQ + (1 + 2 * ((it + 1) & 1)) * 64 * LDS;
+      load_tile_async<HD>(nK, Kg, ld, k0 + 64, L, tid, 128);
+      load_tile_async<HD>(nK + 64 * LDS, Vg, ld, k0 + 64, L, tid, 128);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
     __syncthreads();
     float sc[8][4];
 #pragma unroll
@@ -165,6 +194,7 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const __nv_bfloat16* __re
         mma16816(o[dn + 1], pa, b[2], b[3]);
       }
     }
+    __syncthreads();   // every warp is done with this buffer before it is refilled
   }
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -211,20 +241,22 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* _
                                                           float* __restrict__ dqkv, long long ldg, int T) {
   constexpr int LDS = HD + 8;
   extern __shared__ __align__(16) uint8_t attn_smem[];
+  // Q, dO, then two (K, V) buffers (the next key tile is copied while this one computes)
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(attn_smem);
   __nv_bfloat16* sO = sQ + 64 * LDS;
-  __nv_bfloat16* sK = sO + 64 * LDS;
-  __nv_bfloat16* sV = sK + 64 * LDS;
   const int s = blockIdx.z, h = blockIdx.y;
   const int a = cu[s], L = cu[s + 1] - a;
   const int q0 = blockIdx.x * 64;
   if (q0 >= L) return;
   const int g = h / (nh / nkv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  load_tile<HD>(sQ, qkv + (size_t)a * ld + (size_t)h * HD, ld, q0, L, tid, 128);
-  load_tile<HD>(sO, dout + (size_t)a * lddo + (size_t)h * HD, lddo, q0, L, tid, 128);
   const __nv_bfloat16* Kg = qkv + (size_t)a * ld + (size_t)(nh + g) * HD;
   const __nv_bfloat16* Vg = qkv + (size_t)a * ld + (size_t)(nh + nkv + g) * HD;
+  load_tile_async<HD>(sQ, qkv + (size_t)a * ld + (size_t)h * HD, ld, q0, L, tid, 128);
+  load_tile_async<HD>(sO, dout + (size_t)a * lddo + (size_t)h * HD, lddo, q0, L, tid, 128);
+  load_tile_async<HD>(sO + 64 * LDS, Kg, ld, 0, L, tid, 128);
+  load_tile_async<HD>(sO + 2 * 64 * LDS, Vg, ld, 0, L, tid, 128);
+  cp_async_commit();
   const float c2 = scale * kLog2e;
   const int row0 = q0 + warp * 16 + (lane >> 2);
   float lrow[2], drow[2];
@@ -238,10 +270,18 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* _
 #pragma unroll
   for (int i = 0; i < HD / 8; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
   const int kend = min(L, q0 + 64);
-  for (int k0 = 0; k0 < kend; k0 += 64) {
-    __syncthreads();
-    load_tile<HD>(sK, Kg, ld, k0, L, tid, 128);
-    load_tile<HD>(sV, Vg, ld, k0, L, tid, 128);
+  for (int k0 = 0, it = 0; k0 < kend; k0 += 64, ++it) {
+    __nv_bfloat16* sK = sO + (1 + 2 * (it & 1)) * 64 * LDS;
+    __nv_bfloat16* sV = sK + 64 * LDS;
+    if (k0 + 64 < kend) {
+      __nv_bfloat16* nK = sO + (1 + 2 * ((it + 1) & 1)) * 64 * LDS;
+      load_tile_async<HD>(nK, Kg, ld, k0 + 64, L, tid, 128);
+      load_tile_async<HD>(nK + 64 * LDS, Vg, ld, k0 + 64, L, tid, 128);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
     __syncthreads();
     float p[8][4], dp[8][4];
 #pragma unroll
@@ -285,6 +325,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* _
         mma16816(dq[dn + 1], da, b[2], b[3]);
       }
     }
+    __syncthreads();   // every warp is done with this buffer before it is refilled
   }
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -311,19 +352,18 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16*
                                                             long long ldg, int T) {
   constexpr int LDS = HD + 8;
   extern __shared__ __align__(16) uint8_t attn_smem[];
+  // K, V, then two (Q, dO) buffers and two (lse, D) rows: the next query tile is copied
+  // while this one computes
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(attn_smem);
   __nv_bfloat16* sV = sK + 64 * LDS;
-  __nv_bfloat16* sQ = sV + 64 * LDS;
-  __nv_bfloat16* sO = sQ + 64 * LDS;
-  float* sL = reinterpret_cast<float*>(sO + 64 * LDS);
-  float* sD = sL + 64;
+  float* sLD = reinterpret_cast<float*>(sV + 5 * 64 * LDS);   // [2][2][64]
   const int s = blockIdx.z, g = blockIdx.y;
   const int a = cu[s], L = cu[s + 1] - a;
   const int k0 = blockIdx.x * 64;
   if (k0 >= L) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  load_tile<HD>(sK, qkv + (size_t)a * ld + (size_t)(nh + g) * HD, ld, k0, L, tid, 128);
-  load_tile<HD>(sV, qkv + (size_t)a * ld + (size_t)(nh + nkv + g) * HD, ld, k0, L, tid, 128);
+  load_tile_async<HD>(sK, qkv + (size_t)a * ld + (size_t)(nh + g) * HD, ld, k0, L, tid, 128);
+  load_tile_async<HD>(sV, qkv + (size_t)a * ld + (size_t)(nh + nkv + g) * HD, ld, k0, L, tid, 128);
   const float c2 = scale * kLog2e;
   const int key0 = k0 + warp * 16 + (lane >> 2);
   float dk[HD / 8][4], dv[HD / 8][4];
@@ -332,16 +372,34 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16*
 #pragma unroll
     for (int e = 0; e < 4; ++e) dk[i][e] = dv[i][e] = 0.f;
   const int group = nh / nkv;
-  for (int hh = 0; hh < group; ++hh) {
-    const int h = g * group + hh;
-    for (int q0 = k0; q0 < L; q0 += 64) {
-      __syncthreads();
-      load_tile<HD>(sQ, qkv + (size_t)a * ld + (size_t)h * HD, ld, q0, L, tid, 128);
-      load_tile<HD>(sO, dout + (size_t)a * lddo + (size_t)h * HD, lddo, q0, L, tid, 128);
-      if (tid < 64) {
-        const int q = q0 + tid;
-        sL[tid] = q < L ? lse[(size_t)h * T + a + q] * kLog2e : 0.f;
-        sD[tid] = q < L ? D[(size_t)h * T + a + q] : 0.f;
+  // flat loop over (query head of the group, query tile from the key tile on)
+  const int nqt = (L - k0 + 63) / 64;
+  const int nit = group * nqt;
+  auto issue = [&](int j) {
+    const int h = g * group + j / nqt, q0 = k0 + (j % nqt) * 64, buf = j & 1;
+    __nv_bfloat16* dQ = sV + (1 + 2 * buf) * 64 * LDS;
+    load_tile_async<HD>(dQ, qkv + (size_t)a * ld + (size_t)h * HD, ld, q0, L, tid, 128);
+    load_tile_async<HD>(dQ + 64 * LDS, dout + (size_t)a * lddo + (size_t)h * HD, lddo, q0, L, tid, 128);
+    if (tid < 64) {
+      const int q = q0 + tid;
+      sLD[buf * 128 + tid] = q < L ? lse[(size_t)h * T + a + q] * kLog2e : 0.f;
+      sLD[buf * 128 + 64 + tid] = q < L ? D[(size_t)h * T + a + q] : 0.f;
+    }
+    cp_async_commit();
+  };
+  issue(0);
+  for (int j = 0; j < nit; ++j) {
+    const int q0 = k0 + (j % nqt) * 64, buf = j & 1;
+    const __nv_bfloat16* sQ = sV + (1 + 2 * buf) * 64 * LDS;
+    const __nv_bfloat16* sO = sQ + 64 * LDS;
+    const float* sL = sLD + buf * 128;
+    const float* sD = sL + 64;
+    {
+      if (j + 1 < nit) {
+        issue(j + 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
       }
       __syncthreads();
       float pt[8][4], dpt[8][4];
@@ -392,6 +450,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16*
           mma16816(dk[dn + 1], da, b[2], b[3]);
         }
       }
+      __syncthreads();   // every warp is done with this buffer before it is refilled
     }
   }
 #pragma unroll

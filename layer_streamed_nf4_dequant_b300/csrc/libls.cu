@@ -492,7 +492,7 @@ cudaError_t gemm(int mode, const bf16* A, long long lda, int M, const uint8_t* W
 template <int HD>
 cudaError_t attn_fwd_launch(const bf16* qkv, long long ld, const int* cu, int nseq, int maxlen, int nh, int nkv,
                             bf16* out, long long ldo, float* lse, int T, cudaStream_t st) {
-  const int smem = 3 * 64 * (HD + 8) * 2;
+  const int smem = 5 * 64 * (HD + 8) * 2;   // Q + two (K, V) buffers
   static bool set = false;
   if (!set) {
     cudaFuncSetAttribute(ls::attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -507,8 +507,8 @@ template <int HD>
 cudaError_t attn_bwd_launch(const bf16* qkv, long long ld, const bf16* dout, const bf16* o, long long lddo,
                             const float* lse, const int* cu, int nseq, int maxlen, int nh, int nkv, float* D,
                             float* dqkv, long long ldg, int T, cudaStream_t st) {
-  const int smem_q = 4 * 64 * (HD + 8) * 2;
-  const int smem_k = 4 * 64 * (HD + 8) * 2 + 2 * 64 * 4;
+  const int smem_q = 6 * 64 * (HD + 8) * 2;                  // Q, dO + two (K, V) buffers
+  const int smem_k = 6 * 64 * (HD + 8) * 2 + 4 * 64 * 4;     // K, V + two (Q, dO, lse, D) buffers
   static bool set = false;
   if (!set) {
     cudaFuncSetAttribute(ls::attn_bwd_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
