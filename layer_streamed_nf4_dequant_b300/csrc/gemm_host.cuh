@@ -90,37 +90,38 @@ static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Pick the tile shape.  Each CTA dequantises its BN x 64 weight tile once per k-step,
-// so above 128 rows two accumulators (BM = 256) always pay: they halve the dequant work
-// per MMA FLOP (measured 1.4-1.5x faster at every 8B-shape product).  Between BN = 128
-// and 256 the tile with the lower (waves x per-CTA time) wins.  Per-CTA time relative
-// to BN = 256, measured on the 8B shapes: forward (register-table dequant, one thread
-// per row, BN = 128 tiles alternate k-steps between two halves of the dequant warps)
-// 0.76; input gradient (shared-memory table dequant) 0.5.  Ties go to BN = 256 for the
-// forward and to BN = 128 for the input gradient (measured).
+// Pick the tile shape by estimated time = waves x per-CTA time.  Per-CTA time per
+// k-step relative to the 256 x 256 tile, measured on the 3B / 8B / 32B product shapes
+// (bench.py --gemm): forward 128x256 (NACC 2, BN 128) 0.76, 128-row tiles BN 256 0.92,
+// BN 128 0.62; input gradient 0.67 / 0.87 / 0.60.  128 x 128 tiles fit two CTAs per SM,
+// so past one CTA per SM they share it (time x 2 per 296 CTAs).  Grids smaller than the
+// SM count finish in one CTA time: there the smallest tile wins (the 3B-shape products
+// at 512 rows gain 15-20%); large grids prefer 256 x 256 (half the dequant per MMA FLOP).
 static void choose_tile(int mode, int M, int Nout, int& nacc, int& bn) {
   const int sms = 148;
-  if (M > 128) {
-    nacc = 2;
-    const long long mt = (M + 255) / 256;
-    const long long w256 = (mt * ((Nout + 255) / 256) + sms - 1) / sms;
-    const long long w128 = (mt * ((Nout + 127) / 128) + sms - 1) / sms;
-    const double t128 = mode == GEMM_FWD ? 0.76 : 0.5;
-    const double c128 = (double)w128 * t128, c256 = (double)w256;
-    bn = (mode == GEMM_FWD ? c128 < c256 - 1e-9 : c128 <= c256 + 1e-9) ? 128 : 256;
-    return;
-  }
-  struct Opt { int nacc, bn, per_sm; } opts[4] = {{2, 256, 1}, {2, 128, 1}, {1, 256, 1}, {1, 128, 2}};
+  struct Opt {
+    int nacc, bn, per_sm;
+    double cost_fwd, cost_dx;
+  };
+  // in preference order for ties: forward larger tiles first, input gradient (2, 128) first
+  const Opt fwd_opts[4] = {{2, 256, 1, 1.0, 1.0}, {2, 128, 1, 0.76, 0.67}, {1, 256, 1, 0.92, 0.87},
+                           {1, 128, 2, 0.62, 0.60}};
+  const Opt dx_opts[4] = {fwd_opts[1], fwd_opts[0], fwd_opts[2], fwd_opts[3]};
+  const Opt* opts = mode == GEMM_FWD ? fwd_opts : dx_opts;
   double best = 1e30;
-  for (auto& o : opts) {
+  for (int i = 0; i < 4; ++i) {
+    const Opt& o = opts[i];
     if (o.nacc == 2 && M <= 128) continue;
-    long long ctas = (long long)((M + 128 * o.nacc - 1) / (128 * o.nacc)) * ((Nout + o.bn - 1) / o.bn);
-    long long waves = (ctas + (long long)sms * o.per_sm - 1) / ((long long)sms * o.per_sm);
-    // per-CTA time ~ tile area; two CTAs per SM share it
-    double t = (double)waves * (128.0 * o.nacc * o.bn) / o.per_sm;
-    // dequant cost per CTA does not shrink with NACC: penalise single-accumulator tiles a little
-    if (o.nacc == 1) t *= 1.15;
-    if (t < best - 1e-9) { best = t; nacc = o.nacc; bn = o.bn; }
+    const long long ctas = (long long)((M + 128 * o.nacc - 1) / (128 * o.nacc)) * ((Nout + o.bn - 1) / o.bn);
+    const double cost = mode == GEMM_FWD ? o.cost_fwd : o.cost_dx;
+    const double t = ctas <= sms ? cost
+                                 : (double)((ctas + (long long)sms * o.per_sm - 1) / ((long long)sms * o.per_sm)) *
+                                       cost * o.per_sm;
+    if (t < best - 1e-9) {
+      best = t;
+      nacc = o.nacc;
+      bn = o.bn;
+    }
   }
 }
 

@@ -361,6 +361,47 @@ def test_unpinned_layer_memory_is_refused():
 # ------------------------------------------------------------------ full sizes
 
 @pytest.mark.slow
+def test_llama8b_full_sampled_layers_and_vocab_match_oracle():
+    """The full 32-layer Llama-3.1-8B-shaped stack in the bench's launch configuration
+    (shared-read DPO forward over 2 x 512 tokens): layers 0, 15 and 31 recomputed by the
+    oracle from the GPU's own stored input of each (normwise <= 1e-2), and the full
+    128256-row vocabulary head on 16 sampled token rows from the GPU's final hidden
+    state (per-token logprob and log-sum-exp <= 2e-2)."""
+    cfg = synth.LLAMA_8B
+    tok, cu, mask = _batch(cfg)
+    st = _stack(cfg)
+    t, c, m = st.upload_batch(tok, cu, mask)
+    pi = torch.empty(cfg.nseq, dtype=torch.float32, device=DEV)
+    ref = torch.empty_like(pi)
+    st.fwd_dpo(t, c, m, pi, ref)
+    lp, lse = st.logprobs()
+    sample_layers = [0, 15, 31]
+    acts = {l: st.activation(l, len(tok)) for l in sample_layers + [l + 1 for l in sample_layers]}
+    hL = st.activation(cfg.layers, len(tok))
+    assert st.sync(300000) == 0, L.last_error(st.ctx)
+    st.close()
+    ads = om.build_adapters(cfg, 0, synth)
+    with torch.no_grad():
+        for l in sample_layers:
+            w = {n: om.dequant_weight(synth.weight(cfg, l, n, 0)) for n in ("q", "k", "v", "o", "gate", "up", "down")}
+            lw = om.LayerWeights(w["q"], w["k"], w["v"], w["o"], w["gate"], w["up"], w["down"],
+                                 om.t64(synth.norm_weight(cfg, l, 0, 0)), om.t64(synth.norm_weight(cfg, l, 1, 0)))
+            x = om.t64(acts[l].float().cpu().numpy())
+            y = om.decoder_layer(x, lw, ads[l], cfg, cu, adapter_on=True)
+            assert rel_err(to_np(acts[l + 1]), y.numpy()) <= TOL_GRAD, l
+        rows = np.random.default_rng(3).choice(len(tok), 16, replace=False)
+        head = om.dequant_weight(synth.weight(cfg, -1, "lm_head", 0))
+        hf = om.rmsnorm(om.t64(hL.float().cpu().numpy()[rows]), om.t64(synth.norm_weight(cfg, -1, 0, 0)), cfg.eps)
+        logits = hf @ head.T
+        lse_o = torch.logsumexp(logits, dim=-1).numpy()
+        y = om.targets(tok, cu)[rows]
+        lp_o = np.where(y >= 0, logits.numpy()[np.arange(len(rows)), np.maximum(y, 0)] - lse_o, 0.0)
+    # policy rows are the first T of the shared pass
+    assert np.abs(to_np(lse)[rows] - lse_o).max() <= TOL_LP
+    assert np.abs(to_np(lp)[rows] - lp_o).max() <= TOL_LP
+
+
+@pytest.mark.slow
 def test_llama8b_full_streamed_equals_resident_and_ln2():
     """The full 32-layer Llama-3.1-8B-shaped DPO step, in the bench's launch
     configuration: streamed = resident bit for bit; B = 0 gives ln 2."""
