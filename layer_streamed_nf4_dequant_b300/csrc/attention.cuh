@@ -341,15 +341,18 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* _
 }
 
 // ------------------------------------------------------------------ backward: dk, dv
-// grid (ceil(maxlen / 64), nkv, nseq).  Warp w owns keys 16w..16w+15 of the tile;
-// loops over the query heads of the group, then query tiles from the key tile on.
+// grid (ceil(maxlen / 64), nkv * hsplit, nseq).  Warp w owns keys 16w..16w+15 of the
+// tile; loops over its slice of the group's query heads (all of them when hsplit = 1),
+// then query tiles from the key tile on.  hsplit > 1: the slice's dk / dv go to
+// part [hsplit][T][2 nkv HD] (fp32, dk already scaled) for attn_dkdv_reduce_kernel.
 template <int HD>
 __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16* __restrict__ qkv, long long ld,
                                                             const __nv_bfloat16* __restrict__ dout, long long lddo,
                                                             const float* __restrict__ lse,
                                                             const float* __restrict__ D, const int* __restrict__ cu,
                                                             int nh, int nkv, float scale, float* __restrict__ dqkv,
-                                                            long long ldg, int T) {
+                                                            long long ldg, int T, int hsplit,
+                                                            float* __restrict__ part) {
   constexpr int LDS = HD + 8;
   extern __shared__ __align__(16) uint8_t attn_smem[];
   // K, V, then two (Q, dO) buffers and two (lse, D) rows: the next query tile is copied
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16*
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(attn_smem);
   __nv_bfloat16* sV = sK + 64 * LDS;
   float* sLD = reinterpret_cast<float*>(sV + 5 * 64 * LDS);   // [2][2][64]
-  const int s = blockIdx.z, g = blockIdx.y;
+  const int s = blockIdx.z, g = blockIdx.y / hsplit, hs = blockIdx.y % hsplit;
   const int a = cu[s], L = cu[s + 1] - a;
   const int k0 = blockIdx.x * 64;
   if (k0 >= L) return;
@@ -372,11 +375,15 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16*
 #pragma unroll
     for (int e = 0; e < 4; ++e) dk[i][e] = dv[i][e] = 0.f;
   const int group = nh / nkv;
-  // flat loop over (query head of the group, query tile from the key tile on)
+  // this CTA's query heads: [h_lo, h_lo + nheads) of the group
+  const int per = (group + hsplit - 1) / hsplit;
+  const int h_lo = g * group + hs * per;
+  const int nheads = max(0, min(per, group - hs * per));
+  // flat loop over (query head, query tile from the key tile on)
   const int nqt = (L - k0 + 63) / 64;
-  const int nit = group * nqt;
+  const int nit = nheads * nqt;
   auto issue = [&](int j) {
-    const int h = g * group + j / nqt, q0 = k0 + (j % nqt) * 64, buf = j & 1;
+    const int h = h_lo + j / nqt, q0 = k0 + (j % nqt) * 64, buf = j & 1;
     __nv_bfloat16* dQ = sV + (1 + 2 * buf) * 64 * LDS;
     load_tile_async<HD>(dQ, qkv + (size_t)a * ld + (size_t)h * HD, ld, q0, L, tid, 128);
     load_tile_async<HD>(dQ + 64 * LDS, dout + (size_t)a * lddo + (size_t)h * HD, lddo, q0, L, tid, 128);
@@ -387,7 +394,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16*
     }
     cp_async_commit();
   };
-  issue(0);
+  if (nit > 0) issue(0);
+  else cp_async_commit();   // K / V only (no query head in this slice): nothing to wait on
   for (int j = 0; j < nit; ++j) {
     const int q0 = k0 + (j % nqt) * 64, buf = j & 1;
     const __nv_bfloat16* sQ = sV + (1 + 2 * buf) * 64 * LDS;
@@ -453,18 +461,33 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16*
       __syncthreads();   // every warp is done with this buffer before it is refilled
     }
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int key = key0 + r * 8;
     if (key >= L) continue;
-    float* krow = dqkv + (size_t)(a + key) * ldg + (size_t)(nh + g) * HD;
-    float* vrow = dqkv + (size_t)(a + key) * ldg + (size_t)(nh + nkv + g) * HD;
+    float* krow = hsplit > 1 ? part + ((size_t)hs * T + a + key) * (2 * nkv * HD) + (size_t)g * HD
+                             : dqkv + (size_t)(a + key) * ldg + (size_t)(nh + g) * HD;
+    float* vrow = hsplit > 1 ? krow + (size_t)nkv * HD : dqkv + (size_t)(a + key) * ldg + (size_t)(nh + nkv + g) * HD;
 #pragma unroll
     for (int dn = 0; dn < HD / 8; ++dn) {
       const int col = dn * 8 + 2 * (lane & 3);
       *reinterpret_cast<float2*>(krow + col) = make_float2(dk[dn][2 * r] * scale, dk[dn][2 * r + 1] * scale);
       *reinterpret_cast<float2*>(vrow + col) = make_float2(dv[dn][2 * r], dv[dn][2 * r + 1]);
     }
+  }
+}
+
+// dk / dv = sum over the head slices in slice order, into the k / v columns of dqkv.
+__global__ void attn_dkdv_reduce_kernel(const float* __restrict__ part, int hsplit, int nh, int nkv, int hd, int T,
+                                        float* __restrict__ dqkv, long long ldg) {
+  const long long w = 2LL * nkv * hd;
+  const long long n = (long long)T * w;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
+    const long long t = e / w, c = e % w;
+    float v = 0.f;
+    for (int k = 0; k < hsplit; ++k) v += part[(size_t)k * n + e];
+    dqkv[t * ldg + (long long)nh * hd + c] = v;
   }
 }
 

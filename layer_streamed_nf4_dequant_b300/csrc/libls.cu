@@ -162,6 +162,7 @@ struct ls_ctx {
   float *rstdf_save, *rstdf_tmp, *pmax, *psum, *tgt_logit, *lse_save, *lse_tmp, *lp, *coef, *dhf, *loss_tmp;
   int32_t *tgt, *pos;
   int32_t *tok2 = nullptr, *cu2 = nullptr;   // shared-read DPO forward: doubled batch
+  float* attn_part = nullptr;                 // per-query-head dk / dv partials
   int Tf = 0;                                 // forward row capacity (2 max_tokens with shared read)
   int P = 0;
   size_t lora_part_floats = 0;
@@ -396,6 +397,8 @@ Planned lay_out(const ls_config& k, ls_ctx* c) {
   // LoRA scratch: outer-product partials, and the K-split partials of the projections
   const size_t lpf = std::max((size_t)chunks * std::max(nqkv, H) * 16, (size_t)kLoraSplitMax * T * 32);
   float* lpart = b.take<float>(lpf);
+  // attention backward: dk / dv of every query head before the ordered sum over its group
+  float* apart = k.heads > k.kv_heads ? b.take<float>((size_t)k.heads / k.kv_heads * T * 2 * nkvd) : nullptr;
   // union: layer-backward big buffers / vocabulary dlogits
   const size_t u0 = align_up(b.off, 256);
   Bump u1{c ? c->ws : nullptr, u0};
@@ -445,7 +448,7 @@ Planned lay_out(const ls_config& k, ls_ctx* c) {
     c->hf_save = hfs; c->hf_tmp = hft; c->rstdf_save = rfs; c->rstdf_tmp = rft; c->pmax = pmax; c->psum = psum;
     c->tgt_logit = tl; c->lse_save = lses; c->lse_tmp = lset; c->lp = lp; c->coef = coef; c->dhf = dhf;
     c->loss_tmp = losst; c->tgt = tgt; c->pos = pos; c->P = p.P;
-    c->tok2 = tok2; c->cu2 = cu2; c->Tf = (int)Tf;
+    c->tok2 = tok2; c->cu2 = cu2; c->Tf = (int)Tf; c->attn_part = apart;
     c->vrows = vrows; c->nvch = nvch; c->vch_abs_off = abs_off;
   }
   return p;
@@ -503,10 +506,13 @@ cudaError_t attn_fwd_launch(const bf16* qkv, long long ld, const int* cu, int ns
   return cudaGetLastError();
 }
 
+// part (fp32, >= (nh / nkv) * T * 2 * nkv * HD): split each KV group's query heads
+// over CTAs (one head each) and sum the per-head dk / dv in head order; without it
+// one CTA loops over the whole group.
 template <int HD>
 cudaError_t attn_bwd_launch(const bf16* qkv, long long ld, const bf16* dout, const bf16* o, long long lddo,
                             const float* lse, const int* cu, int nseq, int maxlen, int nh, int nkv, float* D,
-                            float* dqkv, long long ldg, int T, cudaStream_t st) {
+                            float* dqkv, long long ldg, int T, cudaStream_t st, float* part = nullptr) {
   const int smem_q = 6 * 64 * (HD + 8) * 2;                  // Q, dO + two (K, V) buffers
   const int smem_k = 6 * 64 * (HD + 8) * 2 + 4 * 64 * 4;     // K, V + two (Q, dO, lse, D) buffers
   static bool set = false;
@@ -522,8 +528,14 @@ cudaError_t attn_bwd_launch(const bf16* qkv, long long ld, const bf16* dout, con
   }
   dim3 gq((maxlen + 63) / 64, nh, nseq);
   ls::attn_bwd_dq_kernel<HD><<<gq, 128, smem_q, st>>>(qkv, ld, dout, lddo, lse, D, cu, nh, nkv, scale, dqkv, ldg, T);
-  dim3 gk((maxlen + 63) / 64, nkv, nseq);
-  ls::attn_bwd_dkdv_kernel<HD><<<gk, 128, smem_k, st>>>(qkv, ld, dout, lddo, lse, D, cu, nh, nkv, scale, dqkv, ldg, T);
+  const int hsplit = part ? nh / nkv : 1;
+  dim3 gk((maxlen + 63) / 64, nkv * hsplit, nseq);
+  ls::attn_bwd_dkdv_kernel<HD><<<gk, 128, smem_k, st>>>(qkv, ld, dout, lddo, lse, D, cu, nh, nkv, scale, dqkv, ldg, T,
+                                                        hsplit, part);
+  if (hsplit > 1) {
+    const long long n = (long long)T * 2 * nkv * HD;
+    ls::attn_dkdv_reduce_kernel<<<grid1d(n, 256), 256, 0, st>>>(part, hsplit, nh, nkv, HD, T, dqkv, ldg);
+  }
   return cudaGetLastError();
 }
 
@@ -534,9 +546,10 @@ cudaError_t attn_fwd(int hd, const bf16* qkv, long long ld, const int* cu, int n
 }
 cudaError_t attn_bwd(int hd, const bf16* qkv, long long ld, const bf16* dout, const bf16* o, long long lddo,
                      const float* lse, const int* cu, int nseq, int maxlen, int nh, int nkv, float* D, float* dqkv,
-                     long long ldg, int T, cudaStream_t st) {
-  return hd == 64 ? attn_bwd_launch<64>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st)
-                  : attn_bwd_launch<128>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st);
+                     long long ldg, int T, cudaStream_t st, float* part = nullptr) {
+  return hd == 64
+             ? attn_bwd_launch<64>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st, part)
+             : attn_bwd_launch<128>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st, part);
 }
 
 cudaError_t lora_outer(const bf16* X, long long ldx, int ncols, const float* Uf, const bf16* Ub, int ldu, int r, int T,
@@ -850,8 +863,8 @@ int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int 
               nullptr, 0, st));
   GEMM_T(LS_K_ATTN_BWD, 2 * attn_flop(c, T, nseq), 2.0 * T * (c->nqkv + 2 * c->nq) + 4.0 * T * c->nqkv,
          attn_bwd(c->hd, c->qkv, c->nqkv, c->do_bf, c->attn_o, c->nq, c->lse_attn, cu, nseq, c->maxlen, c->nh,
-                  c->nkv, c->Dattn, c->dqkv_f, c->nqkv, T, st));
-  c->st.kernel_launches += 2;
+                  c->nkv, c->Dattn, c->dqkv_f, c->nqkv, T, st, c->nh > c->nkv ? c->attn_part : nullptr));
+  c->st.kernel_launches += c->nh > c->nkv ? 3 : 2;
   {
     const long long n = (long long)T * c->nqkv;
     TIMED(LS_K_OTHER, 0, 6.0 * n, 1,
