@@ -543,3 +543,51 @@ def test_layer_file_errors_are_reported(tmp_path):
     assert "shorter" in L.last_error(st.ctx)
     assert L.lib().load_layer_file(st.ctx, 0, str(tmp_path / "missing.bin").encode(), 0) == L.LS_ERR_ARG
     st.close()
+
+
+def test_degenerate_inputs():
+    """Empty batches and out-of-range sizes are refused on the host; a zero-row product
+    launches nothing; single-token sequences (no next-token target) contribute zero
+    logprob and the rest of the batch is unaffected."""
+    import ctypes as C
+    cfg = SMALL_DPO.with_(method="sft", prompt_len=0)
+    st = _stack(cfg, max_tokens=cfg.tokens, max_seqs=6)
+    tok, cu, mask = _batch(cfg)
+    t, c, m = st.upload_batch(tok, cu, mask)
+    sums = torch.empty(cfg.nseq, dtype=torch.float32, device=DEV)
+    assert L.lib().stream_step_fwd(st.ctx, t.data_ptr(), 0, cfg.nseq, c.data_ptr(), m.data_ptr(), 1, 0,
+                                   sums.data_ptr()) == L.LS_ERR_ARG
+    st.close()
+    st = _stack(cfg, max_tokens=cfg.tokens, max_seqs=6)
+    assert L.lib().stream_step_fwd(st.ctx, t.data_ptr(), cfg.tokens + 1, cfg.nseq, c.data_ptr(), m.data_ptr(), 1, 0,
+                                   sums.data_ptr()) == L.LS_ERR_ARG
+    st.close()
+    # single-token sequences next to a normal one
+    st = _stack(cfg, max_tokens=cfg.tokens, max_seqs=6)
+    cu1 = np.array([0, 1, 2, 50, 51], np.int32)
+    tok1 = tok[:51]
+    mask1 = np.ones(51, np.uint8)
+    mask1[cu1[1:] - 1] = 0
+    t1, c1, m1 = st.upload_batch(tok1, cu1, mask1)
+    st.fwd(t1, c1, m1, adapter_on=True, save=False)
+    lp1, _ = st.logprobs(51)
+    cu2 = np.array([0, 48], np.int32)
+    t2, c2, m2 = st.upload_batch(tok[2:50], cu2, np.ones(48, np.uint8))
+    st.fwd(t2, c2, m2, adapter_on=True, save=False)
+    lp2, _ = st.logprobs(48)
+    assert st.sync(60000) == 0
+    st.close()
+    lp1n, lp2n = to_np(lp1), to_np(lp2)
+    assert lp1n[0] == 0.0 and lp1n[1] == 0.0 and lp1n[50] == 0.0
+    # the 48-token sequence gives the same logprobs wherever it sits in the batch
+    np.testing.assert_array_equal(lp1n[2:50], lp2n)
+    # zero-row product: nothing launched, output untouched
+    w = synth.weight(cfg, 0, "q")
+    pk, am = L.quantize_host(w)
+    p, a = torch.from_numpy(pk).to(DEV), torch.from_numpy(am).to(DEV)
+    out = torch.full((4, w.shape[0]), 7.0, dtype=torch.bfloat16, device=DEV)
+    x = torch.zeros((4, w.shape[1]), dtype=torch.bfloat16, device=DEV)
+    L.call("lsk_nf4_gemm", 0, x, w.shape[1], 0, p, a, w.shape[0], w.shape[1], None, None, 0, 0, out, w.shape[0], None,
+           0, 0, 0, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
