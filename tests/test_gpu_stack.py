@@ -360,14 +360,9 @@ def test_unpinned_layer_memory_is_refused():
 
 # ------------------------------------------------------------------ full sizes
 
-@pytest.mark.slow
-def test_llama8b_full_sampled_layers_and_vocab_match_oracle():
-    """The full 32-layer Llama-3.1-8B-shaped stack in the bench's launch configuration
-    (shared-read DPO forward over 2 x 512 tokens): layers 0, 15 and 31 recomputed by the
-    oracle from the GPU's own stored input of each (normwise <= 1e-2), and the full
-    128256-row vocabulary head on 16 sampled token rows from the GPU's final hidden
-    state (per-token logprob and log-sum-exp <= 2e-2)."""
-    cfg = synth.LLAMA_8B
+def _full_size_sampled(cfg, sample_layers):
+    """Run the stack's shared-read DPO forward in the bench's launch configuration and
+    check sampled layers and vocabulary rows against the oracle, teacher-forced."""
     tok, cu, mask = _batch(cfg)
     st = _stack(cfg)
     t, c, m = st.upload_batch(tok, cu, mask)
@@ -375,7 +370,6 @@ def test_llama8b_full_sampled_layers_and_vocab_match_oracle():
     ref = torch.empty_like(pi)
     st.fwd_dpo(t, c, m, pi, ref)
     lp, lse = st.logprobs()
-    sample_layers = [0, 15, 31]
     acts = {l: st.activation(l, len(tok)) for l in sample_layers + [l + 1 for l in sample_layers]}
     hL = st.activation(cfg.layers, len(tok))
     assert st.sync(300000) == 0, L.last_error(st.ctx)
@@ -399,6 +393,24 @@ def test_llama8b_full_sampled_layers_and_vocab_match_oracle():
     # policy rows are the first T of the shared pass
     assert np.abs(to_np(lse)[rows] - lse_o).max() <= TOL_LP
     assert np.abs(to_np(lp)[rows] - lp_o).max() <= TOL_LP
+
+
+@pytest.mark.slow
+def test_llama8b_full_sampled_layers_and_vocab_match_oracle():
+    """The full 32-layer Llama-3.1-8B-shaped stack in the bench's launch configuration
+    (shared-read DPO forward over 2 x 512 tokens): layers 0, 15 and 31 recomputed by the
+    oracle from the GPU's own stored input of each (normwise <= 1e-2), and the full
+    128256-row vocabulary head on 16 sampled token rows from the GPU's final hidden
+    state (per-token logprob and log-sum-exp <= 2e-2)."""
+    _full_size_sampled(synth.LLAMA_8B, [0, 15, 31])
+
+
+@pytest.mark.slow
+def test_qwen32b_full_capped_sampled_layers_and_vocab_match_oracle():
+    """The full 64-layer Qwen2.5-32B-shaped stack under its 4 GiB workspace cap
+    (shared-read DPO forward over 2 x 1024 tokens): layers 0 and 63 and 16 rows of the
+    152064-row vocabulary head against the oracle, teacher-forced, as above."""
+    _full_size_sampled(synth.QWEN_32B, [0, 63])
 
 
 @pytest.mark.slow
