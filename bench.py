@@ -44,11 +44,11 @@ import synth  # noqa: E402
 
 METRIC = "train tokens/s streamed NF4 LoRA (8B shape, SFT+DPO); H2D GB/s; % roofline"
 # DRAM bytes (read + write) per algorithmic byte of the forward NF4 GEMM, from one ncu
-# capture of the 8B gate|up launch (M 2048, N 28672, K 4096: 156.0 MB measured against
-# 200.3 MB algorithmic; output rows partly still in L2 at kernel end).  It scales the
-# class's algorithmic bytes per launch to the reported traffic; set to None whenever the
-# kernel changes until it is captured again.
-GEMM_FWD_TRAFFIC_PER_ALG_BYTE = 156.0 / 200.3
+# capture of the 8B gate|up launch on the split schedule (M 2048, N 28672, K 4096:
+# 86.0 MB read + 106.1 MB written against 200.3 MB algorithmic; output rows partly still
+# in L2 at kernel end).  It scales the class's algorithmic bytes per launch to the
+# reported traffic; set to None whenever the kernel changes until it is captured again.
+GEMM_FWD_TRAFFIC_PER_ALG_BYTE = 192.1 / 200.3
 UNIT = "tokens/s"
 NF4_BYTES_PER_PARAM = 0.5625
 
@@ -442,13 +442,16 @@ def run_gpu_arm(args, s, ws, rank, local):
 
 
 def gemm_microbench(spec: str, reps: int = 10) -> dict:
-    """One NF4-dequant-fused matrix product through the C ABI (lsk_nf4_gemm), timed with
-    CUDA events after warm-up: spec = "mode,M,N,K[,bn,nacc]" (mode 0: Y = X deq(W)^T,
-    mode 1: dX = dY deq(W); W [N, K] drawn N(0, 0.02) and NF4-quantised on the host)."""
+    """One NF4-dequant-fused matrix product through the C ABI (lsk_nf4_gemm_sk, the
+    schedule the training step uses), timed with CUDA events after warm-up:
+    spec = "mode,M,N,K[,bn,nacc[,split]]" (mode 0: Y = X deq(W)^T, mode 1: dX = dY deq(W);
+    W [N, K] drawn N(0, 0.02) and NF4-quantised on the host; split 0 = cost model,
+    1 = split tiles, -1 = whole tiles)."""
     import layer_streamed_nf4_dequant_b300 as L
     f = [int(x) for x in spec.split(",")]
     mode, M, N, K = f[:4]
     bn, nacc = (f[4], f[5]) if len(f) >= 6 else (0, 0)
+    split = f[6] if len(f) >= 7 else 0
     dev = torch.device("cuda:0")
     g = torch.Generator().manual_seed(0)
     pk, am = L.quantize_host((torch.randn(N, K, generator=g) * 0.02).numpy())
@@ -457,10 +460,11 @@ def gemm_microbench(spec: str, reps: int = 10) -> dict:
     x = torch.randn(M, red, device=dev).to(torch.bfloat16)
     out = torch.empty(M, outc, device=dev, dtype=torch.bfloat16 if mode == 0 else torch.float32)
     st = torch.cuda.current_stream().cuda_stream
+    ws = torch.zeros(int(L.lib().lsk_nf4_gemm_workspace_bytes()), dtype=torch.uint8, device=dev)
 
     def run():
-        L.call("lsk_nf4_gemm", mode, x, red, M, p, a, N, K, None, None, 0, 0 if mode == 0 else 1, out, outc, None, 0,
-               bn, nacc, st)
+        L.call("lsk_nf4_gemm_sk", mode, x, red, M, p, a, N, K, None, None, 0, 0 if mode == 0 else 1, out, outc, None,
+               0, bn, nacc, split, ws, ws.numel(), st)
 
     for _ in range(3):
         run()
@@ -474,7 +478,7 @@ def gemm_microbench(spec: str, reps: int = 10) -> dict:
     us = e0.elapsed_time(e1) / reps * 1e3
     peaks = read_peaks()
     tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
-    return {"kernel": "nf4_gemm", "mode": mode, "M": M, "N": N, "K": K, "bn": bn, "nacc": nacc,
+    return {"kernel": "nf4_gemm", "mode": mode, "M": M, "N": N, "K": K, "bn": bn, "nacc": nacc, "split": split,
             "us": round(us, 2), "tflops": round(tf, 1), "frac_of_burst_peak": round(tf / peaks["bf16_tflops"], 4),
             "peak_source": peaks["source"]}
 

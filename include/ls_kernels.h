@@ -39,6 +39,29 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
                  int32_t ext_k, int32_t epi, void* out, int64_t ldo, const uint16_t* residual, int64_t ldr,
                  int32_t force_bn, int32_t force_nacc, void* stream);
 
+/* The same product with a stream-K tile schedule available (the stack's own GEMMs use
+ * it).  One CTA per SM: whole 256 x 256 tiles round-robin, then the k-iterations of the
+ * remaining tiles split evenly over the SMs; a CTA whose share starts inside a tile
+ * leaves an fp32 partial in `workspace`, and the CTA holding that tile's first
+ * k-iteration adds the partials, in CTA order, before the epilogue (so the result is
+ * deterministic, but split tiles sum in a different order than whole ones).  The split
+ * launch is cooperative (all CTAs resident at once); its waits are time-bounded and a
+ * timeout sets the device error word (lsk_device_error).
+ *  split: 0 = the cost model chooses between whole tiles and the split schedule,
+ *         1 = split schedule whenever M > 128 (tests), -1 = whole tiles only.
+ *  workspace: device memory, >= lsk_nf4_gemm_workspace_bytes() bytes, 256-byte
+ *         aligned, zero-filled once before its first use (it holds epoch words that
+ *         must not match a future launch; no reset is needed between calls).  Calls
+ *         sharing a workspace must be ordered (one stream, or events): two in flight at
+ *         once corrupt each other's partials.
+ * Other arguments and errors as lsk_nf4_gemm. */
+uint64_t lsk_nf4_gemm_workspace_bytes(void);
+int lsk_nf4_gemm_sk(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const uint8_t* w_packed,
+                    const float* w_absmax, int32_t N, int32_t K, const uint16_t* ext_a, const uint16_t* ext_b,
+                    int32_t ext_k, int32_t epi, void* out, int64_t ldo, const uint16_t* residual, int64_t ldr,
+                    int32_t force_bn, int32_t force_nacc, int32_t split, void* workspace,
+                    uint64_t workspace_bytes, void* stream);
+
 /* RMSNorm: y = bf16(w * bf16(x * rstd)), rstd = 1/sqrt(mean(x^2) + eps) (fp32).
  * x, y bf16 [T, H] (H % 8 == 0), w bf16 [H], rstd fp32 [T] (may be NULL). */
 int lsk_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, float* rstd, int32_t T, int32_t H,
@@ -140,10 +163,11 @@ int lsk_build_ext_fwd(const uint16_t* b_q, int32_t q0, int32_t nq, const uint16_
 int lsk_build_ext_bwd(const uint16_t* a_q, const uint16_t* a_v, int32_t r, int32_t K, uint16_t* ext,
                       void* stream);
 
-/* NF4 embedding gather: x[t] = dequant(row tokens[t]); packed/absmax may be mapped
- * pinned host memory. */
-int lsk_embed_gather(const int32_t* tokens, const uint8_t* packed, const float* absmax, uint16_t* x, int32_t T,
-                     int32_t H, void* stream);
+/* NF4 embedding gather: x[t] = dequant(row tokens[t]) of the V-row table; packed/absmax
+ * may be mapped pinned host memory.  A token id outside [0, V) gives a zero row and sets
+ * the device error word (lsk_device_error). */
+int lsk_embed_gather(const int32_t* tokens, const uint8_t* packed, const float* absmax, int32_t V, uint16_t* x,
+                     int32_t T, int32_t H, void* stream);
 
 /* Vocabulary logprobs without materialising the logits: logits = h . deq(W)^T
  * (h bf16 [T, H], W NF4 [V, H]) reduced on the fly to per-128-column (max, sum-exp)

@@ -101,6 +101,7 @@ _SIGS = {
     "ls_profile_read": [P, C.POINTER(ls_profile_t)],
     "lsk_nf4_dequant": [P, P, I64, I32, P, P],
     "lsk_nf4_gemm": [I32, P, I64, I32, P, P, I32, I32, P, P, I32, I32, P, I64, P, I64, I32, I32, P],
+    "lsk_nf4_gemm_sk": [I32, P, I64, I32, P, P, I32, I32, P, P, I32, I32, P, I64, P, I64, I32, I32, I32, P, U64, P],
     "lsk_rmsnorm_fwd": [P, P, P, P, I32, I32, F32, P],
     "lsk_rmsnorm_bwd": [P, P, P, P, P, P, I32, I32, I32, P],
     "ls_rope_table": [P, P, I32, I32, F32],
@@ -116,7 +117,7 @@ _SIGS = {
     "lsk_lora_outer_noalloc": [P, I64, I32, P, P, I32, I32, I32, I32, I32, I32, P, P],
     "lsk_build_ext_fwd": [P, I32, I32, P, I32, I32, I32, I32, P, P],
     "lsk_build_ext_bwd": [P, P, I32, I32, P, P],
-    "lsk_embed_gather": [P, P, P, P, I32, I32, P],
+    "lsk_embed_gather": [P, P, P, I32, P, I32, I32, P],
     "lsk_vocab_logprob": [P, I32, I32, P, P, I32, P, P, P, P, P, P],
     "lsk_vocab_bwd": [P, I32, I32, P, P, I32, I32, P, P, P, P, P, I32, P],
     "lsk_device_error": [C.POINTER(I32), I32],
@@ -142,6 +143,8 @@ def lib() -> C.CDLL:
             f.restype = C.c_int
         l.ls_last_error.argtypes = [P]
         l.ls_last_error.restype = C.c_char_p
+        l.lsk_nf4_gemm_workspace_bytes.argtypes = []
+        l.lsk_nf4_gemm_workspace_bytes.restype = U64
         _lib = l
     return _lib
 

@@ -89,6 +89,20 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // ------------------------------------------------------------------ forward
 // grid (ceil(maxlen / 64), nh, nseq), 128 threads: warp w owns query rows 16w..16w+15.
+// Rows [a, a + L) of sequence s.  The offsets come from the caller; a list that is not
+// 0 <= cu[s] <= cu[s+1] <= T is clamped into the batch and raises the device error word,
+// so a malformed batch cannot make a kernel read or write outside its buffers.
+__device__ __forceinline__ void seq_range(const int* __restrict__ cu, int s, int T, int& a, int& L) {
+  int x = cu[s], y = cu[s + 1];
+  if (x < 0 || y < x || y > T) {
+    raise_error(DEV_BAD_ARG);
+    x = min(max(x, 0), T);
+    y = min(max(y, x), T);
+  }
+  a = x;
+  L = y - x;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(128) attn_fwd_kernel(const __nv_bfloat16* __restrict__ qkv, long long ld,
                                                        const int* __restrict__ cu, int nh, int nkv, float scale,
@@ -99,7 +113,8 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const __nv_bfloat16* __re
   // Q, then two (K, V) buffers: the next key tile is copied while this one computes
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(attn_smem);
   const int s = blockIdx.z, h = blockIdx.y;
-  const int a = cu[s], L = cu[s + 1] - a;
+  int a, L;
+  seq_range(cu, s, T, a, L);
   const int q0 = blockIdx.x * 64;
   if (q0 >= L) return;
   const int g = h / (nh / nkv);
@@ -245,7 +260,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const __nv_bfloat16* _
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(attn_smem);
   __nv_bfloat16* sO = sQ + 64 * LDS;
   const int s = blockIdx.z, h = blockIdx.y;
-  const int a = cu[s], L = cu[s + 1] - a;
+  int a, L;
+  seq_range(cu, s, T, a, L);
   const int q0 = blockIdx.x * 64;
   if (q0 >= L) return;
   const int g = h / (nh / nkv);
@@ -361,7 +377,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16*
   __nv_bfloat16* sV = sK + 64 * LDS;
   float* sLD = reinterpret_cast<float*>(sV + 5 * 64 * LDS);   // [2][2][64]
   const int s = blockIdx.z, g = blockIdx.y / hsplit, hs = blockIdx.y % hsplit;
-  const int a = cu[s], L = cu[s + 1] - a;
+  int a, L;
+  seq_range(cu, s, T, a, L);
   const int k0 = blockIdx.x * 64;
   if (k0 >= L) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

@@ -66,6 +66,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
   }
 }
+// ----------------------------------------------------------------- flags between CTAs
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Bounded wait until *p == v (another CTA of the same grid publishes it); false (and
+// the error flag) on timeout.
+__device__ __forceinline__ bool flag_wait_eq(const unsigned* p, unsigned v) {
+  if (ld_acquire_gpu(p) == v) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    for (int i = 0; i < 16; ++i) {
+      __nanosleep(64);
+      if (ld_acquire_gpu(p) == v) return true;
+    }
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      raise_error(DEV_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Arrive on `bar` once all of this thread's earlier cp.async copies have landed.
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");

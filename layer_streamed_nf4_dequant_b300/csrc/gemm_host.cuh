@@ -1,5 +1,6 @@
 // Host side of the NF4 GEMM: tensor-map encoding, tile-shape choice, launch.
 #pragma once
+#include <atomic>
 #include <mutex>
 #include "nf4_gemm.cuh"
 
@@ -36,6 +37,47 @@ static bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Stream-K scratch: kSkMaxCtas x 8 epoch words, then one fp32 partial tile per CTA.
+// The words must not hold a future epoch before first use (zero-fill once); epochs come
+// from one process-wide counter, so no reset between launches is needed.
+struct SkWorkspace {
+  float* ws = nullptr;
+  unsigned* flags = nullptr;
+};
+constexpr size_t kSkFlagBytes = 8192;
+constexpr size_t kSkWorkspaceBytes = kSkFlagBytes + (size_t)kSkMaxCtas * kSkSlotFloats * sizeof(float);
+static_assert((size_t)kSkMaxCtas * 8 * sizeof(unsigned) <= kSkFlagBytes, "flag words");
+
+static inline SkWorkspace sk_workspace_at(void* base) {
+  SkWorkspace w;
+  if (base) {
+    w.flags = reinterpret_cast<unsigned*>(base);
+    w.ws = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(base) + kSkFlagBytes);
+  }
+  return w;
+}
+
+static unsigned next_sk_epoch() {
+  static std::atomic<unsigned> epoch{0};
+  unsigned e = ++epoch;
+  if (e == 0) e = ++epoch;
+  return e;
+}
+
+// CTAs of a split schedule: one per SM (the split tiles use one CTA per SM), at most
+// kSkMaxCtas.
+static int sk_max_ctas() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kSkMaxCtas;
+  static int cached[64] = {0};
+  if (cached[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = kSkMaxCtas;
+    cached[dev] = sms < kSkMaxCtas ? sms : kSkMaxCtas;
+  }
+  return cached[dev];
+}
+
 struct GemmCall {
   int mode;                          // GEMM_FWD / GEMM_DX
   const __nv_bfloat16* A;            // [M, Kred] bf16, row pitch lda elements
@@ -44,16 +86,23 @@ struct GemmCall {
   const __nv_bfloat16* ext_a;        // [M, 64] bf16 (when ext_k > 0)
   int force_bn;                      // 0 = choose
   int force_nacc;                    // 0 = choose
+  SkWorkspace sk;                    // stream-K scratch (none: whole tiles only)
+  int split;                         // 0 = by the cost model, 1 = split schedule when possible, -1 = never
   GemmArgs g;
 };
 
 template <int NACC, int BN, int S, int SB, int MODE>
-static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
+static cudaError_t launch_cfg(const GemmCall& c, bool split, cudaStream_t st) {
   using C = GemmCfg<NACC, BN, S, SB>;
-  auto kern = nf4_gemm_kernel<NACC, BN, S, SB, MODE>;
+  // split schedules only for the one-CTA-per-SM (NACC = 2) tiles
+  constexpr bool kCanSplit = NACC == 2;
+  auto kern_whole = nf4_gemm_kernel<NACC, BN, S, SB, MODE, false>;
+  auto kern_split = nf4_gemm_kernel<NACC, BN, S, SB, MODE, kCanSplit>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern_whole, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e == cudaSuccess && kCanSplit)
+      e = cudaFuncSetAttribute(kern_split, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -84,10 +133,60 @@ static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
   // N-fastest order lets a wave share activation tiles instead.
   GemmArgs ga = g;
   ga.n_fast = (double)g.M * g.Kred * 2.0 > (double)g.Nw * g.Kw * 0.5625;
-  const unsigned tm = (unsigned)((g.M + C::BM - 1) / C::BM), tn = (unsigned)((g.Nout + BN - 1) / BN);
-  dim3 grid = ga.n_fast ? dim3(tn, tm) : dim3(tm, tn);
-  kern<<<grid, C::THREADS, C::SMEM, st>>>(tA, tW, tX, ga);
-  return cudaGetLastError();
+  const long long tm = (g.M + C::BM - 1) / C::BM, tn = (g.Nout + BN - 1) / BN, nt = tm * tn;
+  const int niter = g.Kred / 64 + (g.ext_k > 0 ? 1 : 0);
+  ga.tiles_m = (int)tm;
+  ga.tiles_n = (int)tn;
+  ga.sk_iters = 0;
+  ga.sk_ws = nullptr;
+  ga.sk_flags = nullptr;
+  ga.sk_epoch = 0;
+  // whole tiles, one per CTA
+  ga.sched_ctas = (int)nt;
+  ga.sched_dp = 1;
+  if (split && kCanSplit && c.sk.ws && c.sk.flags) {
+    // one CTA per SM: full rounds of whole tiles, then the last one to two rounds' worth
+    // of tiles split evenly by k-iterations (each CTA at least 4 of them)
+    const int gmax = sk_max_ctas();
+    const long long full = nt / gmax;
+    if (nt % gmax == 0) {
+      ga.sched_ctas = gmax;
+      ga.sched_dp = (int)full;
+    } else {
+      const long long dp = full > 0 ? full - 1 : 0;
+      const long long iters = (nt - dp * gmax) * niter;
+      long long G = gmax;
+      if (dp == 0 && iters / 4 < G) G = iters / 4 > 0 ? iters / 4 : 1;
+      if (G > 1) {
+        ga.sched_ctas = (int)G;
+        ga.sched_dp = (int)dp;
+        ga.sk_iters = iters;
+        ga.sk_ws = c.sk.ws;
+        ga.sk_flags = c.sk.flags;
+        ga.sk_epoch = next_sk_epoch();
+      }
+    }
+  }
+  if (ga.sk_iters == 0) {
+    if (ga.sched_dp == 1 && ga.sched_ctas == nt)
+      kern_whole<<<(unsigned)nt, C::THREADS, C::SMEM, st>>>(tA, tW, tX, ga);
+    else   // whole tiles, several per CTA
+      kern_split<<<(unsigned)ga.sched_ctas, C::THREADS, C::SMEM, st>>>(tA, tW, tX, ga);
+    return cudaGetLastError();
+  }
+  // CTAs of a split schedule wait for one another's partial tiles: a cooperative launch
+  // guarantees they are all resident at once (or fails instead of starting).
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)ga.sched_ctas);
+  lc.blockDim = dim3(C::THREADS);
+  lc.dynamicSmemBytes = C::SMEM;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kern_split, tA, tW, tX, ga);
 }
 
 // Pick the tile shape by estimated time = waves x per-CTA time.  Per-CTA time per
@@ -97,7 +196,7 @@ static cudaError_t launch_cfg(const GemmCall& c, cudaStream_t st) {
 // so past one CTA per SM they share it (time x 2 per 296 CTAs).  Grids smaller than the
 // SM count finish in one CTA time: there the smallest tile wins (the 3B-shape products
 // at 512 rows gain 15-20%); large grids prefer 256 x 256 (half the dequant per MMA FLOP).
-static void choose_tile(int mode, int M, int Nout, int& nacc, int& bn) {
+static double choose_tile(int mode, int M, int Nout, int& nacc, int& bn) {
   const int sms = 148;
   struct Opt {
     int nacc, bn, per_sm;
@@ -123,24 +222,42 @@ static void choose_tile(int mode, int M, int Nout, int& nacc, int& bn) {
       bn = o.bn;
     }
   }
+  return best;
 }
 
+// With stream-K scratch the 256 x 256 tile can also run as a split schedule: every SM
+// gets the same number of k-iterations, so the estimate is tiles / SMs tile times (plus
+// the partial-tile exchange) instead of whole waves.
 static cudaError_t launch_nf4_gemm(const GemmCall& c, cudaStream_t st) {
   const GemmArgs& g = c.g;
   int nacc = 0, bn = 0;
-  choose_tile(c.mode, g.M, g.Nout, nacc, bn);
+  const double t_whole = choose_tile(c.mode, g.M, g.Nout, nacc, bn);
+  bool split = false;
+  if (c.sk.ws && c.split >= 0 && g.M > 128) {
+    const double nt = (double)((g.M + 255) / 256) * (double)((g.Nout + 255) / 256);
+    // the split kernel's k-iteration costs 1.09 x the whole-tile kernel's (measured on
+    // the 8B product shapes), plus about 12 k-iterations per CTA for the partial-tile
+    // exchange and the extra pipeline fill
+    const int niter = g.Kred / 64 + (g.ext_k > 0 ? 1 : 0);
+    const double t_split = 1.09 * nt / sk_max_ctas() + 12.0 / niter;
+    if (c.split > 0 || t_split < t_whole) {
+      split = true;
+      nacc = 2;
+      bn = 256;
+    }
+  }
   if (c.force_bn) bn = c.force_bn;
   if (c.force_nacc) nacc = c.force_nacc;
   if (c.mode == GEMM_FWD) {
-    if (nacc == 2 && bn == 256) return launch_cfg<2, 256, 3, 2, GEMM_FWD>(c, st);
-    if (nacc == 2 && bn == 128) return launch_cfg<2, 128, 4, 2, GEMM_FWD>(c, st);
-    if (nacc == 1 && bn == 256) return launch_cfg<1, 256, 4, 2, GEMM_FWD>(c, st);
-    return launch_cfg<1, 128, 3, 2, GEMM_FWD>(c, st);
+    if (nacc == 2 && bn == 256) return launch_cfg<2, 256, 3, 2, GEMM_FWD>(c, split, st);
+    if (nacc == 2 && bn == 128) return launch_cfg<2, 128, 4, 2, GEMM_FWD>(c, split, st);
+    if (nacc == 1 && bn == 256) return launch_cfg<1, 256, 4, 2, GEMM_FWD>(c, false, st);
+    return launch_cfg<1, 128, 3, 2, GEMM_FWD>(c, false, st);
   } else {
-    if (nacc == 2 && bn == 256) return launch_cfg<2, 256, 3, 2, GEMM_DX>(c, st);
-    if (nacc == 2 && bn == 128) return launch_cfg<2, 128, 4, 2, GEMM_DX>(c, st);
-    if (nacc == 1 && bn == 256) return launch_cfg<1, 256, 4, 2, GEMM_DX>(c, st);
-    return launch_cfg<1, 128, 3, 2, GEMM_DX>(c, st);
+    if (nacc == 2 && bn == 256) return launch_cfg<2, 256, 3, 2, GEMM_DX>(c, split, st);
+    if (nacc == 2 && bn == 128) return launch_cfg<2, 128, 4, 2, GEMM_DX>(c, split, st);
+    if (nacc == 1 && bn == 256) return launch_cfg<1, 256, 4, 2, GEMM_DX>(c, false, st);
+    return launch_cfg<1, 128, 3, 2, GEMM_DX>(c, false, st);
   }
 }
 

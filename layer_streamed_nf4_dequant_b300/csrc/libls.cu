@@ -163,6 +163,8 @@ struct ls_ctx {
   int32_t *tgt, *pos;
   int32_t *tok2 = nullptr, *cu2 = nullptr;   // shared-read DPO forward: doubled batch
   float* attn_part = nullptr;                 // per-query-head dk / dv partials
+  ls::SkWorkspace skw;                        // split-tile (stream-K) scratch of the NF4 GEMMs
+  bool whole_tiles_only = false;              // set while the shared-read DPO forward runs
   int Tf = 0;                                 // forward row capacity (2 max_tokens with shared read)
   int P = 0;
   size_t lora_part_floats = 0;
@@ -189,6 +191,14 @@ struct ls_ctx {
 };
 
 namespace {
+
+// Split-tile scratch for the stack's NF4 GEMMs, or none (whole tiles).  The shared-read
+// DPO forward stacks the policy and reference copies of the batch into one product;
+// whole tiles make each output row depend on that row's inputs alone, so identical
+// policy and reference rows give bit-identical results (the B = 0 start has policy =
+// reference exactly), which a split tile schedule (different k-splits for the two
+// halves' tiles) would not.
+ls::SkWorkspace gemm_ws(const ls_ctx* c) { return c->whole_tiles_only ? ls::SkWorkspace{} : c->skw; }
 
 int fail(ls_ctx* c, int code, const std::string& m) {
   if (c && c->err == 0) {
@@ -425,6 +435,7 @@ Planned lay_out(const ls_config& k, ls_ctx* c) {
   int32_t* pos = b.take<int32_t>(Tf);
   int32_t* tok2 = k.dpo_shared_read ? b.take<int32_t>(Tf) : nullptr;
   int32_t* cu2 = k.dpo_shared_read ? b.take<int32_t>(2 * (size_t)k.max_seqs + 1) : nullptr;
+  uint8_t* skbase = b.take<uint8_t>(ls::kSkWorkspaceBytes);
   p.total = align_up(b.off, 256);
 
   if (c) {
@@ -449,6 +460,7 @@ Planned lay_out(const ls_config& k, ls_ctx* c) {
     c->tgt_logit = tl; c->lse_save = lses; c->lse_tmp = lset; c->lp = lp; c->coef = coef; c->dhf = dhf;
     c->loss_tmp = losst; c->tgt = tgt; c->pos = pos; c->P = p.P;
     c->tok2 = tok2; c->cu2 = cu2; c->Tf = (int)Tf; c->attn_part = apart;
+    c->skw = ls::sk_workspace_at(skbase);
     c->vrows = vrows; c->nvch = nvch; c->vch_abs_off = abs_off;
   }
   return p;
@@ -465,7 +477,8 @@ inline int grid1d(long long n, int threads, int cap = 148 * 16) {
 
 cudaError_t gemm(int mode, const bf16* A, long long lda, int M, const uint8_t* Wp, const float* Wa, int Nw, int Kw,
                  const bf16* ext_a, const bf16* ext_b, int ext_k, int epi, void* out, long long ldo,
-                 const bf16* residual, long long ldr, cudaStream_t st, int force_bn = 0, int force_nacc = 0) {
+                 const bf16* residual, long long ldr, cudaStream_t st, ls::SkWorkspace sk = {}, int force_bn = 0,
+                 int force_nacc = 0, int split = 0) {
   GemmCall c{};
   c.mode = mode;
   c.A = A;
@@ -474,6 +487,8 @@ cudaError_t gemm(int mode, const bf16* A, long long lda, int M, const uint8_t* W
   c.ext_a = ext_a;
   c.force_bn = force_bn;
   c.force_nacc = force_nacc;
+  c.sk = sk;
+  c.split = split;
   GemmArgs& g = c.g;
   g.M = M;
   g.Nw = Nw;
@@ -805,7 +820,7 @@ int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16*
   const int ek = use ? 32 : 0;
   GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, c->nqkv, H, ek), gemm_bytes(0, T, c->nqkv, H, 2, false),
          gemm(ls::GEMM_FWD, c->n1, H, T, w.pqkv, w.aqkv, c->nqkv, H, c->u_ext, c->ext_fwd, ek, ls::EPI_BF16, c->qkv,
-              c->nqkv, nullptr, 0, st));
+              c->nqkv, nullptr, 0, st, gemm_ws(c)));
   {
     const long long n = (long long)T * (c->nh + c->nkv) * (c->hd / 2);
     TIMED(LS_K_OTHER, 0, 4.0 * n * 2, 1,
@@ -816,12 +831,12 @@ int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16*
          attn_fwd(c->hd, c->qkv, c->nqkv, cu, nseq, c->maxlen, c->nh, c->nkv, c->attn_o, c->nq, c->lse_attn, T, st));
   GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, H, c->nq, 0), gemm_bytes(0, T, H, c->nq, 2, true),
          gemm(ls::GEMM_FWD, c->attn_o, c->nq, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->x1, H,
-              x_in, H, st));
+              x_in, H, st, gemm_ws(c)));
   TIMED(LS_K_OTHER, 0, 4 * TH, 1,
         ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->x1, w.w2, c->n2, c->rstd2, T, H, c->cfg.eps));
   GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, 2 * I, H, 0), gemm_bytes(0, T, 2 * I, H, 2, false),
          gemm(ls::GEMM_FWD, c->n2, H, T, w.pgu, w.agu, 2 * I, H, nullptr, nullptr, 0, ls::EPI_BF16, c->gu, 2 * I,
-              nullptr, 0, st));
+              nullptr, 0, st, gemm_ws(c)));
   if (recompute) return LS_OK;
   {
     const long long n = (long long)T * (I / 8);
@@ -830,7 +845,7 @@ int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16*
   }
   GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, H, I, 0), gemm_bytes(0, T, H, I, 2, true),
          gemm(ls::GEMM_FWD, c->hbuf, I, T, w.pd, w.ad, H, I, nullptr, nullptr, 0, ls::EPI_BF16, x_out, H, c->x1, H,
-              st));
+              st, gemm_ws(c)));
   return LS_OK;
 }
 
@@ -846,7 +861,7 @@ int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int 
   // MLP
   GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, H, I, 0), gemm_bytes(1, T, H, I, 4, false),
          gemm(ls::GEMM_DX, c->gx_bf, H, T, w.pd, w.ad, H, I, nullptr, nullptr, 0, ls::EPI_F32, c->dh, I, nullptr, 0,
-              st));
+              st, gemm_ws(c)));
   {
     const long long n = (long long)T * (I / 4);
     TIMED(LS_K_OTHER, 0, 12.0 * T * I, 1,
@@ -854,13 +869,13 @@ int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int 
   }
   GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, 2 * I, H, 0), gemm_bytes(1, T, 2 * I, H, 4, false),
          gemm(ls::GEMM_DX, c->dgu, 2 * I, T, w.pgu, w.agu, 2 * I, H, nullptr, nullptr, 0, ls::EPI_F32, c->dn, H,
-              nullptr, 0, st));
+              nullptr, 0, st, gemm_ws(c)));
   TIMED(LS_K_OTHER, 0, 16 * TH, 1,
         ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, c->x1, c->rstd2, w.w2, c->gx, c->gx_bf, T, H, 1));
   // attention
   GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, H, c->nq, 0), gemm_bytes(1, T, H, c->nq, 2, false),
          gemm(ls::GEMM_DX, c->gx_bf, H, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->do_bf, c->nq,
-              nullptr, 0, st));
+              nullptr, 0, st, gemm_ws(c)));
   GEMM_T(LS_K_ATTN_BWD, 2 * attn_flop(c, T, nseq), 2.0 * T * (c->nqkv + 2 * c->nq) + 4.0 * T * c->nqkv,
          attn_bwd(c->hd, c->qkv, c->nqkv, c->do_bf, c->attn_o, c->nq, c->lse_attn, cu, nseq, c->maxlen, c->nh,
                   c->nkv, c->Dattn, c->dqkv_f, c->nqkv, T, st, c->nh > c->nkv ? c->attn_part : nullptr));
@@ -896,7 +911,7 @@ int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int 
   const int ek = use ? 32 : 0;
   GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, c->nqkv, H, ek), gemm_bytes(1, T, c->nqkv, H, 4, false),
          gemm(ls::GEMM_DX, c->dqkv_bf, c->nqkv, T, w.pqkv, w.aqkv, c->nqkv, H, c->du_ext, c->ext_bwd, ek, ls::EPI_F32,
-              c->dn, H, nullptr, 0, st));
+              c->dn, H, nullptr, 0, st, gemm_ws(c)));
   TIMED(LS_K_OTHER, 0, 16 * TH, 1,
         ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, x_in, c->rstd1, w.w1, c->gx, c->gx_bf, T, H, 1));
   return LS_OK;
@@ -993,8 +1008,10 @@ int ls_create(const ls_config* cfg, void* d_workspace, uint64_t ws_bytes, void* 
   const int half = c->hd / 2;
   std::vector<float> hc((size_t)c->maxlen * half), hs((size_t)c->maxlen * half);
   ls_rope_table(hc.data(), hs.data(), c->maxlen, c->hd, cfg->rope_theta);
+  // the split-tile epoch words start at zero (no launch uses epoch 0)
   if (cudaMemcpyAsync(c->rope_cos, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice, c->cs) != cudaSuccess ||
       cudaMemcpyAsync(c->rope_sin, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice, c->cs) != cudaSuccess ||
+      cudaMemsetAsync(c->skw.flags, 0, ls::kSkFlagBytes, c->cs) != cudaSuccess ||
       cudaStreamSynchronize(c->cs) != cudaSuccess) {
     ls_destroy(c);
     return set_thread_err(LS_ERR_CUDA, "rope table upload failed");
@@ -1197,7 +1214,7 @@ int stream_step_fwd(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t nseq,
   {
     const long long n = (long long)T * (H / 8);
     TIMED(LS_K_OTHER, 0, (0.5625 + 2.0) * T * H, 1,
-          ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, st>>>(d_tokens, c->emb_p, c->emb_a, x0, T, H));
+          ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, st>>>(d_tokens, c->emb_p, c->emb_a, x0, T, H, c->V));
   }
   bf16* hf = save ? c->hf_save : c->hf_tmp;
   float* rstdf = save ? c->rstdf_save : c->rstdf_tmp;
@@ -1227,6 +1244,7 @@ int stream_step_fwd(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t nseq,
     g.lda = H;
     g.Wp = img;
     g.force_bn = 256;
+    g.sk = gemm_ws(c);
     g.g.M = T; g.g.Nw = n; g.g.Kw = H; g.g.Nout = n; g.g.Kred = H;
     g.g.absmax = reinterpret_cast<const float*>(img + c->vch_abs_off);
     g.g.epi = ls::EPI_LOGPROB;
@@ -1264,6 +1282,11 @@ int stream_step_fwd_dpo(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t n
   for (int l = 0; l < c->L; ++l)
     if (!c->hl_ok[l]) return fail(c, LS_ERR_STATE, "stream_step_fwd_dpo: layer " + std::to_string(l) + " not loaded");
   if (!c->hv_ok) return fail(c, LS_ERR_STATE, "stream_step_fwd_dpo: vocabulary not loaded");
+  struct WholeTiles {
+    ls_ctx* c;
+    explicit WholeTiles(ls_ctx* x) : c(x) { c->whole_tiles_only = true; }
+    ~WholeTiles() { c->whole_tiles_only = false; }
+  } whole_tiles(c);
   cudaStream_t st = c->cs;
   const int H = c->H, T2 = 2 * T, n2 = 2 * nseq;
   const size_t TH = (size_t)T * H, T2H = (size_t)T2 * H;
@@ -1278,7 +1301,7 @@ int stream_step_fwd_dpo(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t n
   {
     const long long n = (long long)T * (H / 8);
     TIMED(LS_K_OTHER, 0, (0.5625 + 2.0) * T * H, 1,
-          ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, st>>>(d_tokens, c->emb_p, c->emb_a, x0, T, H));
+          ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, st>>>(d_tokens, c->emb_p, c->emb_a, x0, T, H, c->V));
   }
   CK(cudaMemcpyAsync(x0 + TH, x0, TH * sizeof(bf16), cudaMemcpyDeviceToDevice, st));
   CK(cudaMemcpyAsync(c->acts, x0, TH * sizeof(bf16), cudaMemcpyDeviceToDevice, st));
@@ -1312,6 +1335,7 @@ int stream_step_fwd_dpo(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t n
     g.lda = H;
     g.Wp = img;
     g.force_bn = 256;
+    g.sk = gemm_ws(c);
     g.g.M = T2; g.g.Nw = n; g.g.Kw = H; g.g.Nout = n; g.g.Kred = H;
     g.g.absmax = reinterpret_cast<const float*>(img + c->vch_abs_off);
     g.g.epi = ls::EPI_LOGPROB;
@@ -1443,6 +1467,7 @@ int stream_step_bwd(ls_ctx* c, const float* d_coeffs) {
       g.lda = H;
       g.Wp = img;
       g.force_bn = 256;
+      g.sk = gemm_ws(c);
       g.g.M = T; g.g.Nw = n; g.g.Kw = H; g.g.Nout = n; g.g.Kred = H;
       g.g.absmax = wa;
       g.g.epi = ls::EPI_DLOGITS;
@@ -1452,7 +1477,7 @@ int stream_step_bwd(ls_ctx* c, const float* d_coeffs) {
       GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, n, H, 0), gemm_bytes(0, T, n, H, 2, false), ls::launch_nf4_gemm(g, st));
       const int epi = first_chunk ? ls::EPI_F32 : ls::EPI_F32_ACC;
       GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, n, H, 0), gemm_bytes(1, T, n, H, first_chunk ? 4 : 8, false),
-             gemm(ls::GEMM_DX, c->dlogits, n, T, img, wa, n, H, nullptr, nullptr, 0, epi, c->dhf, H, nullptr, 0, st));
+             gemm(ls::GEMM_DX, c->dlogits, n, T, img, wa, n, H, nullptr, nullptr, 0, epi, c->dhf, H, nullptr, 0, st, gemm_ws(c)));
       first_chunk = false;
       if (ch == 0) {
         const bf16* xL = c->acts + (size_t)c->L * (size_t)c->Tmax * H;
@@ -1678,7 +1703,38 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
   if (residual && epi != 0) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: residual only with bf16 output");
   KCK(gemm(mode, reinterpret_cast<const bf16*>(A), lda, M, wp, wa, N, K, reinterpret_cast<const bf16*>(ext_a),
            reinterpret_cast<const bf16*>(ext_b), ext_k, epi, out, ldo, reinterpret_cast<const bf16*>(residual), ldr,
-           STREAM(s), force_bn, force_nacc));
+           STREAM(s), ls::SkWorkspace{}, force_bn, force_nacc));
+  return LS_OK;
+}
+
+uint64_t lsk_nf4_gemm_workspace_bytes(void) { return ls::kSkWorkspaceBytes; }
+
+int lsk_nf4_gemm_sk(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const uint8_t* wp, const float* wa,
+                    int32_t N, int32_t K, const uint16_t* ext_a, const uint16_t* ext_b, int32_t ext_k, int32_t epi,
+                    void* out, int64_t ldo, const uint16_t* residual, int64_t ldr, int32_t force_bn,
+                    int32_t force_nacc, int32_t split, void* workspace, uint64_t workspace_bytes, void* s) {
+  if (split < -1 || split > 1) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: split must be -1, 0 or 1");
+  if (!workspace || workspace_bytes < ls::kSkWorkspaceBytes || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: workspace missing, smaller than "
+                                      "lsk_nf4_gemm_workspace_bytes() or not 256-byte aligned");
+  if (mode != 0 && mode != 1) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: mode must be 0 or 1");
+  if (!A || !wp || !wa || !out || M < 0 || N <= 0 || K <= 0 || K % 64 || N % 64)
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: null pointer or N, K not positive multiples of 64");
+  if (epi < 0 || epi > 2) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: epi must be 0, 1 or 2");
+  if (ext_k != 0 && ext_k != 16 && ext_k != 32)
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: ext_k must be 0, 16, 32");
+  if (ext_k && (!ext_a || !ext_b)) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: ext operands missing");
+  const int outc = mode == 0 ? N : K;
+  const int red = mode == 0 ? K : N;
+  if (lda < red || lda % 8 || ldo < outc || ldo % 8 || (residual && (ldr < outc || ldr % 8)))
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: leading dimensions too small or not multiples of 8");
+  if (force_bn != 0 && force_bn != 128 && force_bn != 256)
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: force_bn");
+  if (force_nacc < 0 || force_nacc > 2) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: force_nacc");
+  if (residual && epi != 0) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: residual only with bf16 output");
+  KCK(gemm(mode, reinterpret_cast<const bf16*>(A), lda, M, wp, wa, N, K, reinterpret_cast<const bf16*>(ext_a),
+           reinterpret_cast<const bf16*>(ext_b), ext_k, epi, out, ldo, reinterpret_cast<const bf16*>(residual), ldr,
+           STREAM(s), ls::sk_workspace_at(workspace), force_bn, force_nacc, split));
   return LS_OK;
 }
 
@@ -1882,12 +1938,14 @@ int lsk_build_ext_bwd(const uint16_t* aq, const uint16_t* av, int32_t r, int32_t
   return LS_OK;
 }
 
-int lsk_embed_gather(const int32_t* tokens, const uint8_t* packed, const float* absmax, uint16_t* x, int32_t T,
-                     int32_t H, void* s) {
-  if (!tokens || !packed || !absmax || !x || T < 0 || H % 64) return set_thread_err(LS_ERR_ARG, "lsk_embed_gather: bad args");
+int lsk_embed_gather(const int32_t* tokens, const uint8_t* packed, const float* absmax, int32_t V, uint16_t* x,
+                     int32_t T, int32_t H, void* s) {
+  if (!tokens || !packed || !absmax || !x || V < 1 || T < 0 || H % 64)
+    return set_thread_err(LS_ERR_ARG, "lsk_embed_gather: bad args");
   const long long n = (long long)T * (H / 8);
   if (n == 0) return LS_OK;
-  ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(tokens, packed, absmax, reinterpret_cast<bf16*>(x), T, H);
+  ls::embed_gather_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(tokens, packed, absmax, reinterpret_cast<bf16*>(x), T,
+                                                                 H, V);
   KLAUNCH();
   return LS_OK;
 }

@@ -13,7 +13,8 @@
 // (backward).  deq(w) = bf16_rne(fp32(q[code]) * absmax): one fp32 multiply and one
 // rounding, identical bit for bit to the host definition.
 //
-// Pipeline per CTA (one BM x BN output tile, BM = 128 x NACC):
+// Pipeline per CTA (BM x BN output tiles, BM = 128 x NACC, one after another as the
+// tile schedule GemmSched hands them out: whole tiles, or k-ranges of split tiles):
 //   warp 0      TMA producer: activation tile (SW128, K-major) + packed code tile,
 //               and the tile's absmax values by cp.async, into an S-deep ring.
 //   warps 2..9  dequantise codes into a SW128 bf16 tile, an SB-deep ring (one thread
@@ -65,7 +66,94 @@ struct GemmArgs {
   float* tgt_logit;                  // EPI_LOGPROB: [M] logit of the target
   const float* lse;                  // EPI_DLOGITS: [M]
   const float* coef;                 // EPI_DLOGITS: [M] dL/dlogprob per row
-  int n_fast;                        // grid.x walks output-column tiles (CTAs of a wave share A rows)
+  int n_fast;                        // tile order walks output-column tiles first (a wave shares A rows)
+  // Tile schedule (see GemmSched): tiles_m x tiles_n output tiles over sched_ctas CTAs.
+  int tiles_m, tiles_n;
+  int sched_ctas;                    // CTAs of the launch
+  int sched_dp;                      // whole tiles per CTA, tile j * sched_ctas + cta, taken first
+  long long sk_iters;                // k-iterations of the remaining tiles, split evenly over the CTAs
+  float* sk_ws;                      // split tiles: one fp32 partial slot (kSkSlotFloats) per CTA
+  unsigned* sk_flags;                // [sched_ctas][8]: epoch word per (CTA, epilogue warp)
+  unsigned sk_epoch;                 // this launch's nonzero epoch
+};
+
+// Stream-K workspace: one 256 x 256 fp32 partial tile per CTA, at most kSkMaxCtas CTAs.
+constexpr int kSkMaxCtas = 148;
+constexpr int kSkSlotFloats = 256 * 256;
+
+// Work of one CTA as a sequence of pieces (tile, k-iterations [k0, k1)).  First the
+// round-robin whole tiles j * G + c (j < sched_dp; with sched_ctas = tiles and
+// sched_dp = 1 this is one tile per CTA), then the CTA's contiguous share
+// [c I / G, (c+1) I / G) of the I = sk_iters iterations that the remaining tiles span in
+// (tile, k) order.  A share that starts inside a tile leaves a partial sum for the CTA
+// that holds the tile's k = 0 piece; that CTA adds the partials of the following CTAs
+// (the ones whose shares start inside the tile, in increasing order) before its
+// epilogue.  Every CTA's share is non-empty (I >= G, checked on the host), so each
+// split tile's partials come from the immediately following CTAs.
+// SPLIT = false compiles the one-tile-per-CTA form (tile = CTA index, all k) with no
+// trace of the split machinery.
+template <bool SPLIT>
+struct GemmSched {
+  int c, G, ndp, niter, tm, tn, nf, j;
+  long long I, pos, end;
+  __device__ __forceinline__ void init(const GemmArgs& g, int cta, int niter_) {
+    c = cta;
+    G = g.sched_ctas;
+    ndp = g.sched_dp;
+    niter = niter_;
+    tm = g.tiles_m;
+    tn = g.tiles_n;
+    nf = g.n_fast;
+    I = SPLIT ? g.sk_iters : 0;
+    j = 0;
+    pos = SPLIT ? start(c) : 0;
+    end = SPLIT ? start(c + 1) : 0;
+  }
+  __device__ __forceinline__ long long start(int d) const { return (long long)d * I / G; }
+  // next piece: tile id, k-iteration range; false when the CTA's work is done
+  __device__ __forceinline__ bool next(int& tile, int& k0, int& k1) {
+    if constexpr (!SPLIT) {
+      if (j) return false;
+      j = 1;
+      tile = c;
+      k0 = 0;
+      k1 = niter;
+      return true;
+    }
+    if (j < ndp) {
+      tile = j * G + c;
+      k0 = 0;
+      k1 = niter;
+      ++j;
+      return true;
+    }
+    if (pos < end) {
+      const long long t = pos / niter;
+      k0 = (int)(pos - t * niter);
+      const long long rem = end - pos;
+      k1 = rem < (long long)(niter - k0) ? k0 + (int)rem : niter;
+      tile = ndp * G + (int)t;
+      pos += k1 - k0;
+      return true;
+    }
+    return false;
+  }
+  __device__ __forceinline__ void tile_origin(int tile, int bm, int bn, int& m0, int& n0) const {
+    if (nf) {
+      n0 = (tile % tn) * bn;
+      m0 = (tile / tn) * bm;
+    } else {
+      m0 = (tile % tm) * bm;
+      n0 = (tile / tm) * bn;
+    }
+  }
+  // CTAs c+1 .. last whose shares start inside split tile `tile` (its k = 0 piece is c's)
+  __device__ __forceinline__ int last_peer(int tile) const {
+    const long long tend = (long long)(tile - ndp * G + 1) * niter;
+    int d = c + 1;
+    while (d + 1 < G && start(d + 1) < tend) ++d;
+    return d;
+  }
 };
 
 template <int NACC, int BN, int S, int SB>
@@ -90,7 +178,7 @@ struct GemmCfg {
   static constexpr int OFF_W = OFF_B + SB * B_BYTES;
   static constexpr int OFF_ABS = OFF_W + S * W_BYTES;
   static constexpr int OFF_BAR = OFF_ABS + S * ABS_PER_STAGE * 4;
-  static constexpr int NBAR = 2 * S + 2 * SB + 1;
+  static constexpr int NBAR = 2 * S + 2 * SB + 3;   // + accumulator full / drained, TMEM free
   static constexpr int OFF_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_SLOT + 16 + 1024;   // + slack to align the base to 1024
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
@@ -209,7 +297,7 @@ __device__ __forceinline__ void store_bf16_32(__nv_bfloat16* dst, const float (&
 
 // -------------------------------------------------------------------------- kernel
 
-template <int NACC, int BN, int S, int SB, int MODE>
+template <int NACC, int BN, int S, int SB, int MODE, bool SPLIT>
 __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX, const GemmArgs g) {
@@ -219,7 +307,6 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = (g.n_fast ? blockIdx.y : blockIdx.x) * C::BM, n0 = (g.n_fast ? blockIdx.x : blockIdx.y) * BN;
   const int KB = g.Kred / 64;
   const int KBw = g.Kw / 64;
   const int niter = KB + (g.ext_k > 0 ? 1 : 0);
@@ -229,7 +316,9 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
   auto empty = [&](int s) { return bar0 + (S + s) * 8; };
   auto bfull = [&](int s) { return bar0 + (2 * S + s) * 8; };
   auto bempty = [&](int s) { return bar0 + (2 * S + SB + s) * 8; };
-  const uint32_t accfull = bar0 + (2 * S + 2 * SB) * 8;
+  const uint32_t accfull = bar0 + (2 * S + 2 * SB) * 8;       // one phase per piece
+  const uint32_t tmemfree = bar0 + (2 * S + 2 * SB + 1) * 8;  // epilogue done reading TMEM
+  const uint32_t drained = bar0 + (2 * S + 2 * SB + 2) * 8;   // every MMA retired
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -241,6 +330,8 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
       mbar_init(bempty(s), 1);
     }
     mbar_init(accfull, 1);
+    mbar_init(tmemfree, C::NDQ_WARPS);
+    mbar_init(drained, 1);
     fence_barrier_init();
     s_abort = 0;
   }
@@ -258,122 +349,180 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
 
+  // Every role walks the same piece sequence; gi counts k-iterations across pieces and
+  // drives the ring stages and their phases.
+  GemmSched<SPLIT> sc;
+  sc.init(g, blockIdx.x, niter);
+  int tile, k0, k1;
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int issued = 0;
-    for (int it = 0; it < niter; ++it) {
-      const int s = it % S;
-      if (s_abort || !mbar_wait(empty(s), ((it / S) & 1) ^ 1)) { s_abort = 1; break; }
-      const uint32_t a_dst = sb + C::OFF_A + s * C::A_BYTES;
-      if (lane == 0) {
+    int gi = 0;
+    bool stop = false;
+    while (!stop && sc.next(tile, k0, k1)) {
+      int m0, n0;
+      sc.tile_origin(tile, C::BM, BN, m0, n0);
+      for (int it = k0; it < k1; ++it, ++gi) {
+        const int s = gi % S;
+        if (s_abort || !mbar_wait(empty(s), ((gi / S) & 1) ^ 1)) {
+          s_abort = 1;
+          stop = true;
+          break;
+        }
+        const uint32_t a_dst = sb + C::OFF_A + s * C::A_BYTES;
+        if (lane == 0) {
+          if (it < KB) {
+            mbar_arrive_expect_tx(full(s), C::A_BYTES + C::W_BYTES);
+            tma_load_2d(a_dst, &tmA, it * 64, m0, full(s));
+            const uint32_t w_dst = sb + C::OFF_W + s * C::W_BYTES;
+            if (MODE == GEMM_FWD) tma_load_2d(w_dst, &tmW, it * 32, n0, full(s));
+            else tma_load_2d(w_dst, &tmW, n0 / 2, it * 64, full(s));
+          } else {
+            mbar_arrive_expect_tx(full(s), C::A_BYTES);
+            tma_load_2d(a_dst, &tmX, 0, m0, full(s));
+          }
+        }
         if (it < KB) {
-          mbar_arrive_expect_tx(full(s), C::A_BYTES + C::W_BYTES);
-          tma_load_2d(a_dst, &tmA, it * 64, m0, full(s));
-          const uint32_t w_dst = sb + C::OFF_W + s * C::W_BYTES;
-          if (MODE == GEMM_FWD) tma_load_2d(w_dst, &tmW, it * 32, n0, full(s));
-          else tma_load_2d(w_dst, &tmW, n0 / 2, it * 64, full(s));
-        } else {
-          mbar_arrive_expect_tx(full(s), C::A_BYTES);
-          tma_load_2d(a_dst, &tmX, 0, m0, full(s));
-        }
-      }
-      if (it < KB) {
-        const uint32_t abs_dst = sb + C::OFF_ABS + s * C::ABS_PER_STAGE * 4;
-        if (MODE == GEMM_FWD) {
-          for (int j = lane; j < C::UNITS; j += 32) {
-            const int n = n0 + j;
-            const float* src = n < g.Nw ? g.absmax + (size_t)n * KBw + it : g_zero_word;
-            cp_async_4(abs_dst + j * 4, src);
-          }
-        } else {
-          constexpr int CB = C::UNITS / 64;
-          for (int e = lane; e < 64 * CB; e += 32) {
-            const int r = e / CB, c = e % CB;
-            const int kb = n0 / 64 + c;
-            const float* src = kb < KBw ? g.absmax + (size_t)(it * 64 + r) * KBw + kb : g_zero_word;
-            cp_async_4(abs_dst + e * 4, src);
+          const uint32_t abs_dst = sb + C::OFF_ABS + s * C::ABS_PER_STAGE * 4;
+          if (MODE == GEMM_FWD) {
+            for (int j = lane; j < C::UNITS; j += 32) {
+              const int n = n0 + j;
+              const float* src = n < g.Nw ? g.absmax + (size_t)n * KBw + it : g_zero_word;
+              cp_async_4(abs_dst + j * 4, src);
+            }
+          } else {
+            constexpr int CB = C::UNITS / 64;
+            for (int e = lane; e < 64 * CB; e += 32) {
+              const int r = e / CB, c = e % CB;
+              const int kb = n0 / 64 + c;
+              const float* src = kb < KBw ? g.absmax + (size_t)(it * 64 + r) * KBw + kb : g_zero_word;
+              cp_async_4(abs_dst + e * 4, src);
+            }
           }
         }
+        cp_async_mbar_arrive_noinc(full(s));
       }
-      cp_async_mbar_arrive_noinc(full(s));
-      ++issued;
     }
     if (s_abort) {
       // let copies already in flight land before the CTA's shared memory goes away
-      for (int j = issued - S < 0 ? 0 : issued - S; j < issued; ++j) mbar_wait(full(j % S), (j / S) & 1);
+      for (int j = gi - S < 0 ? 0 : gi - S; j < gi; ++j) mbar_wait(full(j % S), (j / S) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
-      for (int it = 0; it < niter; ++it) {
-        const int s = it % S, b = it % SB;
-        if (s_abort || !mbar_wait(full(s), (it / S) & 1) || !mbar_wait(bfull(b), (it / SB) & 1)) {
+      int gi = 0, pc = 0;
+      bool stop = false;
+      while (!stop && sc.next(tile, k0, k1)) {
+        // the epilogue of the previous piece has read TMEM out
+        if (pc > 0 && (s_abort || !mbar_wait(tmemfree, (pc - 1) & 1))) {
           s_abort = 1;
           break;
         }
-        tc_fence_after();
-        const int nk = it < KB ? 4 : g.ext_k / 16;
-        const uint32_t a_base = sb + C::OFF_A + s * C::A_BYTES;
-        const uint32_t b_base = sb + C::OFF_B + b * C::B_BYTES;
-        // the input-gradient main loop reads B MN-major (16 reduction rows = two 1 KB
-        // 8-row groups per instruction); the LoRA extra stage is K-major in both modes
-        const bool mn = MODE == GEMM_DX && it < KB;
-        const uint32_t idesc = mn ? IDESC | (1u << 16) : IDESC;
-        for (int k = 0; k < nk; ++k) {
-          const uint64_t bd = mn ? sw128_mnmajor_desc(b_base + k * 2048, 8192) : sw128_kmajor_desc(b_base + k * 32);
-#pragma unroll
-          for (int a = 0; a < NACC; ++a) {
-            const uint64_t ad = sw128_kmajor_desc(a_base + a * 16384 + k * 32);
-            tc_mma_bf16(tmem + a * BN, ad, bd, idesc, (it > 0 || k > 0) ? 1u : 0u);
+        for (int it = k0; it < k1; ++it, ++gi) {
+          const int s = gi % S, b = gi % SB;
+          if (s_abort || !mbar_wait(full(s), (gi / S) & 1) || !mbar_wait(bfull(b), (gi / SB) & 1)) {
+            s_abort = 1;
+            stop = true;
+            break;
           }
+          tc_fence_after();
+          const int nk = it < KB ? 4 : g.ext_k / 16;
+          const uint32_t a_base = sb + C::OFF_A + s * C::A_BYTES;
+          const uint32_t b_base = sb + C::OFF_B + b * C::B_BYTES;
+          // the input-gradient main loop reads B MN-major (16 reduction rows = two 1 KB
+          // 8-row groups per instruction); the LoRA extra stage is K-major in both modes
+          const bool mn = MODE == GEMM_DX && it < KB;
+          const uint32_t idesc = mn ? IDESC | (1u << 16) : IDESC;
+          for (int k = 0; k < nk; ++k) {
+            const uint64_t bd = mn ? sw128_mnmajor_desc(b_base + k * 2048, 8192) : sw128_kmajor_desc(b_base + k * 32);
+#pragma unroll
+            for (int a = 0; a < NACC; ++a) {
+              const uint64_t ad = sw128_kmajor_desc(a_base + a * 16384 + k * 32);
+              tc_mma_bf16(tmem + a * BN, ad, bd, idesc, (it > k0 || k > 0) ? 1u : 0u);
+            }
+          }
+          tc_commit(empty(s));
+          tc_commit(bempty(b));
         }
-        tc_commit(empty(s));
-        tc_commit(bempty(b));
+        if (stop) break;
+        tc_commit(accfull);
+        ++pc;
       }
-      tc_commit(accfull);
-      mbar_wait(accfull, 0);   // every MMA has retired before TMEM is released
+      tc_commit(drained);
+      mbar_wait(drained, 0);   // every MMA has retired before TMEM is released
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ dequant warps
     const int tq = threadIdx.x - 64;
-    // group grp takes k-steps it = grp, grp + FWD_GROUPS, ...; its threads one unit each
+    // group grp takes the k-iterations gi = grp (mod FWD_GROUPS); its threads one unit each
     const int grp = tq / C::UNITS;
     const int step = C::FWD_GROUPS;
     const int tg = tq - grp * C::UNITS;
-    for (int it = grp; it < niter; it += step) {
-      const int s = it % S, b = it % SB;
-      if (s_abort || !mbar_wait(full(s), (it / S) & 1) || !mbar_wait(bempty(b), ((it / SB) & 1) ^ 1)) {
+    const int ew = warp - 2;   // epilogue warp: TMEM lane quarter wq, column half `half`
+    const int wq = warp & 3;
+    const int half = ew >> 2;
+    int gi = 0, pc = 0;
+    while (sc.next(tile, k0, k1)) {
+      int m0, n0;
+      sc.tile_origin(tile, C::BM, BN, m0, n0);
+      const int n = k1 - k0;
+      bool stop = false;
+      for (int gj = gi + ((grp - gi % step) + step) % step; gj < gi + n; gj += step) {
+        const int it = k0 + (gj - gi);
+        const int s = gj % S, b = gj % SB;
+        if (s_abort || !mbar_wait(full(s), (gj / S) & 1) || !mbar_wait(bempty(b), ((gj / SB) & 1) ^ 1)) {
+          s_abort = 1;
+          stop = true;
+          break;
+        }
+        uint8_t* Bt = smem + C::OFF_B + b * C::B_BYTES;
+        if (it < KB) {
+          const uint8_t* Wt = smem + C::OFF_W + s * C::W_BYTES;
+          const float* absS = reinterpret_cast<const float*>(smem + C::OFF_ABS + s * C::ABS_PER_STAGE * 4);
+          if (MODE == GEMM_FWD) dequant_fwd_unit(Wt, absS, Bt, tg, 0);
+          else dequant_dx_unit(Wt, absS, Bt, tg, C::W_BYTES / 64, 0);
+        } else {
+          copy_ext_rows(g.ext_b, n0, g.Nout, Bt, 0, C::UNITS, tg, C::UNITS);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bfull(b));
+      }
+      gi += n;
+      if (stop || s_abort || !mbar_wait(accfull, pc & 1)) {
         s_abort = 1;
         break;
       }
-      uint8_t* Bt = smem + C::OFF_B + b * C::B_BYTES;
-      if (it < KB) {
-        const uint8_t* Wt = smem + C::OFF_W + s * C::W_BYTES;
-        const float* absS = reinterpret_cast<const float*>(smem + C::OFF_ABS + s * C::ABS_PER_STAGE * 4);
-        if (MODE == GEMM_FWD) dequant_fwd_unit(Wt, absS, Bt, tg, 0);
-        else dequant_dx_unit(Wt, absS, Bt, tg, C::W_BYTES / 64, 0);
-      } else {
-        copy_ext_rows(g.ext_b, n0, g.Nout, Bt, 0, C::UNITS, tg, C::UNITS);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bfull(b));
-    }
-
-    // ------------------------------------------------------------ epilogue
-    if (!s_abort && mbar_wait(accfull, 0)) {
       tc_fence_after();
-      const int wq = warp & 3;
-      const int half = (warp - 2) >> 2;
+
+      // ---------------------------------------------------------- epilogue of the piece
+      // partial: the share started inside the tile -> fp32 partial to this CTA's slot;
+      // finish: the tile's k = 0 piece of a split tile -> add the following CTAs' partials.
+      // The same (warp, lane) writes and reads each partial element, so a per-warp
+      // epoch flag orders them.
+      const bool partial = SPLIT && k0 > 0;
+      const bool finish = SPLIT && k0 == 0 && k1 < niter;
+      const int dlast = finish ? sc.last_peer(tile) : 0;
+      if (finish) {
+        bool ok = true;
+        if (lane == 0)
+          for (int d = sc.c + 1; d <= dlast && ok; ++d) ok = flag_wait_eq(g.sk_flags + d * 8 + ew, g.sk_epoch);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        __syncwarp();   // the other lanes' partial loads follow lane 0's acquire
+        if (!ok) {
+          s_abort = 1;
+          break;
+        }
+      }
       for (int a = 0; a < NACC; ++a) {
         const int row = m0 + a * 128 + wq * 32 + lane;
         const bool rok = row < g.M;
         float run_m = -INFINITY, run_s = 0.f;
         int tgt = -1;
         float lse_r = 0.f, coef_r = 0.f;
-        if (g.epi == EPI_LOGPROB || g.epi == EPI_DLOGITS) {
+        if (!partial && (g.epi == EPI_LOGPROB || g.epi == EPI_DLOGITS)) {
           tgt = rok ? g.targets[row] - g.vocab_off : -1;
           if (g.epi == EPI_DLOGITS && rok) {
             lse_r = g.lse[row];
@@ -385,12 +534,36 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * BN + c0), v);
           tmem_ld_wait();
+          // partial-slot position of this thread's 32 values: chunk (a, wq, c0 / 32),
+          // 8 float4 groups of 32 lanes
+          const size_t chunk = ((size_t)(a * 4 + wq) * (BN / 32) + c0 / 32) * 1024 + (size_t)lane * 4;
+          if (partial) {
+            float4* dst = reinterpret_cast<float4*>(g.sk_ws + (size_t)sc.c * kSkSlotFloats + chunk);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              __stcg(dst + q * 32, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+            continue;
+          }
           const int gc = n0 + c0;
           const int nvalid = min(32, g.Nout - gc);
           if (!rok || nvalid <= 0) continue;
           float f[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          if (finish) {
+            for (int d = sc.c + 1; d <= dlast; ++d) {
+              const float4* srcp = reinterpret_cast<const float4*>(g.sk_ws + (size_t)d * kSkSlotFloats + chunk);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float4 p4 = __ldcg(srcp + q * 32);
+                f[4 * q] += p4.x;
+                f[4 * q + 1] += p4.y;
+                f[4 * q + 2] += p4.z;
+                f[4 * q + 3] += p4.w;
+              }
+            }
+          }
           if (g.epi == EPI_BF16) {
             if (g.residual) {
               const __nv_bfloat16* rp = g.residual + (size_t)row * g.ldr + gc;
@@ -460,12 +633,24 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
             store_bf16_32(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
           }
         }
-        if (g.epi == EPI_LOGPROB && rok && n0 + half * (BN / 2) < g.Nout) {
+        if (!partial && g.epi == EPI_LOGPROB && rok && n0 + half * (BN / 2) < g.Nout) {
           const int p = (g.vocab_off + n0 + half * (BN / 2)) / (BN / 2);
           g.part_max[(size_t)row * g.part_ld + p] = run_m;
           g.part_sum[(size_t)row * g.part_ld + p] = run_s;
         }
       }
+      if (partial) {
+        // publish this warp's part of the partial tile
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          st_release_gpu(g.sk_flags + sc.c * 8 + ew, g.sk_epoch);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmemfree);
+      ++pc;
     }
   }
 

@@ -192,15 +192,22 @@ __global__ void swiglu_bwd_kernel(const float* __restrict__ dh, const __nv_bfloa
 // ------------------------------------------------------------------ embedding
 // x[t] = dequant(row tokens[t] of the NF4 embedding); packed/absmax may live in
 // mapped pinned host memory (only the T selected rows cross the host link).
+// A token id outside [0, V) gives a zero row and raises the device error word (the
+// table may be mapped host memory: an unchecked id would read outside the mapping).
 __global__ void embed_gather_kernel(const int* __restrict__ tokens, const uint8_t* __restrict__ packed,
                                     const float* __restrict__ absmax, __nv_bfloat16* __restrict__ x, int T,
-                                    int H) {
+                                    int H, int V) {
   const int nch = H >> 3;   // 8-element chunks per row
   const long long total = (long long)T * nch;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     const int t = (int)(idx / nch), c = (int)(idx % nch);
     const long long tok = tokens[t];
+    if (tok < 0 || tok >= V) {
+      if (c == 0) raise_error(DEV_BAD_ARG);
+      reinterpret_cast<uint4*>(x + (size_t)t * H)[c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
     const uint32_t w = *reinterpret_cast<const uint32_t*>(packed + tok * (H >> 1) + c * 4);
     const float a = absmax[tok * (H >> 6) + (c >> 3)];
     uint32_t o[4];
@@ -242,7 +249,7 @@ __global__ void seq_setup_kernel(const int* __restrict__ tokens, const int* __re
   while (s + 1 < nseq && cu[s + 1] <= t) ++s;
   const int a = cu[s], b = cu[s + 1];
   if (pos) pos[t] = t - a;
-  if (tgt) tgt[t] = (t + 1 < b) ? tokens[t + 1] : -1;
+  if (tgt) tgt[t] = (t + 1 < b && t + 1 < T) ? tokens[t + 1] : -1;
   if (coef) coef[t] = (seq_coef && mask && mask[t] && t + 1 < b) ? seq_coef[s] : 0.f;
 }
 

@@ -8,7 +8,9 @@ host-to-device copy), as the layer-streaming design on the Soup pages prescribes
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
+import functools
 import os
 from concurrent.futures import ThreadPoolExecutor
 from typing import Dict, List, Optional
@@ -20,6 +22,15 @@ from ._binding import (LSError, call, check, last_error, lib, ls_config, ls_laye
                        ls_vocab_host)
 
 MATS = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+def _stream_ordered(fn):
+    """Run a Stack method's library calls in stream order with the caller (Stack._ordered)."""
+    @functools.wraps(fn)
+    def wrapper(self, *args, **kwargs):
+        with self._ordered():
+            return fn(self, *args, **kwargs)
+    return wrapper
 
 
 def make_config(s, max_tokens: int = 0, max_seqs: int = 0, max_seq_len: int = 0, resident: bool = False,
@@ -104,6 +115,24 @@ class Stack:
         self._keep = []
 
     # ------------------------------------------------------------------ loading
+    @contextlib.contextmanager
+    def _ordered(self):
+        """The library runs on the stack's own compute stream while callers make and free
+        tensors on their current stream.  Join the two around every call that queues device
+        work: the compute stream first waits for what the caller queued (uploads of the
+        tokens, offsets and mask, adapter factors), and the caller's stream then waits for
+        the stack's work, so its outputs are ready there and the caching allocator cannot
+        hand a tensor the library still reads or writes to a new owner."""
+        cur = torch.cuda.current_stream(self.dev)
+        if cur == self.compute:
+            yield
+            return
+        self.compute.wait_stream(cur)
+        try:
+            yield
+        finally:
+            cur.wait_stream(self.compute)
+
     def _shape(self, name):
         s = self.s
         H, I, nq, nkv = s.hidden, s.inter, s.heads * s.head_dim, s.kv_heads * s.head_dim
@@ -216,6 +245,7 @@ class Stack:
             self.images = [None] * self.s.layers
 
     # ------------------------------------------------------------------ adapters
+    @_stream_ordered
     def set_adapter(self, layer: int, aq, bq, av, bv):
         """Bind bf16 device LoRA factors (A [r,H], B [N,r]); fp32 grads are allocated here."""
         d = {"aq": aq, "bq": bq, "av": av, "bv": bv}
@@ -235,6 +265,7 @@ class Stack:
             t = [torch.from_numpy(x).to(torch.bfloat16).to(self.dev) for x in (aq, bq, av, bv)]
             self.set_adapter(l, *t)
 
+    @_stream_ordered
     def export_adapter(self, path: str):
         """Write the bound LoRA factors with canonical keys (see adapters.py)."""
         from .adapters import save_adapter
@@ -252,6 +283,7 @@ class Stack:
                  for k in ("aq", "bq", "av", "bv")]
             self.set_adapter(l, *t)
 
+    @_stream_ordered
     def init_optimizer(self, lr: float = 1e-4, betas=(0.9, 0.999), eps: float = 1e-8, weight_decay: float = 0.0):
         """AdamW state for the bound adapters: fp32 master (from the bf16 factors) and moments."""
         n = self.grad_numel()
@@ -261,6 +293,7 @@ class Stack:
                     "step": 0, "lr": lr, "betas": betas, "eps": eps, "wd": weight_decay}
         check(lib().lora_params(self.ctx, self.opt["master"].data_ptr()), self.ctx)
 
+    @_stream_ordered
     def optimizer_step(self, zero_grads: bool = True):
         """One AdamW step on every bound adapter from its accumulated gradient."""
         o = self.opt
@@ -280,6 +313,7 @@ class Stack:
         m = torch.from_numpy(np.ascontiguousarray(mask, np.uint8)).to(self.dev)
         return t, c, m
 
+    @_stream_ordered
     def fwd(self, tok, cu, mask, adapter_on: bool = True, save: bool = True, sums: Optional[torch.Tensor] = None):
         nseq = cu.numel() - 1
         self._last_rows = tok.numel()
@@ -289,6 +323,7 @@ class Stack:
                                     int(adapter_on), int(save), sums.data_ptr()), self.ctx)
         return sums
 
+    @_stream_ordered
     def logprobs(self, T: int = 0):
         """Per-token logprobs and log-sum-exp of the last forward (2T rows after a
         shared-read DPO forward: policy, then reference)."""
@@ -298,21 +333,25 @@ class Stack:
         check(lib().seq_logprobs(self.ctx, lp.data_ptr(), lse.data_ptr()), self.ctx)
         return lp, lse
 
+    @_stream_ordered
     def activation(self, layer: int, T: int) -> torch.Tensor:
         """Entry `layer` (0..L) of the activation store of the last saved forward, bf16 [T, H]."""
         out = torch.empty((T, self.s.hidden), dtype=torch.bfloat16, device=self.dev)
         check(lib().ls_read_activation(self.ctx, layer, out.data_ptr()), self.ctx)
         return out
 
+    @_stream_ordered
     def bwd(self, coeffs: torch.Tensor):
         check(lib().stream_step_bwd(self.ctx, coeffs.data_ptr()), self.ctx)
 
+    @_stream_ordered
     def fwd_dpo(self, tok, cu, mask, pi: torch.Tensor, ref: torch.Tensor):
         """Policy and reference forward in one sweep (needs a shared-read context)."""
         check(lib().stream_step_fwd_dpo(self.ctx, tok.data_ptr(), tok.numel(), cu.numel() - 1, cu.data_ptr(),
                                         mask.data_ptr(), pi.data_ptr(), ref.data_ptr()), self.ctx)
         self._last_rows = 2 * tok.numel()
 
+    @_stream_ordered
     def dpo_step(self, tok, cu, mask, beta: float, out: Optional[Dict] = None) -> Dict:
         """Policy pass (adapter on, store kept) and reference pass (adapter off) -- one
         shared sweep of the layers, or two -- then the DPO loss and the backward."""
@@ -332,6 +371,7 @@ class Stack:
         self.bwd(o["coeffs"])
         return o
 
+    @_stream_ordered
     def pref_step(self, method: str, tok, cu, mask, out: Optional[Dict] = None) -> Dict:
         """One preference-optimisation step on (chosen, rejected) pairs: "dpo", "kto"
         (policy and reference forward), "simpo" or "orpo" (policy forward only), then the
@@ -367,6 +407,7 @@ class Stack:
         self.bwd(o["coeffs"])
         return o
 
+    @_stream_ordered
     def sft_step(self, tok, cu, mask, count: float, out: Optional[Dict] = None) -> Dict:
         nseq = cu.numel() - 1
         o = out if out is not None else {
@@ -379,6 +420,7 @@ class Stack:
         self.bwd(o["coeffs"])
         return o
 
+    @_stream_ordered
     def train_step(self, h_tokens: torch.Tensor, h_cu: torch.Tensor, h_mask: torch.Tensor, method: str,
                    beta: float = 0.1, h_loss: Optional[torch.Tensor] = None, grads_out: Optional[torch.Tensor] = None,
                    dev_bufs: Optional[Dict] = None) -> torch.Tensor:
@@ -420,11 +462,13 @@ class Stack:
         self.compute.synchronize()
         return h_loss
 
+    @_stream_ordered
     def grads(self, zero_after: bool = False) -> torch.Tensor:
         flat = torch.empty(self.grad_numel(), dtype=torch.float32, device=self.dev)
         check(lib().lora_grads(self.ctx, flat.data_ptr(), int(zero_after)), self.ctx)
         return flat
 
+    @_stream_ordered
     def zero_grads(self):
         check(lib().lora_grads(self.ctx, None, 1), self.ctx)
 

@@ -86,3 +86,8 @@ def test_rope_table_matches_fp64():
     ang = np.arange(maxp)[:, None] * theta ** (-2.0 * np.arange(hd // 2) / hd)[None, :]
     np.testing.assert_array_equal(c, np.cos(ang).astype(np.float32))
     np.testing.assert_array_equal(s, np.sin(ang).astype(np.float32))
+
+
+def test_gemm_split_workspace_size():
+    """Epoch words (8 KiB) plus one 256 x 256 fp32 partial tile for each of 148 CTAs."""
+    assert int(L.lib().lsk_nf4_gemm_workspace_bytes()) == 8192 + 148 * 256 * 256 * 4

@@ -4,6 +4,7 @@ Tolerances: NF4 dequantisation bit-exact; matrix products and layer pieces
 normwise relative error <= 1e-2 (max|gpu - oracle| / max|oracle|); logprobs
 absolute error <= 2e-2.
 """
+import ctypes
 import math
 
 import numpy as np
@@ -153,6 +154,34 @@ def test_lora_linear_single_shape_fwd_bwd():
     k("lsk_nf4_gemm", 0, xd, Kd, T, p, am, Nd, Kd, None, None, 0, 0, yb, Nd, None, 0, 0, 0)
     torch.cuda.synchronize()
     assert torch.equal(y0, yb)
+
+
+# ------------------------------------------------------------------ embedding gather
+
+def test_embed_gather_rows_and_out_of_range_ids():
+    """Rows of the NF4 embedding bit-exact against the oracle's dequantisation; ids V and
+    -1 give zero rows and set the device error word (checked before any access with the
+    id), and the context stays usable."""
+    V, H = 300, 256
+    w = _w(V, H, seed=41)
+    p, a, _, _ = nf4_dev(w)
+    wd = _oracle_deq(w)
+    ids = np.array([0, 299, 7, 300, -1, 150], np.int32)
+    tok = torch.from_numpy(ids).to(DEV)
+    x = torch.full((len(ids), H), 1.0, dtype=torch.bfloat16, device=DEV)
+    e = ctypes.c_int32(0)
+    assert L.lib().lsk_device_error(ctypes.byref(e), 1) == 0
+    k("lsk_embed_gather", tok, p, a, V, x, len(ids), H)
+    torch.cuda.synchronize()
+    got = x.float().cpu().numpy()
+    for i in (0, 1, 2, 5):
+        np.testing.assert_array_equal(got[i], wd[ids[i]])
+    assert not got[3].any() and not got[4].any()
+    assert L.lib().lsk_device_error(ctypes.byref(e), 1) == 0
+    assert e.value == 2   # bad argument seen by a kernel
+    k("lsk_embed_gather", tok[:3], p, a, V, x, 3, H)
+    torch.cuda.synchronize()
+    assert L.lib().lsk_device_error(ctypes.byref(e), 1) == 0 and e.value == 0
 
 
 # ------------------------------------------------------------------ norms, rope, swiglu

@@ -218,7 +218,13 @@ def test_streamed_equals_resident_bit_exact(vrows):
                                                                nseq=2, prompt_len=256)], ids=["tiny", "8b-width"])
 def test_shared_read_dpo_equals_two_passes(cfg):
     """Policy and reference forward in one sweep of the streamed layers give the same
-    sums, loss and gradients as two separate sweeps, with 2 instead of 3 layer reads."""
+    sums, loss and gradients as two separate sweeps, with 2 instead of 3 layer reads.
+
+    The one-sweep products have twice the rows, so the NF4 GEMM's split-tile schedule
+    (which k-ranges of a tile different SMs sum, and where their fp32 partials meet)
+    differs between the two forms.  Each form is deterministic and within the oracle
+    tolerances of the exact values, so the two agree to twice those tolerances (two
+    independent roundings through bf16 activations)."""
     tok, cu, mask = _batch(cfg)
     two = _stack(cfg, dpo_shared_read=False)
     one = L.Stack(cfg, device="cuda:0", dpo_shared_read=True)
@@ -236,10 +242,12 @@ def test_shared_read_dpo_equals_two_passes(cfg):
     (o2, g2, lp2), (o1, g1, lp1) = res["two"], res["one"]
     T = len(tok)
     # reference-pass logprobs: the two-pass form leaves them as its last forward
-    assert torch.equal(lp1[T:], lp2)
-    for k in ("pi", "ref", "loss", "coeffs"):
-        assert torch.equal(o1[k], o2[k]), k
-    assert torch.equal(g1, g2)
+    assert (lp1[T:] - lp2).abs().max().item() <= 2 * TOL_LP
+    for k in ("pi", "ref"):
+        assert rel_err(to_np(o1[k]), to_np(o2[k])) <= 2 * TOL_LOSS, k
+    assert abs(float(o1["loss"]) - float(o2["loss"])) <= 2 * TOL_LOSS * max(1.0, abs(float(o2["loss"])))
+    assert rel_err(to_np(o1["coeffs"]), to_np(o2["coeffs"])) <= 2 * TOL_GRAD
+    assert rel_err(to_np(g1), to_np(g2)) <= 2 * TOL_GRAD
     assert reads["two"] >= 3 * cfg.layers - 2 and reads["one"] <= 2 * cfg.layers
 
 
