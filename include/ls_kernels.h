@@ -56,6 +56,20 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
  *         once corrupt each other's partials.
  * Other arguments and errors as lsk_nf4_gemm. */
 uint64_t lsk_nf4_gemm_workspace_bytes(void);
+
+/* The tile shape and schedule lsk_nf4_gemm_sk (and the stack) would launch for a product
+ * (host only: no device work, no GPU needed).  Arguments as lsk_nf4_gemm_sk, plus
+ * with_workspace (0: no split scratch, whole tiles only) and sms (SMs to plan for;
+ * 0 = the current device's, at most 148).  Output tiles are (128 nacc) x bn;
+ * ctas = CTAs launched; each first takes whole_per_cta whole tiles round-robin, then an
+ * even share of split_iters k-iterations of the remaining tiles (0: none); k_iters =
+ * k-iterations of one tile (reduction / 64, + 1 with the LoRA stage). */
+typedef struct lsk_gemm_plan {
+  int32_t nacc, bn, tiles_m, tiles_n, ctas, whole_per_cta, k_iters, reserved;
+  int64_t split_iters;
+} lsk_gemm_plan;
+int lsk_nf4_gemm_plan(int32_t mode, int32_t M, int32_t N, int32_t K, int32_t ext_k, int32_t split,
+                      int32_t with_workspace, int32_t force_bn, int32_t force_nacc, int32_t sms, lsk_gemm_plan* out);
 int lsk_nf4_gemm_sk(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const uint8_t* w_packed,
                     const float* w_absmax, int32_t N, int32_t K, const uint16_t* ext_a, const uint16_t* ext_b,
                     int32_t ext_k, int32_t epi, void* out, int64_t ldo, const uint16_t* residual, int64_t ldr,

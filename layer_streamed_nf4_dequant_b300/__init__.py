@@ -8,10 +8,10 @@ or without a CUDA device raises.
 """
 from ._binding import (LSError, LS_OK, LS_ERR_ARG, LS_ERR_CAP, LS_ERR_CUDA, LS_ERR_TIMEOUT, LS_ERR_STATE,
                        LS_ERR_DEVICE, ls_config, ls_layer_host, ls_nf4_host, ls_profile_t, ls_stats_t, ls_vocab_host, lib, call,
-                       check, last_error, header_functions, LIB_PATH)
-from .runtime import (Stack, make_config, plan_bytes, quantize_host, layer_layout)
+                       check, last_error, header_functions, LIB_PATH, lsk_gemm_plan)
+from .runtime import (Stack, make_config, plan_bytes, quantize_host, layer_layout, gemm_plan)
 
 __all__ = ["LSError", "ls_config", "ls_layer_host", "ls_nf4_host", "ls_profile_t", "ls_stats_t", "ls_vocab_host", "lib", "call",
            "check", "last_error", "header_functions", "Stack", "make_config", "plan_bytes", "quantize_host",
            "layer_layout", "LIB_PATH", "LS_OK", "LS_ERR_ARG", "LS_ERR_CAP", "LS_ERR_CUDA", "LS_ERR_TIMEOUT",
-           "LS_ERR_STATE", "LS_ERR_DEVICE"]
+           "LS_ERR_STATE", "LS_ERR_DEVICE", "lsk_gemm_plan", "gemm_plan"]

@@ -91,8 +91,18 @@ struct GemmCall {
   GemmArgs g;
 };
 
+// Tile shape and schedule of one product, decided on the host (plan_tile, plan_schedule).
+struct GemmPlan {
+  int nacc = 0, bn = 0;          // accumulators (tile rows / 128) and tile columns
+  bool split = false;            // split schedule wanted (only with NACC = 2 and scratch)
+  int tiles_m = 0, tiles_n = 0;  // output tile grid
+  int ctas = 0;                  // CTAs launched
+  int whole_per_cta = 1;         // round-robin whole tiles per CTA
+  long long split_iters = 0;     // k-iterations split evenly over the CTAs (0: none)
+};
+
 template <int NACC, int BN, int S, int SB, int MODE>
-static cudaError_t launch_cfg(const GemmCall& c, bool split, cudaStream_t st) {
+static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t st) {
   using C = GemmCfg<NACC, BN, S, SB>;
   // split schedules only for the one-CTA-per-SM (NACC = 2) tiles
   constexpr bool kCanSplit = NACC == 2;
@@ -133,40 +143,23 @@ static cudaError_t launch_cfg(const GemmCall& c, bool split, cudaStream_t st) {
   // N-fastest order lets a wave share activation tiles instead.
   GemmArgs ga = g;
   ga.n_fast = (double)g.M * g.Kred * 2.0 > (double)g.Nw * g.Kw * 0.5625;
-  const long long tm = (g.M + C::BM - 1) / C::BM, tn = (g.Nout + BN - 1) / BN, nt = tm * tn;
-  const int niter = g.Kred / 64 + (g.ext_k > 0 ? 1 : 0);
-  ga.tiles_m = (int)tm;
-  ga.tiles_n = (int)tn;
+  const long long nt = (long long)p.tiles_m * p.tiles_n;
+  ga.tiles_m = p.tiles_m;
+  ga.tiles_n = p.tiles_n;
+  ga.sched_ctas = p.ctas;
+  ga.sched_dp = p.whole_per_cta;
   ga.sk_iters = 0;
   ga.sk_ws = nullptr;
   ga.sk_flags = nullptr;
   ga.sk_epoch = 0;
-  // whole tiles, one per CTA
-  ga.sched_ctas = (int)nt;
-  ga.sched_dp = 1;
-  if (split && kCanSplit && c.sk.ws && c.sk.flags) {
-    // one CTA per SM: full rounds of whole tiles, then the last one to two rounds' worth
-    // of tiles split evenly by k-iterations (each CTA at least 4 of them)
-    const int gmax = sk_max_ctas();
-    const long long full = nt / gmax;
-    if (nt % gmax == 0) {
-      ga.sched_ctas = gmax;
-      ga.sched_dp = (int)full;
-    } else {
-      const long long dp = full > 0 ? full - 1 : 0;
-      const long long iters = (nt - dp * gmax) * niter;
-      long long G = gmax;
-      if (dp == 0 && iters / 4 < G) G = iters / 4 > 0 ? iters / 4 : 1;
-      if (G > 1) {
-        ga.sched_ctas = (int)G;
-        ga.sched_dp = (int)dp;
-        ga.sk_iters = iters;
-        ga.sk_ws = c.sk.ws;
-        ga.sk_flags = c.sk.flags;
-        ga.sk_epoch = next_sk_epoch();
-      }
-    }
+  if (p.split_iters > 0) {
+    if (!kCanSplit || !c.sk.ws || !c.sk.flags) return cudaErrorInvalidValue;
+    ga.sk_iters = p.split_iters;
+    ga.sk_ws = c.sk.ws;
+    ga.sk_flags = c.sk.flags;
+    ga.sk_epoch = next_sk_epoch();
   }
+  if (!kCanSplit && (ga.sched_dp != 1 || ga.sched_ctas != nt)) return cudaErrorInvalidValue;
   if (ga.sk_iters == 0) {
     if (ga.sched_dp == 1 && ga.sched_ctas == nt)
       kern_whole<<<(unsigned)nt, C::THREADS, C::SMEM, st>>>(tA, tW, tX, ga);
@@ -227,37 +220,79 @@ static double choose_tile(int mode, int M, int Nout, int& nacc, int& bn) {
 
 // With stream-K scratch the 256 x 256 tile can also run as a split schedule: every SM
 // gets the same number of k-iterations, so the estimate is tiles / SMs tile times (plus
-// the partial-tile exchange) instead of whole waves.
-static cudaError_t launch_nf4_gemm(const GemmCall& c, cudaStream_t st) {
-  const GemmArgs& g = c.g;
-  int nacc = 0, bn = 0;
-  const double t_whole = choose_tile(c.mode, g.M, g.Nout, nacc, bn);
-  bool split = false;
-  if (c.sk.ws && c.split >= 0 && g.M > 128) {
-    const double nt = (double)((g.M + 255) / 256) * (double)((g.Nout + 255) / 256);
+// the partial-tile exchange) instead of whole waves.  split_pref: 0 = estimate,
+// 1 = split whenever possible, -1 = whole tiles.
+static void plan_tile(int mode, int M, int Nout, int Kred, int ext_k, bool has_ws, int split_pref, int force_bn,
+                      int force_nacc, int sms, GemmPlan& p) {
+  const double t_whole = choose_tile(mode, M, Nout, p.nacc, p.bn);
+  p.split = false;
+  if (has_ws && split_pref >= 0 && M > 128) {
+    const double nt = (double)((M + 255) / 256) * (double)((Nout + 255) / 256);
     // the split kernel's k-iteration costs 1.09 x the whole-tile kernel's (measured on
     // the 8B product shapes), plus about 12 k-iterations per CTA for the partial-tile
     // exchange and the extra pipeline fill
-    const int niter = g.Kred / 64 + (g.ext_k > 0 ? 1 : 0);
-    const double t_split = 1.09 * nt / sk_max_ctas() + 12.0 / niter;
-    if (c.split > 0 || t_split < t_whole) {
-      split = true;
-      nacc = 2;
-      bn = 256;
+    const int niter = Kred / 64 + (ext_k > 0 ? 1 : 0);
+    const double t_split = 1.09 * nt / sms + 12.0 / niter;
+    if (split_pref > 0 || t_split < t_whole) {
+      p.split = true;
+      p.nacc = 2;
+      p.bn = 256;
     }
   }
-  if (c.force_bn) bn = c.force_bn;
-  if (c.force_nacc) nacc = c.force_nacc;
+  if (force_bn) p.bn = force_bn;
+  if (force_nacc) p.nacc = force_nacc;
+  if (p.nacc != 2) p.split = false;   // split schedules use one CTA per SM
+}
+
+// Whole tiles, one per CTA; or, for a split plan, one CTA per SM (at most `sms`): full
+// rounds of whole tiles, then the last one to two rounds' worth of tiles split evenly by
+// k-iterations (each CTA at least 4 of them).
+static void plan_schedule(int M, int Nout, int Kred, int ext_k, int sms, GemmPlan& p) {
+  const long long tm = (M + 128 * p.nacc - 1) / (128 * p.nacc), tn = (Nout + p.bn - 1) / p.bn, nt = tm * tn;
+  const int niter = Kred / 64 + (ext_k > 0 ? 1 : 0);
+  p.tiles_m = (int)tm;
+  p.tiles_n = (int)tn;
+  p.ctas = (int)nt;
+  p.whole_per_cta = 1;
+  p.split_iters = 0;
+  if (!p.split) return;
+  const long long full = nt / sms;
+  if (nt % sms == 0) {
+    p.ctas = sms;
+    p.whole_per_cta = (int)full;
+    return;
+  }
+  const long long dp = full > 0 ? full - 1 : 0;
+  const long long iters = (nt - dp * sms) * niter;
+  long long G = sms;
+  if (dp == 0 && iters / 4 < G) G = iters / 4 > 0 ? iters / 4 : 1;
+  if (G > 1) {
+    p.ctas = (int)G;
+    p.whole_per_cta = (int)dp;
+    p.split_iters = iters;
+  }
+}
+
+static GemmPlan plan_gemm(const GemmCall& c, int sms) {
+  const GemmArgs& g = c.g;
+  GemmPlan p;
+  plan_tile(c.mode, g.M, g.Nout, g.Kred, g.ext_k, c.sk.ws && c.sk.flags, c.split, c.force_bn, c.force_nacc, sms, p);
+  plan_schedule(g.M, g.Nout, g.Kred, g.ext_k, sms, p);
+  return p;
+}
+
+static cudaError_t launch_nf4_gemm(const GemmCall& c, cudaStream_t st) {
+  const GemmPlan p = plan_gemm(c, sk_max_ctas());
   if (c.mode == GEMM_FWD) {
-    if (nacc == 2 && bn == 256) return launch_cfg<2, 256, 3, 2, GEMM_FWD>(c, split, st);
-    if (nacc == 2 && bn == 128) return launch_cfg<2, 128, 4, 2, GEMM_FWD>(c, split, st);
-    if (nacc == 1 && bn == 256) return launch_cfg<1, 256, 4, 2, GEMM_FWD>(c, false, st);
-    return launch_cfg<1, 128, 3, 2, GEMM_FWD>(c, false, st);
+    if (p.nacc == 2 && p.bn == 256) return launch_cfg<2, 256, 3, 2, GEMM_FWD>(c, p, st);
+    if (p.nacc == 2 && p.bn == 128) return launch_cfg<2, 128, 4, 2, GEMM_FWD>(c, p, st);
+    if (p.nacc == 1 && p.bn == 256) return launch_cfg<1, 256, 4, 2, GEMM_FWD>(c, p, st);
+    return launch_cfg<1, 128, 3, 2, GEMM_FWD>(c, p, st);
   } else {
-    if (nacc == 2 && bn == 256) return launch_cfg<2, 256, 3, 2, GEMM_DX>(c, split, st);
-    if (nacc == 2 && bn == 128) return launch_cfg<2, 128, 4, 2, GEMM_DX>(c, split, st);
-    if (nacc == 1 && bn == 256) return launch_cfg<1, 256, 4, 2, GEMM_DX>(c, false, st);
-    return launch_cfg<1, 128, 3, 2, GEMM_DX>(c, false, st);
+    if (p.nacc == 2 && p.bn == 256) return launch_cfg<2, 256, 3, 2, GEMM_DX>(c, p, st);
+    if (p.nacc == 2 && p.bn == 128) return launch_cfg<2, 128, 4, 2, GEMM_DX>(c, p, st);
+    if (p.nacc == 1 && p.bn == 256) return launch_cfg<1, 256, 4, 2, GEMM_DX>(c, p, st);
+    return launch_cfg<1, 128, 3, 2, GEMM_DX>(c, p, st);
   }
 }
 

@@ -1709,6 +1709,28 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
 
 uint64_t lsk_nf4_gemm_workspace_bytes(void) { return ls::kSkWorkspaceBytes; }
 
+int lsk_nf4_gemm_plan(int32_t mode, int32_t M, int32_t N, int32_t K, int32_t ext_k, int32_t split,
+                      int32_t with_workspace, int32_t force_bn, int32_t force_nacc, int32_t sms, lsk_gemm_plan* out) {
+  if (!out || (mode != 0 && mode != 1) || M < 1 || N <= 0 || K <= 0 || K % 64 || N % 64 ||
+      (ext_k != 0 && ext_k != 16 && ext_k != 32) || split < -1 || split > 1 ||
+      (force_bn != 0 && force_bn != 128 && force_bn != 256) || force_nacc < 0 || force_nacc > 2 || sms < 0)
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_plan: bad args");
+  const int g = sms == 0 ? ls::sk_max_ctas() : std::min(sms, ls::kSkMaxCtas);
+  const int outc = mode == 0 ? N : K, red = mode == 0 ? K : N;
+  ls::GemmPlan p;
+  ls::plan_tile(mode, M, outc, red, ext_k, with_workspace != 0, split, force_bn, force_nacc, g, p);
+  ls::plan_schedule(M, outc, red, ext_k, g, p);
+  out->nacc = p.nacc;
+  out->bn = p.bn;
+  out->tiles_m = p.tiles_m;
+  out->tiles_n = p.tiles_n;
+  out->ctas = p.ctas;
+  out->whole_per_cta = p.whole_per_cta;
+  out->split_iters = p.split_iters;
+  out->k_iters = red / 64 + (ext_k > 0 ? 1 : 0);
+  return LS_OK;
+}
+
 int lsk_nf4_gemm_sk(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const uint8_t* wp, const float* wa,
                     int32_t N, int32_t K, const uint16_t* ext_a, const uint16_t* ext_b, int32_t ext_k, int32_t epi,
                     void* out, int64_t ldo, const uint16_t* residual, int64_t ldr, int32_t force_bn,

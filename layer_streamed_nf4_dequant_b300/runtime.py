@@ -19,7 +19,7 @@ import numpy as np
 import torch
 
 from ._binding import (LSError, call, check, last_error, lib, ls_config, ls_layer_host, ls_nf4_host, ls_stats_t,
-                       ls_vocab_host)
+                       ls_vocab_host, lsk_gemm_plan)
 
 MATS = ("q", "k", "v", "o", "gate", "up", "down")
 
@@ -31,6 +31,16 @@ def _stream_ordered(fn):
         with self._ordered():
             return fn(self, *args, **kwargs)
     return wrapper
+
+
+def gemm_plan(mode: int, M: int, N: int, K: int, ext_k: int = 0, split: int = 0, with_workspace: bool = True,
+              force_bn: int = 0, force_nacc: int = 0, sms: int = 148) -> Dict:
+    """Tile shape and schedule the library picks for one NF4 product (lsk_nf4_gemm_plan;
+    host only).  mode 0: out [M, N] = A [M, K] . deq(W)^T; mode 1: out [M, K] = A [M, N] . deq(W)."""
+    p = lsk_gemm_plan()
+    check(lib().lsk_nf4_gemm_plan(mode, M, N, K, ext_k, split, int(with_workspace), force_bn, force_nacc, sms,
+                                  C.byref(p)))
+    return p.as_dict()
 
 
 def make_config(s, max_tokens: int = 0, max_seqs: int = 0, max_seq_len: int = 0, resident: bool = False,
