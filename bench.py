@@ -464,7 +464,7 @@ def gemm_microbench(spec: str, reps: int = 10) -> dict:
 
     def run():
         L.call("lsk_nf4_gemm_sk", mode, x, red, M, p, a, N, K, None, None, 0, 0 if mode == 0 else 1, out, outc, None,
-               0, bn, nacc, split, ws, ws.numel(), st)
+               0, bn, nacc, split, 0, ws, ws.numel(), st)
 
     for _ in range(3):
         run()

@@ -49,6 +49,10 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
  * timeout sets the device error word (lsk_device_error).
  *  split: 0 = the cost model chooses between whole tiles and the split schedule,
  *         1 = split schedule whenever M > 128 (tests), -1 = whole tiles only.
+ *  pair_rows: 0, or (with M = 2 pair_rows) a batch of two halves whose identical rows
+ *         must give identical outputs: a split tile then takes row r and row
+ *         pair_rows + r in its two accumulators, so both meet the same k-splits (whole
+ *         tiles sum every row in k order and need no pairing).  Otherwise whole tiles.
  *  workspace: device memory, >= lsk_nf4_gemm_workspace_bytes() bytes, 256-byte
  *         aligned, zero-filled once before its first use (it holds epoch words that
  *         must not match a future launch; no reset is needed between calls).  Calls
@@ -63,17 +67,19 @@ uint64_t lsk_nf4_gemm_workspace_bytes(void);
  * 0 = the current device's, at most 148).  Output tiles are (128 nacc) x bn;
  * ctas = CTAs launched; each first takes whole_per_cta whole tiles round-robin, then an
  * even share of split_iters k-iterations of the remaining tiles (0: none); k_iters =
- * k-iterations of one tile (reduction / 64, + 1 with the LoRA stage). */
+ * k-iterations of one tile (reduction / 64, + 1 with the LoRA stage); pair_rows = the
+ * pairing in effect (tiles_m then counts 128-row blocks of one half). */
 typedef struct lsk_gemm_plan {
-  int32_t nacc, bn, tiles_m, tiles_n, ctas, whole_per_cta, k_iters, reserved;
+  int32_t nacc, bn, tiles_m, tiles_n, ctas, whole_per_cta, k_iters, pair_rows;
   int64_t split_iters;
 } lsk_gemm_plan;
 int lsk_nf4_gemm_plan(int32_t mode, int32_t M, int32_t N, int32_t K, int32_t ext_k, int32_t split,
-                      int32_t with_workspace, int32_t force_bn, int32_t force_nacc, int32_t sms, lsk_gemm_plan* out);
+                      int32_t pair_rows, int32_t with_workspace, int32_t force_bn, int32_t force_nacc, int32_t sms,
+                      lsk_gemm_plan* out);
 int lsk_nf4_gemm_sk(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const uint8_t* w_packed,
                     const float* w_absmax, int32_t N, int32_t K, const uint16_t* ext_a, const uint16_t* ext_b,
                     int32_t ext_k, int32_t epi, void* out, int64_t ldo, const uint16_t* residual, int64_t ldr,
-                    int32_t force_bn, int32_t force_nacc, int32_t split, void* workspace,
+                    int32_t force_bn, int32_t force_nacc, int32_t split, int32_t pair_rows, void* workspace,
                     uint64_t workspace_bytes, void* stream);
 
 /* RMSNorm: y = bf16(w * bf16(x * rstd)), rstd = 1/sqrt(mean(x^2) + eps) (fp32).

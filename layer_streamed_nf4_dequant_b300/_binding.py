@@ -59,11 +59,11 @@ class ls_stats_t(C.Structure):
 
 class lsk_gemm_plan(C.Structure):
     _fields_ = [("nacc", C.c_int32), ("bn", C.c_int32), ("tiles_m", C.c_int32), ("tiles_n", C.c_int32),
-                ("ctas", C.c_int32), ("whole_per_cta", C.c_int32), ("k_iters", C.c_int32), ("reserved", C.c_int32),
+                ("ctas", C.c_int32), ("whole_per_cta", C.c_int32), ("k_iters", C.c_int32), ("pair_rows", C.c_int32),
                 ("split_iters", C.c_int64)]
 
     def as_dict(self):
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 class ls_profile_t(C.Structure):
@@ -110,8 +110,9 @@ _SIGS = {
     "ls_profile_read": [P, C.POINTER(ls_profile_t)],
     "lsk_nf4_dequant": [P, P, I64, I32, P, P],
     "lsk_nf4_gemm": [I32, P, I64, I32, P, P, I32, I32, P, P, I32, I32, P, I64, P, I64, I32, I32, P],
-    "lsk_nf4_gemm_plan": [I32, I32, I32, I32, I32, I32, I32, I32, I32, I32, C.POINTER(lsk_gemm_plan)],
-    "lsk_nf4_gemm_sk": [I32, P, I64, I32, P, P, I32, I32, P, P, I32, I32, P, I64, P, I64, I32, I32, I32, P, U64, P],
+    "lsk_nf4_gemm_plan": [I32, I32, I32, I32, I32, I32, I32, I32, I32, I32, I32, C.POINTER(lsk_gemm_plan)],
+    "lsk_nf4_gemm_sk": [I32, P, I64, I32, P, P, I32, I32, P, P, I32, I32, P, I64, P, I64, I32, I32, I32, I32, P, U64,
+                        P],
     "lsk_rmsnorm_fwd": [P, P, P, P, I32, I32, F32, P],
     "lsk_rmsnorm_bwd": [P, P, P, P, P, P, I32, I32, I32, P],
     "ls_rope_table": [P, P, I32, I32, F32],

@@ -43,6 +43,7 @@ static bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
 struct SkWorkspace {
   float* ws = nullptr;
   unsigned* flags = nullptr;
+  int pair_rows = 0;   // > 0: the product's rows are two halves that must round alike (plan_schedule)
 };
 constexpr size_t kSkFlagBytes = 8192;
 constexpr size_t kSkWorkspaceBytes = kSkFlagBytes + (size_t)kSkMaxCtas * kSkSlotFloats * sizeof(float);
@@ -99,6 +100,7 @@ struct GemmPlan {
   int ctas = 0;                  // CTAs launched
   int whole_per_cta = 1;         // round-robin whole tiles per CTA
   long long split_iters = 0;     // k-iterations split evenly over the CTAs (0: none)
+  int pair_rows = 0;             // split tiles pair row r with row pair_rows + r (0: no)
 };
 
 template <int NACC, int BN, int S, int SB, int MODE>
@@ -118,8 +120,11 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   }
   const GemmArgs& g = c.g;
   CUtensorMap tA, tW, tX;
+  if (!kCanSplit && p.pair_rows) return cudaErrorInvalidValue;
+  // a paired tile loads two 128-row boxes (one from each half) per stage
+  const uint32_t a_box_rows = p.pair_rows ? 128u : (uint32_t)C::BM;
   if (!make_map_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.A, (uint64_t)g.Kred, (uint64_t)g.M,
-                   (uint64_t)c.lda * 2, 64, C::BM, CU_TENSOR_MAP_SWIZZLE_128B))
+                   (uint64_t)c.lda * 2, 64, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (MODE == GEMM_FWD) {
     if (!make_map_2d(&tW, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.Wp, (uint64_t)g.Kw / 2, (uint64_t)g.Nw,
@@ -131,7 +136,7 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
       return cudaErrorInvalidValue;
   }
   if (g.ext_k > 0) {
-    if (!make_map_2d(&tX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.ext_a, 64, (uint64_t)g.M, 128, 64, C::BM,
+    if (!make_map_2d(&tX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.ext_a, 64, (uint64_t)g.M, 128, 64, a_box_rows,
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   } else {
@@ -148,6 +153,7 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   ga.tiles_n = p.tiles_n;
   ga.sched_ctas = p.ctas;
   ga.sched_dp = p.whole_per_cta;
+  ga.pair_rows = p.pair_rows;
   ga.sk_iters = 0;
   ga.sk_ws = nullptr;
   ga.sk_flags = nullptr;
@@ -161,9 +167,9 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   }
   if (!kCanSplit && (ga.sched_dp != 1 || ga.sched_ctas != nt)) return cudaErrorInvalidValue;
   if (ga.sk_iters == 0) {
-    if (ga.sched_dp == 1 && ga.sched_ctas == nt)
+    if (ga.sched_dp == 1 && ga.sched_ctas == nt && !p.pair_rows)
       kern_whole<<<(unsigned)nt, C::THREADS, C::SMEM, st>>>(tA, tW, tX, ga);
-    else   // whole tiles, several per CTA
+    else   // whole tiles, several per CTA, or paired rows
       kern_split<<<(unsigned)ga.sched_ctas, C::THREADS, C::SMEM, st>>>(tA, tW, tX, ga);
     return cudaGetLastError();
   }
@@ -247,8 +253,20 @@ static void plan_tile(int mode, int M, int Nout, int Kred, int ext_k, bool has_w
 // Whole tiles, one per CTA; or, for a split plan, one CTA per SM (at most `sms`): full
 // rounds of whole tiles, then the last one to two rounds' worth of tiles split evenly by
 // k-iterations (each CTA at least 4 of them).
-static void plan_schedule(int M, int Nout, int Kred, int ext_k, int sms, GemmPlan& p) {
-  const long long tm = (M + 128 * p.nacc - 1) / (128 * p.nacc), tn = (Nout + p.bn - 1) / p.bn, nt = tm * tn;
+// pair_rows > 0 marks a batch of two halves [rows 0..pair_rows); the same rows again] that
+// must give identical outputs for identical rows (the shared-read DPO forward: policy and
+// reference copies).  Whole tiles do that as they are (every row is summed in k order);
+// a split plan pairs the halves instead, its two 128-row accumulators taking row r and
+// row pair_rows + r, so both meet the same k-splits.  Without two accumulators, or when
+// M is not 2 * pair_rows, the plan falls back to whole tiles.
+static void plan_schedule(int M, int Nout, int Kred, int ext_k, int sms, int pair_rows, GemmPlan& p) {
+  p.pair_rows = 0;
+  if (pair_rows > 0) {
+    if (p.split && p.nacc == 2 && M == 2 * pair_rows) p.pair_rows = pair_rows;
+    else p.split = false;
+  }
+  const long long rows = p.pair_rows ? p.pair_rows : M, tile_rows = p.pair_rows ? 128 : 128 * p.nacc;
+  const long long tm = (rows + tile_rows - 1) / tile_rows, tn = (Nout + p.bn - 1) / p.bn, nt = tm * tn;
   const int niter = Kred / 64 + (ext_k > 0 ? 1 : 0);
   p.tiles_m = (int)tm;
   p.tiles_n = (int)tn;
@@ -277,7 +295,7 @@ static GemmPlan plan_gemm(const GemmCall& c, int sms) {
   const GemmArgs& g = c.g;
   GemmPlan p;
   plan_tile(c.mode, g.M, g.Nout, g.Kred, g.ext_k, c.sk.ws && c.sk.flags, c.split, c.force_bn, c.force_nacc, sms, p);
-  plan_schedule(g.M, g.Nout, g.Kred, g.ext_k, sms, p);
+  plan_schedule(g.M, g.Nout, g.Kred, g.ext_k, sms, c.sk.pair_rows, p);
   return p;
 }
 

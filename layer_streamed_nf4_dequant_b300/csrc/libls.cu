@@ -164,7 +164,7 @@ struct ls_ctx {
   int32_t *tok2 = nullptr, *cu2 = nullptr;   // shared-read DPO forward: doubled batch
   float* attn_part = nullptr;                 // per-query-head dk / dv partials
   ls::SkWorkspace skw;                        // split-tile (stream-K) scratch of the NF4 GEMMs
-  bool whole_tiles_only = false;              // set while the shared-read DPO forward runs
+  int pair_rows = 0;                          // T while the shared-read DPO forward runs
   int Tf = 0;                                 // forward row capacity (2 max_tokens with shared read)
   int P = 0;
   size_t lora_part_floats = 0;
@@ -192,13 +192,15 @@ struct ls_ctx {
 
 namespace {
 
-// Split-tile scratch for the stack's NF4 GEMMs, or none (whole tiles).  The shared-read
-// DPO forward stacks the policy and reference copies of the batch into one product;
-// whole tiles make each output row depend on that row's inputs alone, so identical
-// policy and reference rows give bit-identical results (the B = 0 start has policy =
-// reference exactly), which a split tile schedule (different k-splits for the two
-// halves' tiles) would not.
-ls::SkWorkspace gemm_ws(const ls_ctx* c) { return c->whole_tiles_only ? ls::SkWorkspace{} : c->skw; }
+// Split-tile scratch for the stack's NF4 GEMMs.  The shared-read DPO forward stacks the
+// policy and reference copies of the batch into one product of 2T rows; marking the
+// halves (pair_rows = T) makes identical policy and reference rows round identically
+// under any tile schedule (the B = 0 start has policy = reference exactly).
+ls::SkWorkspace gemm_ws(const ls_ctx* c) {
+  ls::SkWorkspace w = c->skw;
+  w.pair_rows = c->pair_rows;
+  return w;
+}
 
 int fail(ls_ctx* c, int code, const std::string& m) {
   if (c && c->err == 0) {
@@ -1282,11 +1284,11 @@ int stream_step_fwd_dpo(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t n
   for (int l = 0; l < c->L; ++l)
     if (!c->hl_ok[l]) return fail(c, LS_ERR_STATE, "stream_step_fwd_dpo: layer " + std::to_string(l) + " not loaded");
   if (!c->hv_ok) return fail(c, LS_ERR_STATE, "stream_step_fwd_dpo: vocabulary not loaded");
-  struct WholeTiles {
+  struct PairedRows {
     ls_ctx* c;
-    explicit WholeTiles(ls_ctx* x) : c(x) { c->whole_tiles_only = true; }
-    ~WholeTiles() { c->whole_tiles_only = false; }
-  } whole_tiles(c);
+    PairedRows(ls_ctx* x, int t) : c(x) { c->pair_rows = t; }
+    ~PairedRows() { c->pair_rows = 0; }
+  } paired(c, T);
   cudaStream_t st = c->cs;
   const int H = c->H, T2 = 2 * T, n2 = 2 * nseq;
   const size_t TH = (size_t)T * H, T2H = (size_t)T2 * H;
@@ -1709,17 +1711,24 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
 
 uint64_t lsk_nf4_gemm_workspace_bytes(void) { return ls::kSkWorkspaceBytes; }
 
+static ls::SkWorkspace paired_ws(void* workspace, int pair_rows) {
+  ls::SkWorkspace w = ls::sk_workspace_at(workspace);
+  w.pair_rows = pair_rows;
+  return w;
+}
+
 int lsk_nf4_gemm_plan(int32_t mode, int32_t M, int32_t N, int32_t K, int32_t ext_k, int32_t split,
-                      int32_t with_workspace, int32_t force_bn, int32_t force_nacc, int32_t sms, lsk_gemm_plan* out) {
+                      int32_t pair_rows, int32_t with_workspace, int32_t force_bn, int32_t force_nacc, int32_t sms,
+                      lsk_gemm_plan* out) {
   if (!out || (mode != 0 && mode != 1) || M < 1 || N <= 0 || K <= 0 || K % 64 || N % 64 ||
-      (ext_k != 0 && ext_k != 16 && ext_k != 32) || split < -1 || split > 1 ||
+      (ext_k != 0 && ext_k != 16 && ext_k != 32) || split < -1 || split > 1 || pair_rows < 0 ||
       (force_bn != 0 && force_bn != 128 && force_bn != 256) || force_nacc < 0 || force_nacc > 2 || sms < 0)
     return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_plan: bad args");
   const int g = sms == 0 ? ls::sk_max_ctas() : std::min(sms, ls::kSkMaxCtas);
   const int outc = mode == 0 ? N : K, red = mode == 0 ? K : N;
   ls::GemmPlan p;
   ls::plan_tile(mode, M, outc, red, ext_k, with_workspace != 0, split, force_bn, force_nacc, g, p);
-  ls::plan_schedule(M, outc, red, ext_k, g, p);
+  ls::plan_schedule(M, outc, red, ext_k, g, pair_rows, p);
   out->nacc = p.nacc;
   out->bn = p.bn;
   out->tiles_m = p.tiles_m;
@@ -1728,14 +1737,17 @@ int lsk_nf4_gemm_plan(int32_t mode, int32_t M, int32_t N, int32_t K, int32_t ext
   out->whole_per_cta = p.whole_per_cta;
   out->split_iters = p.split_iters;
   out->k_iters = red / 64 + (ext_k > 0 ? 1 : 0);
+  out->pair_rows = p.pair_rows;
   return LS_OK;
 }
 
 int lsk_nf4_gemm_sk(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const uint8_t* wp, const float* wa,
                     int32_t N, int32_t K, const uint16_t* ext_a, const uint16_t* ext_b, int32_t ext_k, int32_t epi,
                     void* out, int64_t ldo, const uint16_t* residual, int64_t ldr, int32_t force_bn,
-                    int32_t force_nacc, int32_t split, void* workspace, uint64_t workspace_bytes, void* s) {
+                    int32_t force_nacc, int32_t split, int32_t pair_rows, void* workspace, uint64_t workspace_bytes,
+                    void* s) {
   if (split < -1 || split > 1) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: split must be -1, 0 or 1");
+  if (pair_rows < 0) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: pair_rows must be >= 0");
   if (!workspace || workspace_bytes < ls::kSkWorkspaceBytes || reinterpret_cast<uintptr_t>(workspace) % 256)
     return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: workspace missing, smaller than "
                                       "lsk_nf4_gemm_workspace_bytes() or not 256-byte aligned");
@@ -1756,7 +1768,7 @@ int lsk_nf4_gemm_sk(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, con
   if (residual && epi != 0) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: residual only with bf16 output");
   KCK(gemm(mode, reinterpret_cast<const bf16*>(A), lda, M, wp, wa, N, K, reinterpret_cast<const bf16*>(ext_a),
            reinterpret_cast<const bf16*>(ext_b), ext_k, epi, out, ldo, reinterpret_cast<const bf16*>(residual), ldr,
-           STREAM(s), ls::sk_workspace_at(workspace), force_bn, force_nacc, split));
+           STREAM(s), paired_ws(workspace, pair_rows), force_bn, force_nacc, split));
   return LS_OK;
 }
 

@@ -75,6 +75,11 @@ struct GemmArgs {
   float* sk_ws;                      // split tiles: one fp32 partial slot (kSkSlotFloats) per CTA
   unsigned* sk_flags;                // [sched_ctas][8]: epoch word per (CTA, epilogue warp)
   unsigned sk_epoch;                 // this launch's nonzero epoch
+  // Split schedule on a paired batch [first half; second half] of 2 * pair_rows rows: the
+  // two accumulators of a tile take rows m0 + a * pair_rows, so row r and row pair_rows + r
+  // always share a CTA, its k-ranges and its partial sums (identical inputs -> identical
+  // outputs).  0: a tile's accumulators take consecutive 128-row blocks.
+  int pair_rows;
 };
 
 // Stream-K workspace: one 256 x 256 fp32 partial tile per CTA, at most kSkMaxCtas CTAs.
@@ -355,13 +360,18 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
   sc.init(g, blockIdx.x, niter);
   int tile, k0, k1;
 
+  // rows of a tile: NACC consecutive 128-row blocks, or (split schedule only) the same
+  // 128 rows of each half of a paired batch
+  const int pair = SPLIT && NACC == 2 ? g.pair_rows : 0;
+  const int tile_rows = pair ? 128 : C::BM;
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int gi = 0;
     bool stop = false;
     while (!stop && sc.next(tile, k0, k1)) {
       int m0, n0;
-      sc.tile_origin(tile, C::BM, BN, m0, n0);
+      sc.tile_origin(tile, tile_rows, BN, m0, n0);
       for (int it = k0; it < k1; ++it, ++gi) {
         const int s = gi % S;
         if (s_abort || !mbar_wait(empty(s), ((gi / S) & 1) ^ 1)) {
@@ -373,13 +383,23 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
         if (lane == 0) {
           if (it < KB) {
             mbar_arrive_expect_tx(full(s), C::A_BYTES + C::W_BYTES);
-            tma_load_2d(a_dst, &tmA, it * 64, m0, full(s));
+            if (pair) {   // two 128-row boxes: this tile's rows of each half
+              tma_load_2d(a_dst, &tmA, it * 64, m0, full(s));
+              tma_load_2d(a_dst + 16384, &tmA, it * 64, m0 + pair, full(s));
+            } else {
+              tma_load_2d(a_dst, &tmA, it * 64, m0, full(s));
+            }
             const uint32_t w_dst = sb + C::OFF_W + s * C::W_BYTES;
             if (MODE == GEMM_FWD) tma_load_2d(w_dst, &tmW, it * 32, n0, full(s));
             else tma_load_2d(w_dst, &tmW, n0 / 2, it * 64, full(s));
           } else {
             mbar_arrive_expect_tx(full(s), C::A_BYTES);
-            tma_load_2d(a_dst, &tmX, 0, m0, full(s));
+            if (pair) {
+              tma_load_2d(a_dst, &tmX, 0, m0, full(s));
+              tma_load_2d(a_dst + 16384, &tmX, 0, m0 + pair, full(s));
+            } else {
+              tma_load_2d(a_dst, &tmX, 0, m0, full(s));
+            }
           }
         }
         if (it < KB) {
@@ -466,7 +486,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
     int gi = 0, pc = 0;
     while (sc.next(tile, k0, k1)) {
       int m0, n0;
-      sc.tile_origin(tile, C::BM, BN, m0, n0);
+      sc.tile_origin(tile, tile_rows, BN, m0, n0);
       const int n = k1 - k0;
       bool stop = false;
       for (int gj = gi + ((grp - gi % step) + step) % step; gj < gi + n; gj += step) {
@@ -517,8 +537,8 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
         }
       }
       for (int a = 0; a < NACC; ++a) {
-        const int row = m0 + a * 128 + wq * 32 + lane;
-        const bool rok = row < g.M;
+        const int row = m0 + a * (pair ? pair : 128) + wq * 32 + lane;
+        const bool rok = row < g.M && (!pair || m0 + wq * 32 + lane < pair);
         float run_m = -INFINITY, run_s = 0.f;
         int tgt = -1;
         float lse_r = 0.f, coef_r = 0.f;

@@ -33,13 +33,13 @@ def _stream_ordered(fn):
     return wrapper
 
 
-def gemm_plan(mode: int, M: int, N: int, K: int, ext_k: int = 0, split: int = 0, with_workspace: bool = True,
-              force_bn: int = 0, force_nacc: int = 0, sms: int = 148) -> Dict:
+def gemm_plan(mode: int, M: int, N: int, K: int, ext_k: int = 0, split: int = 0, pair_rows: int = 0,
+              with_workspace: bool = True, force_bn: int = 0, force_nacc: int = 0, sms: int = 148) -> Dict:
     """Tile shape and schedule the library picks for one NF4 product (lsk_nf4_gemm_plan;
     host only).  mode 0: out [M, N] = A [M, K] . deq(W)^T; mode 1: out [M, K] = A [M, N] . deq(W)."""
     p = lsk_gemm_plan()
-    check(lib().lsk_nf4_gemm_plan(mode, M, N, K, ext_k, split, int(with_workspace), force_bn, force_nacc, sms,
-                                  C.byref(p)))
+    check(lib().lsk_nf4_gemm_plan(mode, M, N, K, ext_k, split, pair_rows, int(with_workspace), force_bn, force_nacc,
+                                  sms, C.byref(p)))
     return p.as_dict()
 
 

@@ -160,3 +160,26 @@ def test_plan_rejects_bad_arguments():
         L.gemm_plan(0, 256, 256, 256, ext_k=8)
     with pytest.raises(L.LSError):
         L.gemm_plan(0, 256, 256, 256, split=2)
+
+
+def test_paired_rows_plan():
+    """Shared-read forward products (2T rows, pair_rows = T): a split plan pairs the
+    halves (128-row blocks of one half, same counts as unpaired); a whole-tile plan, a
+    one-accumulator tile or a batch that is not two halves falls back to whole tiles."""
+    p = L.gemm_plan(0, 2048, 28672, 4096, pair_rows=1024)
+    assert p["pair_rows"] == 1024 and (p["tiles_m"], p["tiles_n"]) == (8, 112)
+    assert p["ctas"] == SMS and p["whole_per_cta"] == 5 and p["split_iters"] == 156 * 64
+    _check_schedule(p)
+    p = L.gemm_plan(0, 2048, 4096, 4096, pair_rows=1024)       # o: the model keeps whole tiles
+    assert p["pair_rows"] == 0 and p["split_iters"] == 0 and p["ctas"] == p["tiles_m"] * p["tiles_n"]
+    for kw in ({"pair_rows": 1000, "split": 1}, {"pair_rows": 1024, "split": 1, "force_nacc": 1}):
+        p = L.gemm_plan(0, 2048, 28672, 4096, **kw)
+        assert p["pair_rows"] == 0 and p["split_iters"] == 0 and p["ctas"] == p["tiles_m"] * p["tiles_n"]
+    rng = random.Random(11)
+    for _ in range(60):
+        T = rng.randint(65, 2048)
+        p = L.gemm_plan(rng.randint(0, 1), 2 * T, 64 * rng.randint(1, 200), 64 * rng.randint(1, 100),
+                        split=1, pair_rows=T)
+        assert p["pair_rows"] == T and p["tiles_m"] == -(-T // 128)
+        if p["split_iters"] or p["whole_per_cta"] != 1:
+            _check_schedule(p)

@@ -46,11 +46,11 @@ def _ws():
     return _WS["ws"]
 
 
-def _sk(mode, x, M, p, a, N, K, ext_a, ext_b, ext_k, epi, out, ldo, res, split):
+def _sk(mode, x, M, p, a, N, K, ext_a, ext_b, ext_k, epi, out, ldo, res, split, pair_rows=0):
     ws = _ws()
     red = K if mode == 0 else N
     k("lsk_nf4_gemm_sk", mode, x, red, M, p, a, N, K, ext_a, ext_b, ext_k, epi, out, ldo, res,
-      (ldo if res is not None else 0), 0, 0, split, ws, ws.numel())
+      (ldo if res is not None else 0), 0, 0, split, pair_rows, ws, ws.numel())
 
 
 def _check_device_error():
@@ -175,6 +175,34 @@ def test_split_matches_whole_tiles_and_auto():
     _check_device_error()
 
 
+@pytest.mark.parametrize("T,N,K,ext", [(1024, 6144, 4096, 0), (300, 640, 1024, 16)])
+def test_paired_halves_round_identically(T, N, K, ext):
+    """The shared-read forward's batch [X; X] (pair_rows = T) on the split schedule: both
+    halves bit-identical (row r and row T + r share a CTA and its k-splits), and within
+    the tolerance of the oracle; T = 300 leaves a ragged last 128-row block."""
+    x = synth.gaussian((T, K), 42, T, K)
+    w = _w(N, K, seed=43)
+    res = synth.gaussian((T, N), 44, T, N)
+    p, a, _, _ = nf4_dev(w)
+    wd = _deq(w)
+    x2, r2 = bf16_dev(np.concatenate([x, x])), bf16_dev(np.concatenate([res, res]))
+    ext_a = ext_b = None
+    if ext:
+        u = synth.gaussian((T, 64), 45, T) * (np.arange(64) < ext)
+        b = synth.gaussian((N, 64), 46, N) * (np.arange(64) < ext) * 0.05
+        ext_a, ext_b = bf16_dev(np.concatenate([u, u])), bf16_dev(b)
+    out = torch.empty((2 * T, N), dtype=torch.bfloat16, device=DEV)
+    _sk(0, x2, 2 * T, p, a, N, K, ext_a, ext_b, ext, 0, out, N, r2, 1, pair_rows=T)
+    torch.cuda.synchronize()
+    assert torch.equal(out[:T], out[T:])
+    lora = None
+    if ext:
+        lora = (om.t64(np.asarray(to_np(ext_a[:T]))), om.t64(np.asarray(to_np(ext_b))))
+    want = om.linear(om.t64(x), om.t64(wd), lora=lora, residual=om.t64(res)).numpy()
+    assert rel_err(to_np(out[:T]), want) <= TOL
+    _check_device_error()
+
+
 def test_split_rejects_small_workspace():
     ws = _ws()
     x = torch.zeros((256, 256), dtype=torch.bfloat16, device=DEV)
@@ -182,5 +210,5 @@ def test_split_rejects_small_workspace():
     p, a, _, _ = nf4_dev(w)
     out = torch.empty((256, 256), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(L.LSError):
-        k("lsk_nf4_gemm_sk", 0, x, 256, 256, p, a, 256, 256, None, None, 0, 0, out, 256, None, 0, 0, 0, 1,
+        k("lsk_nf4_gemm_sk", 0, x, 256, 256, p, a, 256, 256, None, None, 0, 0, out, 256, None, 0, 0, 0, 1, 0,
           ws, ws.numel() - 1)
