@@ -91,3 +91,26 @@ def test_rope_table_matches_fp64():
 def test_gemm_split_workspace_size():
     """Epoch words (8 KiB) plus one 256 x 256 fp32 partial tile for each of 148 CTAs."""
     assert int(L.lib().lsk_nf4_gemm_workspace_bytes()) == 8192 + 148 * 256 * 256 * 4
+
+
+def test_binding_signatures_match_header_declarations():
+    """Every function declared in include/*.h has a ctypes signature with the same number
+    of parameters (catches ABI drift between the headers and the binding)."""
+    import re
+    from layer_streamed_nf4_dequant_b300 import _binding as B
+    decl = {}
+    for h in B.HEADERS:
+        txt = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s+([a-z_][a-z_0-9]*)\s*\(([^)]*)\)\s*;", txt,
+                             flags=re.M):
+            args = m.group(2).strip()
+            decl[m.group(1)] = 0 if args in ("", "void") else len(args.split(","))
+    assert sorted(decl) == sorted(L.header_functions())
+    special = {"ls_last_error": 1, "lsk_nf4_gemm_workspace_bytes": 0}
+    lib = L.lib()
+    for name, n in decl.items():
+        if name in special:
+            assert n == special[name] and len(getattr(lib, name).argtypes) == n, name
+        else:
+            assert name in B._SIGS, f"{name} has no ctypes signature"
+            assert len(B._SIGS[name]) == n, f"{name}: header {n} parameters, binding {len(B._SIGS[name])}"
