@@ -24,6 +24,21 @@ static PFN_encodeTiled get_encode_fn() {
   return fn;
 }
 
+// Raise a kernel's dynamic shared-memory limit on the current device, once per device and
+// kernel (`done` holds one bit per device; the caller keeps one per kernel).  Concurrent
+// first calls both set the same attribute, which is harmless.  Returns the first error.
+template <class Kern>
+static cudaError_t ensure_smem_attr(Kern kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 // 2-D tensor map over a row-major matrix [rows, cols] with row pitch `pitch_bytes`.
 static bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
                         uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
@@ -70,13 +85,15 @@ static unsigned next_sk_epoch() {
 static int sk_max_ctas() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kSkMaxCtas;
-  static int cached[64] = {0};
-  if (cached[dev] == 0) {
+  static std::atomic<int> cached[64];   // zero-initialised: not yet queried
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = kSkMaxCtas;
-    cached[dev] = sms < kSkMaxCtas ? sms : kSkMaxCtas;
+    v = sms < kSkMaxCtas ? sms : kSkMaxCtas;
+    cached[dev].store(v, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return v;
 }
 
 struct GemmCall {
@@ -110,13 +127,11 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   constexpr bool kCanSplit = NACC == 2;
   auto kern_whole = nf4_gemm_kernel<NACC, BN, S, SB, MODE, false>;
   auto kern_split = nf4_gemm_kernel<NACC, BN, S, SB, MODE, kCanSplit>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern_whole, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e == cudaSuccess && kCanSplit)
-      e = cudaFuncSetAttribute(kern_split, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static std::atomic<uint64_t> attr_whole{0}, attr_split{0};
+  {
+    cudaError_t e = ensure_smem_attr(kern_whole, C::SMEM, attr_whole);
+    if (e == cudaSuccess && kCanSplit) e = ensure_smem_attr(kern_split, C::SMEM, attr_split);
     if (e != cudaSuccess) return e;
-    attr_done = true;
   }
   const GemmArgs& g = c.g;
   CUtensorMap tA, tW, tX;

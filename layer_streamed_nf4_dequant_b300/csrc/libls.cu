@@ -513,10 +513,10 @@ template <int HD>
 cudaError_t attn_fwd_launch(const bf16* qkv, long long ld, const int* cu, int nseq, int maxlen, int nh, int nkv,
                             bf16* out, long long ldo, float* lse, int T, cudaStream_t st) {
   const int smem = 5 * 64 * (HD + 8) * 2;   // Q + two (K, V) buffers
-  static bool set = false;
-  if (!set) {
-    cudaFuncSetAttribute(ls::attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    set = true;
+  static std::atomic<uint64_t> attr{0};
+  {
+    const cudaError_t e = ls::ensure_smem_attr(ls::attn_fwd_kernel<HD>, smem, attr);
+    if (e != cudaSuccess) return e;
   }
   dim3 grid((maxlen + 63) / 64, nh, nseq);
   ls::attn_fwd_kernel<HD><<<grid, 128, smem, st>>>(qkv, ld, cu, nh, nkv, 1.0f / sqrtf((float)HD), out, ldo, lse, T);
@@ -532,11 +532,11 @@ cudaError_t attn_bwd_launch(const bf16* qkv, long long ld, const bf16* dout, con
                             float* dqkv, long long ldg, int T, cudaStream_t st, float* part = nullptr) {
   const int smem_q = 6 * 64 * (HD + 8) * 2;                  // Q, dO + two (K, V) buffers
   const int smem_k = 6 * 64 * (HD + 8) * 2 + 4 * 64 * 4;     // K, V + two (Q, dO, lse, D) buffers
-  static bool set = false;
-  if (!set) {
-    cudaFuncSetAttribute(ls::attn_bwd_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q);
-    cudaFuncSetAttribute(ls::attn_bwd_dkdv_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_k);
-    set = true;
+  static std::atomic<uint64_t> attr_q{0}, attr_k{0};
+  {
+    cudaError_t e = ls::ensure_smem_attr(ls::attn_bwd_dq_kernel<HD>, smem_q, attr_q);
+    if (e == cudaSuccess) e = ls::ensure_smem_attr(ls::attn_bwd_dkdv_kernel<HD>, smem_k, attr_k);
+    if (e != cudaSuccess) return e;
   }
   const float scale = 1.0f / sqrtf((float)HD);
   {
