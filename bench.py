@@ -508,7 +508,7 @@ def main():
     ap.add_argument("--method", default=None, choices=["sft", "dpo", "simpo", "orpo", "kto"],
                     help="training method on the config's pairs (default: the config's own)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--gemm", default=None, help="micro-benchmark one NF4 GEMM: mode,M,N,K[,bn,nacc]")
+    ap.add_argument("--gemm", default=None, help="micro-benchmark one NF4 GEMM: mode,M,N,K[,bn,nacc[,split]] (split: 0 cost model, 1 split tiles, -1 whole tiles)")
     ap.add_argument("--stream-source", default="ram", choices=["ram", "file"],
                     help="where the streamed decoder layers live: pinned host RAM, or a file (NVMe tier)")
     ap.add_argument("--file-dir", default=None, help="directory of the layer file (default: the temp dir)")
