@@ -300,6 +300,19 @@ int ls_profile_read(ls_ctx* ctx, ls_profile_t* out);
  * training step never needs it.  LS_ERR_STATE without a saved forward. */
 int ls_read_activation(ls_ctx* ctx, int32_t layer, uint16_t* d_out);
 
+/* Inspection hook for the shared-read DPO forward (the activation store keeps only the
+ * policy rows).  With d_buf non-NULL, every later stream_step_fwd_dpo of T tokens also
+ * copies the reference rows (adapter off) of each activation-store entry 0..L into
+ * d_buf: bf16 [(L+1), T, H], entry l at element offset l * T * H, in the meaning of
+ * ls_read_activation (entry 0 the embedding output, entry L the last layer's output).
+ * The copies are enqueued on the compute stream after each layer; the step's results
+ * are unchanged.  d_buf: caller-owned device memory, 16-byte aligned, at least
+ * (L+1) * max_tokens * H * 2 bytes (LS_ERR_ARG otherwise), kept valid until switched
+ * off with d_buf = NULL or ls_destroy.  LS_ERR_STATE without cfg.dpo_shared_read.
+ * Lets a layer-by-layer check against a reference implementation recompute the very
+ * sweep whose loss it grades; a training step never needs it. */
+int ls_capture_reference(ls_ctx* ctx, uint16_t* d_buf, uint64_t bytes);
+
 /* Test hook: make every later slot copy on the copy stream first wait host_delay_ms
  * on the host (a host callback), so a bounded ls_sync can be shown to give up.  No
  * GPU fault is involved.  0 switches it off. */

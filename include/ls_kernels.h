@@ -141,9 +141,11 @@ int lsk_lora_du(const uint16_t* dy, int64_t ldy, int32_t col_q, int32_t nq, cons
                 int32_t T, void* stream);
 
 /* Deterministic outer product over tokens: out (+)= X^T U with X bf16 [T, ldx]
- * (ncols columns) and U (fp32 u_f32 or bf16 u_bf16, [T, ldu], first r columns).
+ * (ncols columns) and U (fp32 u_f32 or bf16 u_bf16, [T, ldu], first r columns; only
+ * those r columns are read, so a compact U with ldu = r is fine).
  * layout 0: out [ncols, r] (dB shape); layout 1: out [r, ncols] (dA shape).
- * X rows must be 16-byte aligned (X 16-byte aligned, ldx and ncols multiples of 8).
+ * X rows must be 16-byte aligned (X 16-byte aligned, ldx and ncols multiples of 8);
+ * ldx >= ncols, ldu >= r, ceil(T / rows_per_chunk) <= 65535, else LS_ERR_ARG.
  * scratch fp32 of nchunks * ncols * 16 floats, nchunks = ceil(T / rows_per_chunk). */
 int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* u_f32, const uint16_t* u_bf16,
                    int32_t ldu, int32_t r, int32_t T, int32_t layout, int32_t accumulate, float* scratch,
@@ -164,6 +166,9 @@ int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* u
  *    every GPU that loads the library holds it until the process exits.
  *  - The first call on a device looks the array's device address up (with that
  *    device current) and caches it; make that first call before any stream capture.
+ *    The cached address belongs to the device's primary context: after a
+ *    cudaDeviceReset on that device it is stale, so do not call this again in the
+ *    same process after such a reset.
  *  - Every call on a device shares the one array and it keeps the last call's
  *    contents; each call writes every element it later reads, so nothing needs
  *    clearing.  Calls whose kernels overlap on the GPU (e.g. on two streams) race on

@@ -106,6 +106,7 @@ _SIGS = {
     "ls_stats": [P, C.POINTER(ls_stats_t), I32],
     "ls_debug_copy_delay": [P, I32],
     "ls_read_activation": [P, I32, P],
+    "ls_capture_reference": [P, P, U64],
     "ls_profile": [P, I32],
     "ls_profile_read": [P, C.POINTER(ls_profile_t)],
     "lsk_nf4_dequant": [P, P, I64, I32, P, P],

@@ -165,6 +165,8 @@ struct ls_ctx {
   float* attn_part = nullptr;                 // per-query-head dk / dv partials
   ls::SkWorkspace skw;                        // split-tile (stream-K) scratch of the NF4 GEMMs
   int pair_rows = 0;                          // T while the shared-read DPO forward runs
+  bf16* ref_cap = nullptr;                    // ls_capture_reference: caller's [(L+1), T, H] buffer
+  uint64_t ref_cap_bytes = 0;
   int Tf = 0;                                 // forward row capacity (2 max_tokens with shared read)
   int P = 0;
   size_t lora_part_floats = 0;
@@ -477,6 +479,78 @@ inline int grid1d(long long n, int threads, int cap = 148 * 16) {
   return (int)g;
 }
 
+// RMSNorm launches: one block per row with the row's slice in registers for rows up to
+// 8192 wide (the row-per-block kernels), one warp per row beyond that.
+template <int V>
+void rmsnorm_fwd_v(const bf16* x, const bf16* w, bf16* y, float* rstd, int T, int H, float eps, cudaStream_t st) {
+  ls::rmsnorm_fwd_row_kernel<V><<<T, 128, 0, st>>>(x, w, y, rstd, H, eps);
+}
+cudaError_t rmsnorm_fwd(const bf16* x, const bf16* w, bf16* y, float* rstd, int T, int H, float eps,
+                        cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  switch ((H / 8 + 127) / 128) {
+    case 1: rmsnorm_fwd_v<1>(x, w, y, rstd, T, H, eps, st); break;
+    case 2: rmsnorm_fwd_v<2>(x, w, y, rstd, T, H, eps, st); break;
+    case 3: rmsnorm_fwd_v<3>(x, w, y, rstd, T, H, eps, st); break;
+    case 4: rmsnorm_fwd_v<4>(x, w, y, rstd, T, H, eps, st); break;
+    case 5: rmsnorm_fwd_v<5>(x, w, y, rstd, T, H, eps, st); break;
+    case 6: rmsnorm_fwd_v<6>(x, w, y, rstd, T, H, eps, st); break;
+    case 7: rmsnorm_fwd_v<7>(x, w, y, rstd, T, H, eps, st); break;
+    case 8: rmsnorm_fwd_v<8>(x, w, y, rstd, T, H, eps, st); break;
+    default: ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(x, w, y, rstd, T, H, eps);
+  }
+  return cudaGetLastError();
+}
+template <int V>
+void rmsnorm_bwd_v(const float* dy, const bf16* x, const float* rstd, const bf16* w, float* dx, bf16* dxb, int T,
+                   int H, int acc, cudaStream_t st) {
+  ls::rmsnorm_bwd_row_kernel<V><<<T, 256, 0, st>>>(dy, x, rstd, w, dx, dxb, H, acc);
+}
+cudaError_t rmsnorm_bwd(const float* dy, const bf16* x, const float* rstd, const bf16* w, float* dx, bf16* dxb, int T,
+                        int H, int acc, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  switch ((H / 4 + 255) / 256) {
+    case 1: rmsnorm_bwd_v<1>(dy, x, rstd, w, dx, dxb, T, H, acc, st); break;
+    case 2: rmsnorm_bwd_v<2>(dy, x, rstd, w, dx, dxb, T, H, acc, st); break;
+    case 3: rmsnorm_bwd_v<3>(dy, x, rstd, w, dx, dxb, T, H, acc, st); break;
+    case 4: rmsnorm_bwd_v<4>(dy, x, rstd, w, dx, dxb, T, H, acc, st); break;
+    case 5: rmsnorm_bwd_v<5>(dy, x, rstd, w, dx, dxb, T, H, acc, st); break;
+    case 6: rmsnorm_bwd_v<6>(dy, x, rstd, w, dx, dxb, T, H, acc, st); break;
+    case 7: rmsnorm_bwd_v<7>(dy, x, rstd, w, dx, dxb, T, H, acc, st); break;
+    case 8: rmsnorm_bwd_v<8>(dy, x, rstd, w, dx, dxb, T, H, acc, st); break;
+    default: ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(dy, x, rstd, w, dx, dxb, T, H, acc);
+  }
+  return cudaGetLastError();
+}
+
+// RoPE launches: the 16-byte kernels when rows and pointers allow 16-byte access.
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+cudaError_t rope_fwd(bf16* qkv, long long ld, const int* pos, const float* ct, const float* stt, int T, int nheads,
+                     int hd, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (ld % 8 == 0 && al16(qkv) && al16(ct) && al16(stt) && (hd / 2) % 8 == 0) {
+    const long long n = (long long)T * nheads * (hd / 16);
+    ls::rope_fwd_vec_kernel<<<grid1d(n, 256), 256, 0, st>>>(qkv, ld, pos, ct, stt, T, nheads, hd);
+  } else {
+    const long long n = (long long)T * nheads * (hd / 2);
+    ls::rope_fwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(qkv, ld, pos, ct, stt, T, nheads, hd);
+  }
+  return cudaGetLastError();
+}
+cudaError_t rope_bwd_cast(const float* g, bf16* out, long long ld, const int* pos, const float* ct, const float* stt,
+                          int T, int nrot, int hd, int ncols, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (ld % 8 == 0 && al16(g) && al16(out) && al16(ct) && al16(stt) && (hd / 2) % 4 == 0 &&
+      (ncols - nrot * hd) % 8 == 0 && ncols >= nrot * hd) {
+    const long long n = (long long)T * (nrot * (hd / 8) + (ncols - nrot * hd) / 8);
+    ls::rope_bwd_cast_vec_kernel<<<grid1d(n, 256), 256, 0, st>>>(g, out, ld, pos, ct, stt, T, nrot, hd, ncols);
+  } else {
+    const long long n = (long long)T * ncols;
+    ls::rope_bwd_cast_kernel<<<grid1d(n, 256), 256, 0, st>>>(g, out, ld, pos, ct, stt, T, nrot, hd, ncols);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t gemm(int mode, const bf16* A, long long lda, int M, const uint8_t* Wp, const float* Wa, int Nw, int Kw,
                  const bf16* ext_a, const bf16* ext_b, int ext_k, int epi, void* out, long long ldo,
                  const bf16* residual, long long ldr, cudaStream_t st, ls::SkWorkspace sk = {}, int force_bn = 0,
@@ -571,9 +645,9 @@ cudaError_t attn_bwd(int hd, const bf16* qkv, long long ld, const bf16* dout, co
 
 cudaError_t lora_outer(const bf16* X, long long ldx, int ncols, const float* Uf, const bf16* Ub, int ldu, int r, int T,
                        int layout, int accumulate, float* scratch, int rows_per_chunk, float* out, cudaStream_t st) {
-  const int nch = (T + rows_per_chunk - 1) / rows_per_chunk;
-  dim3 g1((ncols + 127) / 128, nch);
-  ls::lora_outer_partial_kernel<<<g1, 256, 0, st>>>(X, ldx, ncols, Uf, Ub, ldu, T, rows_per_chunk, scratch);
+  const int nch = (int)(((long long)T + rows_per_chunk - 1) / rows_per_chunk);
+  dim3 g1((ncols + 63) / 64, nch);
+  ls::lora_outer_partial_kernel<<<g1, 256, 0, st>>>(X, ldx, ncols, Uf, Ub, ldu, r, T, rows_per_chunk, scratch);
   const int n = ncols * r;
   ls::lora_outer_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(scratch, nch, ncols, r, layout, accumulate, out);
   return cudaGetLastError();
@@ -587,7 +661,13 @@ constexpr int kLoraSplit = kLoraSplitMax;
 cudaError_t lora_proj(const bf16* X, long long ldx, int T, ls::LoraProjHalf h0, ls::LoraProjHalf h1, int r, float s,
                       float* out_f32, bf16* out_ext, float* scratch, cudaStream_t st) {
   const int ns = scratch ? kLoraSplit : 1;
-  ls::lora_proj_kernel<<<dim3((T + 15) / 16, ns), 256, 0, st>>>(X, ldx, T, h0, h1, r, s, out_f32, out_ext, scratch);
+  // 16-byte row reads when every half's columns allow them
+  auto v16 = [&](const ls::LoraProjHalf& h) { return !h.w || (h.xcol % 8 == 0 && h.K % 32 == 0); };
+  const dim3 grid((T + 15) / 16, ns);
+  if (ldx % 8 == 0 && (reinterpret_cast<uintptr_t>(X) & 15) == 0 && v16(h0) && v16(h1))
+    ls::lora_proj_kernel<true><<<grid, 256, 0, st>>>(X, ldx, T, h0, h1, r, s, out_f32, out_ext, scratch);
+  else
+    ls::lora_proj_kernel<false><<<grid, 256, 0, st>>>(X, ldx, T, h0, h1, r, s, out_f32, out_ext, scratch);
   if (ns > 1)
     ls::lora_proj_reduce_kernel<<<(T * 32 + 255) / 256, 256, 0, st>>>(scratch, ns, T, s, out_f32, out_ext);
   return cudaGetLastError();
@@ -807,8 +887,7 @@ int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16*
   cudaStream_t st = c->cs;
   const int H = c->H, I = c->I;
   const double TH = (double)T * H;
-  TIMED(LS_K_OTHER, 0, 4 * TH, 1,
-        ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(x_in, w.w1, c->n1, c->rstd1, T, H, c->cfg.eps));
+  GEMM_T(LS_K_OTHER, 0, 4 * TH, rmsnorm_fwd(x_in, w.w1, c->n1, c->rstd1, T, H, c->cfg.eps, st));
   const ls_ctx::Ad& a = c->ad[layer];
   const bool use = adapter && a.on;
   if (use) {
@@ -823,19 +902,14 @@ int layer_forward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, bf16*
   GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, c->nqkv, H, ek), gemm_bytes(0, T, c->nqkv, H, 2, false),
          gemm(ls::GEMM_FWD, c->n1, H, T, w.pqkv, w.aqkv, c->nqkv, H, c->u_ext, c->ext_fwd, ek, ls::EPI_BF16, c->qkv,
               c->nqkv, nullptr, 0, st, gemm_ws(c)));
-  {
-    const long long n = (long long)T * (c->nh + c->nkv) * (c->hd / 2);
-    TIMED(LS_K_OTHER, 0, 4.0 * n * 2, 1,
-          ls::rope_fwd_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->qkv, c->nqkv, c->pos, c->rope_cos, c->rope_sin, T,
-                                                              c->nh + c->nkv, c->hd));
-  }
+  GEMM_T(LS_K_OTHER, 0, 8.0 * T * (c->nh + c->nkv) * c->hd,
+         rope_fwd(c->qkv, c->nqkv, c->pos, c->rope_cos, c->rope_sin, T, c->nh + c->nkv, c->hd, st));
   GEMM_T(LS_K_ATTN_FWD, attn_flop(c, T, nseq), 2.0 * T * (c->nqkv + c->nq),
          attn_fwd(c->hd, c->qkv, c->nqkv, cu, nseq, c->maxlen, c->nh, c->nkv, c->attn_o, c->nq, c->lse_attn, T, st));
   GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, H, c->nq, 0), gemm_bytes(0, T, H, c->nq, 2, true),
          gemm(ls::GEMM_FWD, c->attn_o, c->nq, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->x1, H,
               x_in, H, st, gemm_ws(c)));
-  TIMED(LS_K_OTHER, 0, 4 * TH, 1,
-        ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->x1, w.w2, c->n2, c->rstd2, T, H, c->cfg.eps));
+  GEMM_T(LS_K_OTHER, 0, 4 * TH, rmsnorm_fwd(c->x1, w.w2, c->n2, c->rstd2, T, H, c->cfg.eps, st));
   GEMM_T(LS_K_GEMM_FWD, gemm_flop(0, T, 2 * I, H, 0), gemm_bytes(0, T, 2 * I, H, 2, false),
          gemm(ls::GEMM_FWD, c->n2, H, T, w.pgu, w.agu, 2 * I, H, nullptr, nullptr, 0, ls::EPI_BF16, c->gu, 2 * I,
               nullptr, 0, st, gemm_ws(c)));
@@ -872,8 +946,7 @@ int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int 
   GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, 2 * I, H, 0), gemm_bytes(1, T, 2 * I, H, 4, false),
          gemm(ls::GEMM_DX, c->dgu, 2 * I, T, w.pgu, w.agu, 2 * I, H, nullptr, nullptr, 0, ls::EPI_F32, c->dn, H,
               nullptr, 0, st, gemm_ws(c)));
-  TIMED(LS_K_OTHER, 0, 16 * TH, 1,
-        ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, c->x1, c->rstd2, w.w2, c->gx, c->gx_bf, T, H, 1));
+  GEMM_T(LS_K_OTHER, 0, 16 * TH, rmsnorm_bwd(c->dn, c->x1, c->rstd2, w.w2, c->gx, c->gx_bf, T, H, 1, st));
   // attention
   GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, H, c->nq, 0), gemm_bytes(1, T, H, c->nq, 2, false),
          gemm(ls::GEMM_DX, c->gx_bf, H, T, w.po, w.ao, H, c->nq, nullptr, nullptr, 0, ls::EPI_BF16, c->do_bf, c->nq,
@@ -882,13 +955,9 @@ int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int 
          attn_bwd(c->hd, c->qkv, c->nqkv, c->do_bf, c->attn_o, c->nq, c->lse_attn, cu, nseq, c->maxlen, c->nh,
                   c->nkv, c->Dattn, c->dqkv_f, c->nqkv, T, st, c->nh > c->nkv ? c->attn_part : nullptr));
   c->st.kernel_launches += c->nh > c->nkv ? 3 : 2;
-  {
-    const long long n = (long long)T * c->nqkv;
-    TIMED(LS_K_OTHER, 0, 6.0 * n, 1,
-          ls::rope_bwd_cast_kernel<<<grid1d(n, 256), 256, 0, st>>>(c->dqkv_f, c->dqkv_bf, c->nqkv, c->pos,
-                                                                  c->rope_cos, c->rope_sin, T, c->nh + c->nkv, c->hd,
-                                                                  c->nqkv));
-  }
+  GEMM_T(LS_K_OTHER, 0, 6.0 * T * c->nqkv,
+         rope_bwd_cast(c->dqkv_f, c->dqkv_bf, c->nqkv, c->pos, c->rope_cos, c->rope_sin, T, c->nh + c->nkv, c->hd,
+                       c->nqkv, st));
   const bool use = a.on;
   if (use) {
     const float s = c->cfg.lora_scale;
@@ -914,8 +983,7 @@ int layer_backward(ls_ctx* c, const LayerW& w, int layer, const bf16* x_in, int 
   GEMM_T(LS_K_GEMM_DX, gemm_flop(1, T, c->nqkv, H, ek), gemm_bytes(1, T, c->nqkv, H, 4, false),
          gemm(ls::GEMM_DX, c->dqkv_bf, c->nqkv, T, w.pqkv, w.aqkv, c->nqkv, H, c->du_ext, c->ext_bwd, ek, ls::EPI_F32,
               c->dn, H, nullptr, 0, st, gemm_ws(c)));
-  TIMED(LS_K_OTHER, 0, 16 * TH, 1,
-        ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dn, x_in, c->rstd1, w.w1, c->gx, c->gx_bf, T, H, 1));
+  GEMM_T(LS_K_OTHER, 0, 16 * TH, rmsnorm_bwd(c->dn, x_in, c->rstd1, w.w1, c->gx, c->gx_bf, T, H, 1, st));
   return LS_OK;
 }
 
@@ -1235,8 +1303,7 @@ int stream_step_fwd(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t nseq,
     const int ch = item - c->L;
     if (ch == 0) {
       const bf16* xL = save ? c->acts + (size_t)c->L * (size_t)c->Tmax * H : c->xping + (size_t)(c->L & 1) * TH;
-      TIMED(LS_K_OTHER, 0, 4.0 * T * H, 1,
-            ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(xL, c->wf, hf, rstdf, T, H, c->cfg.eps));
+      GEMM_T(LS_K_OTHER, 0, 4.0 * T * H, rmsnorm_fwd(xL, c->wf, hf, rstdf, T, H, c->cfg.eps, st));
     }
     const int v0 = ch * c->vrows;
     const int n = std::min(c->vrows, c->V - v0);
@@ -1307,6 +1374,7 @@ int stream_step_fwd_dpo(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t n
   }
   CK(cudaMemcpyAsync(x0 + TH, x0, TH * sizeof(bf16), cudaMemcpyDeviceToDevice, st));
   CK(cudaMemcpyAsync(c->acts, x0, TH * sizeof(bf16), cudaMemcpyDeviceToDevice, st));
+  if (c->ref_cap) CK(cudaMemcpyAsync(c->ref_cap, x0 + TH, TH * sizeof(bf16), cudaMemcpyDeviceToDevice, st));
   std::vector<int> items;
   for (int l = 0; l < c->L; ++l) items.push_back(l);
   for (int v = 0; v < c->nvch; ++v) items.push_back(c->L + v);
@@ -1320,14 +1388,15 @@ int stream_step_fwd_dpo(ls_ctx* c, const int32_t* d_tokens, int32_t T, int32_t n
       // the policy rows are the activation store entry of the next layer
       CK(cudaMemcpyAsync(c->acts + (size_t)(l + 1) * (size_t)c->Tmax * H, xout, TH * sizeof(bf16),
                          cudaMemcpyDeviceToDevice, st));
+      if (c->ref_cap)
+        CK(cudaMemcpyAsync(c->ref_cap + (size_t)(l + 1) * TH, xout + TH, TH * sizeof(bf16), cudaMemcpyDeviceToDevice,
+                           st));
       return LS_OK;
     }
     const int ch = item - c->L;
     if (ch == 0) {
       const bf16* xL = c->xping + (size_t)(c->L & 1) * T2H;
-      TIMED(LS_K_OTHER, 0, 4.0 * T2 * H, 1,
-            ls::rmsnorm_fwd_kernel<<<(T2 + 7) / 8, 256, 0, st>>>(xL, c->wf, c->hf_tmp, c->rstdf_tmp, T2, H,
-                                                                c->cfg.eps));
+      GEMM_T(LS_K_OTHER, 0, 4.0 * T2 * H, rmsnorm_fwd(xL, c->wf, c->hf_tmp, c->rstdf_tmp, T2, H, c->cfg.eps, st));
     }
     const int v0 = ch * c->vrows;
     const int n = std::min(c->vrows, c->V - v0);
@@ -1483,9 +1552,8 @@ int stream_step_bwd(ls_ctx* c, const float* d_coeffs) {
       first_chunk = false;
       if (ch == 0) {
         const bf16* xL = c->acts + (size_t)c->L * (size_t)c->Tmax * H;
-        TIMED(LS_K_OTHER, 0, 12.0 * T * H, 1,
-              ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, st>>>(c->dhf, xL, c->rstdf_save, c->wf, c->gx, c->gx_bf,
-                                                                 T, H, 0));
+        GEMM_T(LS_K_OTHER, 0, 12.0 * T * H,
+               rmsnorm_bwd(c->dhf, xL, c->rstdf_save, c->wf, c->gx, c->gx_bf, T, H, 0, st));
       }
       return LS_OK;
     }
@@ -1661,6 +1729,24 @@ int ls_read_activation(ls_ctx* c, int32_t layer, uint16_t* d_out) {
   return LS_OK;
 }
 
+int ls_capture_reference(ls_ctx* c, uint16_t* d_buf, uint64_t bytes) {
+  int rc = sticky(c);
+  if (rc) return rc;
+  if (!d_buf) {
+    c->ref_cap = nullptr;
+    c->ref_cap_bytes = 0;
+    return LS_OK;
+  }
+  if (!c->cfg.dpo_shared_read)
+    return fail(c, LS_ERR_STATE, "ls_capture_reference: context not planned with dpo_shared_read = 1");
+  const uint64_t need = (uint64_t)(c->L + 1) * (uint64_t)c->Tmax * (uint64_t)c->H * 2;
+  if (bytes < need || (reinterpret_cast<uintptr_t>(d_buf) & 15))
+    return fail(c, LS_ERR_ARG, "ls_capture_reference: buffer smaller than (L+1) * max_tokens * H bf16, or unaligned");
+  c->ref_cap = reinterpret_cast<bf16*>(d_buf);
+  c->ref_cap_bytes = bytes;
+  return LS_OK;
+}
+
 int ls_debug_copy_delay(ls_ctx* c, int32_t ms) {
   if (!c) return set_thread_err(LS_ERR_ARG, "null context");
   c->copy_delay_ms = ms > 0 ? ms : 0;
@@ -1776,9 +1862,8 @@ int lsk_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, float* rs
                     void* s) {
   if (!x || !w || !y || T < 0 || H <= 0 || H % 8) return set_thread_err(LS_ERR_ARG, "lsk_rmsnorm_fwd: bad args");
   if (T == 0) return LS_OK;
-  ls::rmsnorm_fwd_kernel<<<(T + 7) / 8, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(x), reinterpret_cast<const bf16*>(w),
-                                                            reinterpret_cast<bf16*>(y), rstd, T, H, eps);
-  KLAUNCH();
+  KCK(rmsnorm_fwd(reinterpret_cast<const bf16*>(x), reinterpret_cast<const bf16*>(w), reinterpret_cast<bf16*>(y),
+                  rstd, T, H, eps, STREAM(s)));
   return LS_OK;
 }
 
@@ -1786,10 +1871,8 @@ int lsk_rmsnorm_bwd(const float* dy, const uint16_t* x, const float* rstd, const
                     uint16_t* dx_bf16, int32_t T, int32_t H, int32_t accumulate, void* s) {
   if (!dy || !x || !rstd || !w || !dx || T < 0 || H <= 0 || H % 4) return set_thread_err(LS_ERR_ARG, "lsk_rmsnorm_bwd: bad args");
   if (T == 0) return LS_OK;
-  ls::rmsnorm_bwd_kernel<<<(T + 7) / 8, 256, 0, STREAM(s)>>>(dy, reinterpret_cast<const bf16*>(x), rstd,
-                                                            reinterpret_cast<const bf16*>(w), dx,
-                                                            reinterpret_cast<bf16*>(dx_bf16), T, H, accumulate);
-  KLAUNCH();
+  KCK(rmsnorm_bwd(dy, reinterpret_cast<const bf16*>(x), rstd, reinterpret_cast<const bf16*>(w), dx,
+                  reinterpret_cast<bf16*>(dx_bf16), T, H, accumulate, STREAM(s)));
   return LS_OK;
 }
 
@@ -1811,10 +1894,8 @@ int lsk_rope_fwd(uint16_t* qkv, int64_t ld, const int32_t* pos, const float* ct,
                  int32_t nheads, int32_t hd, void* s) {
   if (!qkv || !pos || !ct || !stt || T < 0 || nheads < 1 || hd % 2 || ld < (int64_t)nheads * hd)
     return set_thread_err(LS_ERR_ARG, "lsk_rope_fwd: bad args");
-  const long long n = (long long)T * nheads * (hd / 2);
-  if (n == 0) return LS_OK;
-  ls::rope_fwd_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(reinterpret_cast<bf16*>(qkv), ld, pos, ct, stt, T, nheads, hd);
-  KLAUNCH();
+  if ((long long)T * nheads * (hd / 2) == 0) return LS_OK;
+  KCK(rope_fwd(reinterpret_cast<bf16*>(qkv), ld, pos, ct, stt, T, nheads, hd, STREAM(s)));
   return LS_OK;
 }
 
@@ -1822,11 +1903,8 @@ int lsk_rope_bwd_cast(const float* g, uint16_t* out, int64_t ld, const int32_t* 
                       const float* stt, int32_t T, int32_t nrot, int32_t hd, int32_t ncols, void* s) {
   if (!g || !out || !pos || !ct || !stt || T < 0 || ncols > ld || nrot * hd > ncols)
     return set_thread_err(LS_ERR_ARG, "lsk_rope_bwd_cast: bad args");
-  const long long n = (long long)T * ncols;
-  if (n == 0) return LS_OK;
-  ls::rope_bwd_cast_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(g, reinterpret_cast<bf16*>(out), ld, pos, ct, stt, T,
-                                                                  nrot, hd, ncols);
-  KLAUNCH();
+  if ((long long)T * ncols == 0) return LS_OK;
+  KCK(rope_bwd_cast(g, reinterpret_cast<bf16*>(out), ld, pos, ct, stt, T, nrot, hd, ncols, STREAM(s)));
   return LS_OK;
 }
 
@@ -1895,7 +1973,8 @@ int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* u
                    int32_t r, int32_t T, int32_t layout, int32_t accumulate, float* scratch, int32_t rpc, float* out,
                    void* s) {
   if (!X || (!uf && !ub) || !scratch || !out || r < 1 || r > 16 || ncols < 1 || ncols % 8 || ldx % 8 ||
-      (reinterpret_cast<uintptr_t>(X) & 15) || T < 1 || rpc < 1 || (layout != 0 && layout != 1))
+      ldx < ncols || ldu < r || (reinterpret_cast<uintptr_t>(X) & 15) || T < 1 || rpc < 1 ||
+      (layout != 0 && layout != 1) || ((long long)T + rpc - 1) / rpc > 65535)
     return set_thread_err(LS_ERR_ARG, "lsk_lora_outer: bad args");
   KCK(lora_outer(reinterpret_cast<const bf16*>(X), ldx, ncols, uf, reinterpret_cast<const bf16*>(ub), ldu, r, T,
                  layout, accumulate, scratch, rpc, out, STREAM(s)));
@@ -1920,10 +1999,11 @@ extern "C" {
 int lsk_lora_outer_noalloc(const uint16_t* X, int64_t ldx, int32_t ncols, const float* uf, const uint16_t* ub,
                            int32_t ldu, int32_t r, int32_t T, int32_t layout, int32_t accumulate, int32_t rpc,
                            float* out, void* s) {
-  if (!X || (!uf && !ub) || !out || r < 1 || r > 16 || ncols < 1 || ncols % 8 || ldx % 8 ||
-      (reinterpret_cast<uintptr_t>(X) & 15) || T < 1 || rpc < 1 || (layout != 0 && layout != 1))
+  if (!X || (!uf && !ub) || !out || r < 1 || r > 16 || ncols < 1 || ncols % 8 || ldx % 8 || ldx < ncols ||
+      ldu < r || (reinterpret_cast<uintptr_t>(X) & 15) || T < 1 || rpc < 1 || (layout != 0 && layout != 1) ||
+      ((long long)T + rpc - 1) / rpc > 65535)
     return set_thread_err(LS_ERR_ARG, "lsk_lora_outer_noalloc: bad args");
-  const long long need = (long long)((T + rpc - 1) / rpc) * ncols * 16;
+  const long long need = (((long long)T + rpc - 1) / rpc) * (long long)ncols * 16;
   if (need > (long long)LS_OUTER_NOALLOC_SCRATCH_FLOATS) {
     char b[200];
     snprintf(b, sizeof b, "lsk_lora_outer_noalloc: needs %lld scratch floats (ceil(T/rows_per_chunk)*ncols*16), "

@@ -90,6 +90,115 @@ __global__ void rmsnorm_bwd_kernel(const float* __restrict__ dy, const __nv_bflo
   }
 }
 
+// Row-per-block forms of the two RMSNorm kernels above (same formulas).  With one warp
+// per row, T = 1024 rows put only 7 warps on an SM; here a block of 4 (forward) or 8
+// (backward) warps takes one row and keeps its slice of the row in registers, so x and
+// dy are read from memory once and every SM has tens of warps in flight.  Thread i
+// holds the 16-byte (forward: 8 bf16) or float4 (backward) chunks i, i + blockDim, ...
+// (VPT of them, guarded by the row length); the sums run per thread in chunk order, then
+// a warp butterfly, then the warps in order: fixed, so results do not depend on
+// scheduling.
+__device__ __forceinline__ float block_sum_ordered(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int i = 0; i < nw; ++i) t += red[i];
+  return t;
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(128) rmsnorm_fwd_row_kernel(const __nv_bfloat16* __restrict__ x,
+                                                              const __nv_bfloat16* __restrict__ w,
+                                                              __nv_bfloat16* __restrict__ y, float* __restrict__ rstd,
+                                                              int H, float eps) {
+  __shared__ float red[4];
+  const int row = blockIdx.x;
+  const int nv = H >> 3;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * H);
+  uint4 xv[VPT];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * 128;
+    xv[i] = v < nv ? xr[v] : make_uint4(0, 0, 0, 0);
+    const uint32_t q[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = bf16lo(q[e]), b = bf16hi(q[e]);
+      ss += a * a;
+      ss += b * b;
+    }
+  }
+  ss = block_sum_ordered(ss, red);
+  const float r = 1.0f / sqrtf(ss / (float)H + eps);
+  if (threadIdx.x == 0 && rstd) rstd[row] = r;
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * H);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * 128;
+    if (v >= nv) continue;
+    const uint4 wv = wr[v];
+    const uint32_t q[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float n0 = __bfloat162float(__float2bfloat16_rn(bf16lo(q[e]) * r));
+      const float n1 = __bfloat162float(__float2bfloat16_rn(bf16hi(q[e]) * r));
+      o[e] = pack_bf16x2(bf16lo(ww[e]) * n0, bf16hi(ww[e]) * n1);
+    }
+    yr[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_row_kernel(const float* __restrict__ dy,
+                                                              const __nv_bfloat16* __restrict__ x,
+                                                              const float* __restrict__ rstd,
+                                                              const __nv_bfloat16* __restrict__ w,
+                                                              float* __restrict__ dx, __nv_bfloat16* __restrict__ dx_bf16,
+                                                              int H, int accumulate) {
+  __shared__ float red[8];
+  const int row = blockIdx.x;
+  const float r = rstd[row];
+  const int nv = H >> 2;
+  const float4* dyr = reinterpret_cast<const float4*>(dy + (size_t)row * H);
+  const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)row * H);
+  const uint2* wr = reinterpret_cast<const uint2*>(w);
+  float4 d[VPT];
+  uint2 xv[VPT], wv[VPT];
+  float dot = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * 256;
+    const bool ok = v < nv;
+    d[i] = ok ? dyr[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+    xv[i] = ok ? xr[v] : make_uint2(0, 0);
+    wv[i] = ok ? wr[v] : make_uint2(0, 0);
+    dot += d[i].x * bf16lo(wv[i].x) * (bf16lo(xv[i].x) * r);
+    dot += d[i].y * bf16hi(wv[i].x) * (bf16hi(xv[i].x) * r);
+    dot += d[i].z * bf16lo(wv[i].y) * (bf16lo(xv[i].y) * r);
+    dot += d[i].w * bf16hi(wv[i].y) * (bf16hi(xv[i].y) * r);
+  }
+  const float c = block_sum_ordered(dot, red) / (float)H;
+  float4* dxr = reinterpret_cast<float4*>(dx + (size_t)row * H);
+  uint2* db = dx_bf16 ? reinterpret_cast<uint2*>(dx_bf16 + (size_t)row * H) : nullptr;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int v = threadIdx.x + i * 256;
+    if (v >= nv) continue;
+    float4 o = accumulate ? dxr[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+    o.x += r * (d[i].x * bf16lo(wv[i].x) - bf16lo(xv[i].x) * r * c);
+    o.y += r * (d[i].y * bf16hi(wv[i].x) - bf16hi(xv[i].x) * r * c);
+    o.z += r * (d[i].z * bf16lo(wv[i].y) - bf16lo(xv[i].y) * r * c);
+    o.w += r * (d[i].w * bf16hi(wv[i].y) - bf16hi(xv[i].y) * r * c);
+    dxr[v] = o;
+    if (db) db[v] = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
+  }
+}
+
 // ------------------------------------------------------------------ RoPE
 // In place on the q and k heads of qkv [T, ld] (bf16): pair (i, i + hd/2) turned by
 // the angle pos * theta^(-2i/hd); cos/sin come from a [max_pos, hd/2] fp32 table.
@@ -138,6 +247,80 @@ __global__ void rope_bwd_cast_kernel(const float* __restrict__ g, __nv_bfloat16*
       v = gr[col];
     }
     out[(size_t)t * ld + col] = __float2bfloat16_rn(v);
+  }
+}
+
+// 16-byte forms of the two RoPE kernels (same arithmetic, element for element): a
+// thread turns 8 consecutive pairs (i .. i+7, i+hd/2 .. i+hd/2+7) of one head, with
+// 16-byte loads and stores of q/k and 2 x float4 table reads.  hd/2 must be a multiple
+// of 8 (hd 64 and 128 are).
+__global__ void rope_fwd_vec_kernel(__nv_bfloat16* __restrict__ qkv, long long ld, const int* __restrict__ pos,
+                                    const float* __restrict__ cs, const float* __restrict__ sn, int T, int nheads,
+                                    int hd) {
+  const int half = hd >> 1, g8 = half >> 3;
+  const long long total = (long long)T * nheads * g8;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int i0 = (int)(idx % g8) * 8;
+    const long long th = idx / g8;
+    const int h = (int)(th % nheads);
+    const int t = (int)(th / nheads);
+    __nv_bfloat16* p = qkv + (size_t)t * ld + (size_t)h * hd;
+    const size_t tb = (size_t)pos[t] * half + i0;
+    const float4 c0 = *reinterpret_cast<const float4*>(cs + tb), c1 = *reinterpret_cast<const float4*>(cs + tb + 4);
+    const float4 s0 = *reinterpret_cast<const float4*>(sn + tb), s1 = *reinterpret_cast<const float4*>(sn + tb + 4);
+    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    const uint4 a = *reinterpret_cast<const uint4*>(p + i0), b = *reinterpret_cast<const uint4*>(p + i0 + half);
+    const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x1l = bf16lo(aa[e]), x1h = bf16hi(aa[e]), x2l = bf16lo(bb[e]), x2h = bf16hi(bb[e]);
+      const int k = 2 * e;
+      oa[e] = pack_bf16x2(x1l * c[k] - x2l * sv[k], x1h * c[k + 1] - x2h * sv[k + 1]);
+      ob[e] = pack_bf16x2(x2l * c[k] + x1l * sv[k], x2h * c[k + 1] + x1h * sv[k + 1]);
+    }
+    *reinterpret_cast<uint4*>(p + i0) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *reinterpret_cast<uint4*>(p + i0 + half) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  }
+}
+
+// Backward: a thread takes 4 consecutive pairs of one rotated head (float4 reads of
+// both halves, two 8-byte bf16 stores), or 8 consecutive unrotated columns.
+__global__ void rope_bwd_cast_vec_kernel(const float* __restrict__ g, __nv_bfloat16* __restrict__ out, long long ld,
+                                         const int* __restrict__ pos, const float* __restrict__ cs,
+                                         const float* __restrict__ sn, int T, int nrot_heads, int hd, int ncols) {
+  const int half = hd >> 1;
+  const int rot_units = nrot_heads * (half >> 2);        // 4-pair units of the rotated heads
+  const int plain_units = (ncols - nrot_heads * hd) >> 3;  // 8-column units of the rest
+  const int units = rot_units + plain_units;
+  const long long total = (long long)T * units;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int u = (int)(idx % units);
+    const int t = (int)(idx / units);
+    const float* gr = g + (size_t)t * ld;
+    __nv_bfloat16* orow = out + (size_t)t * ld;
+    if (u < rot_units) {
+      const int h = u / (half >> 2), i0 = (u % (half >> 2)) * 4;
+      const int base = h * hd;
+      const size_t tb = (size_t)pos[t] * half + i0;
+      const float4 c = *reinterpret_cast<const float4*>(cs + tb), s = *reinterpret_cast<const float4*>(sn + tb);
+      const float4 y1 = *reinterpret_cast<const float4*>(gr + base + i0);
+      const float4 y2 = *reinterpret_cast<const float4*>(gr + base + i0 + half);
+      *reinterpret_cast<uint2*>(orow + base + i0) =
+          make_uint2(pack_bf16x2(y1.x * c.x + y2.x * s.x, y1.y * c.y + y2.y * s.y),
+                     pack_bf16x2(y1.z * c.z + y2.z * s.z, y1.w * c.w + y2.w * s.w));
+      *reinterpret_cast<uint2*>(orow + base + i0 + half) =
+          make_uint2(pack_bf16x2(y2.x * c.x - y1.x * s.x, y2.y * c.y - y1.y * s.y),
+                     pack_bf16x2(y2.z * c.z - y1.z * s.z, y2.w * c.w - y1.w * s.w));
+    } else {
+      const int col = nrot_heads * hd + (u - rot_units) * 8;
+      const float4 a = *reinterpret_cast<const float4*>(gr + col), b = *reinterpret_cast<const float4*>(gr + col + 4);
+      *reinterpret_cast<uint4*>(orow + col) = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                                         pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+    }
   }
 }
 
@@ -470,6 +653,12 @@ __device__ __forceinline__ uint32_t lora_w_pair(const LoraProjHalf& h, int n, in
 // blockIdx.y / gridDim.y selects a slice of K (fixed split); with gridDim.y > 1 the
 // block writes its unscaled partial sums to part [gridDim.y][T][32] for
 // lora_proj_reduce_kernel instead of the outputs.
+// V16: rows are read 16 bytes per lane (X 16-byte aligned, ldx and the column offsets
+// multiples of 8, K a multiple of 32): lane (g, q) loads columns 8q .. 8q+7 of a 32-wide
+// step for rows g and g + 8, and the two m16n8k16 MMAs of the step take them as their
+// k positions in the order (8q, 8q+1 | 8q+2, 8q+3) and (8q+4, 8q+5 | 8q+6, 8q+7); B is
+// read with the same assignment, so each MMA still sums matching X and W columns.
+template <bool V16>
 __global__ void __launch_bounds__(256) lora_proj_kernel(const __nv_bfloat16* __restrict__ X, long long ldx, int T,
                                                         LoraProjHalf h0, LoraProjHalf h1, int r, float s,
                                                         float* __restrict__ out_f32,
@@ -489,24 +678,44 @@ __global__ void __launch_bounds__(256) lora_proj_kernel(const __nv_bfloat16* __r
   for (int hh = 0; hh < 2; ++hh) {
     const LoraProjHalf& h = hh ? h1 : h0;
     if (!h.w) continue;
-    const int ksteps = h.K >> 4;
-    const int wper = (ksteps + nsplit * 8 - 1) / (nsplit * 8);   // k-steps per warp
-    const int kb = (split * 8 + warp) * wper, ke = min(ksteps, kb + wper);
-#pragma unroll 4
-    for (int ks = kb; ks < ke; ++ks) {
-      const int k0 = ks << 4;
-      const int xc = h.xcol + k0 + 2 * cq;
-      uint32_t a[4];
-      a[0] = ok0 ? *reinterpret_cast<const uint32_t*>(x0 + xc) : 0u;
-      a[1] = ok1 ? *reinterpret_cast<const uint32_t*>(x1 + xc) : 0u;
-      a[2] = ok0 ? *reinterpret_cast<const uint32_t*>(x0 + xc + 8) : 0u;
-      a[3] = ok1 ? *reinterpret_cast<const uint32_t*>(x1 + xc + 8) : 0u;
+    if constexpr (V16) {
+      const int ksteps = h.K >> 5;
+      const int wper = (ksteps + nsplit * 8 - 1) / (nsplit * 8);   // 32-wide k-steps per warp
+      const int kb = (split * 8 + warp) * wper, ke = min(ksteps, kb + wper);
+#pragma unroll 2
+      for (int ks = kb; ks < ke; ++ks) {
+        const int kc = (ks << 5) + 8 * cq;
+        const int xc = h.xcol + kc;
+        const uint4 A0 = ok0 ? *reinterpret_cast<const uint4*>(x0 + xc) : make_uint4(0, 0, 0, 0);
+        const uint4 A1 = ok1 ? *reinterpret_cast<const uint4*>(x1 + xc) : make_uint4(0, 0, 0, 0);
+        const uint32_t a0[4] = {A0.x, A1.x, A0.y, A1.y}, a1[4] = {A0.z, A1.z, A0.w, A1.w};
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int n = nt * 8 + g;
-        const uint32_t b0 = lora_w_pair(h, n, k0 + 2 * cq, r);
-        const uint32_t b1 = lora_w_pair(h, n, k0 + 8 + 2 * cq, r);
-        mma_16816_bf16(acc[hh][nt], a, b0, b1);
+        for (int nt = 0; nt < 2; ++nt) {
+          const int n = nt * 8 + g;
+          mma_16816_bf16(acc[hh][nt], a0, lora_w_pair(h, n, kc, r), lora_w_pair(h, n, kc + 2, r));
+          mma_16816_bf16(acc[hh][nt], a1, lora_w_pair(h, n, kc + 4, r), lora_w_pair(h, n, kc + 6, r));
+        }
+      }
+    } else {
+      const int ksteps = h.K >> 4;
+      const int wper = (ksteps + nsplit * 8 - 1) / (nsplit * 8);   // k-steps per warp
+      const int kb = (split * 8 + warp) * wper, ke = min(ksteps, kb + wper);
+#pragma unroll 4
+      for (int ks = kb; ks < ke; ++ks) {
+        const int k0 = ks << 4;
+        const int xc = h.xcol + k0 + 2 * cq;
+        uint32_t a[4];
+        a[0] = ok0 ? *reinterpret_cast<const uint32_t*>(x0 + xc) : 0u;
+        a[1] = ok1 ? *reinterpret_cast<const uint32_t*>(x1 + xc) : 0u;
+        a[2] = ok0 ? *reinterpret_cast<const uint32_t*>(x0 + xc + 8) : 0u;
+        a[3] = ok1 ? *reinterpret_cast<const uint32_t*>(x1 + xc + 8) : 0u;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int n = nt * 8 + g;
+          const uint32_t b0 = lora_w_pair(h, n, k0 + 2 * cq, r);
+          const uint32_t b1 = lora_w_pair(h, n, k0 + 8 + 2 * cq, r);
+          mma_16816_bf16(acc[hh][nt], a, b0, b1);
+        }
       }
     }
   }
@@ -561,54 +770,66 @@ __global__ void lora_proj_reduce_kernel(const float* __restrict__ part, int nspl
 // Partial outer products over a slice of rows (the LoRA weight gradients dB = dY^T u
 // and dA = du^T x, reduced over tokens without atomics):
 //   part[chunk][c][j] = sum_{t in chunk} X[t, c] * U[t, j]     (c < ncols, j < 16)
-// X bf16 [T, ldx] (16-byte aligned rows, ncols % 8 == 0); U fp32 or bf16 [T, ldu].
-// A block takes 128 columns of one chunk; 32-row tiles of X and U are staged in shared
-// memory with 16-byte loads; thread (c, j-half) accumulates 8 sums in row order.
+// X bf16 [T, ldx] (16-byte aligned rows, ncols % 8 == 0); U fp32 or bf16 [T, ldu], of
+// which only the first r columns are read (the sums of columns r..15 are zero).
+// A block takes a 64-column strip of one chunk of rows, in sub-tiles of up to 128 rows:
+// all of a sub-tile's loads (16 KB of X in 16-byte pieces, its U rows) are issued before
+// any is used, then staged in shared memory; thread (column, j-quarter) adds its 4 sums
+// in row order.  The many small blocks (64 columns x 128 rows each) keep every SM's
+// memory pipe busy; each sum is still a fixed-order walk over the chunk's rows.
 __global__ void __launch_bounds__(256) lora_outer_partial_kernel(const __nv_bfloat16* __restrict__ X, long long ldx,
                                                                  int ncols, const float* __restrict__ Uf,
-                                                                 const __nv_bfloat16* __restrict__ Ub, int ldu, int T,
-                                                                 int rows_per_chunk, float* __restrict__ part) {
-  __shared__ __align__(16) __nv_bfloat16 xs[32][128];
-  __shared__ __align__(16) float us[32][16];
-  const int c0 = blockIdx.x * 128;
+                                                                 const __nv_bfloat16* __restrict__ Ub, int ldu, int r,
+                                                                 int T, int rows_per_chunk, float* __restrict__ part) {
+  __shared__ __align__(16) __nv_bfloat16 xs[128][64];
+  __shared__ __align__(16) float us[128][16];
+  const int c0 = blockIdx.x * 64;
   const int chunk = blockIdx.y;
   const int t0 = chunk * rows_per_chunk, t1 = min(T, t0 + rows_per_chunk);
-  const int cl = threadIdx.x & 127, jh = threadIdx.x >> 7;
-  float acc[8];
+  const int cl = threadIdx.x & 63, jq = threadIdx.x >> 6;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int tb = t0; tb < t1; tb += 128) {
+    const int nt = min(128, t1 - tb);
+    uint4 xv[4];
+    float uv[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-  for (int tb = t0; tb < t1; tb += 32) {
-    const int nt = min(32, t1 - tb);
-    __syncthreads();
-    for (int e = threadIdx.x; e < 32 * 16; e += 256) {
-      const int tt = e >> 4, v = e & 15;
-      const int col = c0 + v * 8;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (tt < nt && col < ncols) val = *reinterpret_cast<const uint4*>(X + (size_t)(tb + tt) * ldx + col);
-      *reinterpret_cast<uint4*>(&xs[tt][v * 8]) = val;
+    for (int i = 0; i < 4; ++i) {
+      const int e = threadIdx.x + i * 256, tt = e >> 3, col = c0 + (e & 7) * 8;
+      xv[i] = (tt < nt && col < ncols) ? *reinterpret_cast<const uint4*>(X + (size_t)(tb + tt) * ldx + col)
+                                       : make_uint4(0, 0, 0, 0);
     }
-    for (int e = threadIdx.x; e < 32 * 16; e += 256) {
-      const int tt = e >> 4, j = e & 15;
-      float v = 0.f;
-      if (tt < nt) v = Uf ? Uf[(size_t)(tb + tt) * ldu + j] : bf2f(Ub[(size_t)(tb + tt) * ldu + j]);
-      us[tt][j] = v;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = threadIdx.x + i * 256, tt = e >> 4, j = e & 15;
+      uv[i] = 0.f;
+      if (tt < nt && j < r) uv[i] = Uf ? Uf[(size_t)(tb + tt) * ldu + j] : bf2f(Ub[(size_t)(tb + tt) * ldu + j]);
+    }
+    __syncthreads();   // the previous sub-tile's readers are done
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = threadIdx.x + i * 256;
+      *reinterpret_cast<uint4*>(&xs[e >> 3][(e & 7) * 8]) = xv[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = threadIdx.x + i * 256;
+      us[e >> 4][e & 15] = uv[i];
     }
     __syncthreads();
 #pragma unroll 8
-    for (int tt = 0; tt < 32; ++tt) {
-      const float xv = bf2f(xs[tt][cl]);
-      const float4 ua = *reinterpret_cast<const float4*>(&us[tt][jh * 8]);
-      const float4 ub = *reinterpret_cast<const float4*>(&us[tt][jh * 8 + 4]);
-      acc[0] += xv * ua.x; acc[1] += xv * ua.y; acc[2] += xv * ua.z; acc[3] += xv * ua.w;
-      acc[4] += xv * ub.x; acc[5] += xv * ub.y; acc[6] += xv * ub.z; acc[7] += xv * ub.w;
+    for (int tt = 0; tt < nt; ++tt) {
+      const float x = bf2f(xs[tt][cl]);
+      const float4 u = *reinterpret_cast<const float4*>(&us[tt][jq * 4]);
+      acc[0] += x * u.x;
+      acc[1] += x * u.y;
+      acc[2] += x * u.z;
+      acc[3] += x * u.w;
     }
   }
   const int c = c0 + cl;
-  if (c < ncols) {
-    float* pp = part + ((size_t)chunk * ncols + c) * 16 + jh * 8;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) pp[j] = acc[j];
-  }
+  if (c < ncols)
+    *reinterpret_cast<float4*>(part + ((size_t)chunk * ncols + c) * 16 + jq * 4) =
+        make_float4(acc[0], acc[1], acc[2], acc[3]);
 }
 
 // out (+)= sum over chunks, in chunk order.  layout 0: out[c * r + j] (B-shaped [ncols, r]);

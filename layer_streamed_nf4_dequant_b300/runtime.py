@@ -350,6 +350,19 @@ class Stack:
         check(lib().ls_read_activation(self.ctx, layer, out.data_ptr()), self.ctx)
         return out
 
+    def capture_reference(self, on: bool = True) -> Optional[torch.Tensor]:
+        """Keep the reference rows of every activation-store entry of later shared-read
+        forwards in a device buffer [(L+1), max_tokens, H] bf16 (ls_capture_reference);
+        entry l of a T-token step is buffer.view(-1)[l*T*H:(l+1)*T*H].  on=False stops."""
+        if not on:
+            check(lib().ls_capture_reference(self.ctx, None, 0), self.ctx)
+            self.ref_capture = None
+            return None
+        n = (self.s.layers + 1) * self.cfg.max_tokens * self.s.hidden
+        self.ref_capture = torch.empty(n, dtype=torch.bfloat16, device=self.dev)
+        check(lib().ls_capture_reference(self.ctx, self.ref_capture.data_ptr(), 2 * n), self.ctx)
+        return self.ref_capture
+
     @_stream_ordered
     def bwd(self, coeffs: torch.Tensor):
         check(lib().stream_step_bwd(self.ctx, coeffs.data_ptr()), self.ctx)

@@ -11,35 +11,58 @@ import bench
 import synth
 
 
+def _roof(s, reads_l, reads_v, shared, tflops, link, nvch=4, layer_b=122.7e6):
+    vb = s.vocab * s.hidden * 0.5625 / nvch
+    k = {"layer_reads": reads_l, "vocab_reads": reads_v, "h2d_bytes": reads_l * layer_b + reads_v * vb}
+    return bench.link_roofline_ms(s, s.tokens, s.seq_len, s.nseq, k, layer_b, vb, nvch, tflops, link, shared), vb
+
+
 def test_step_roofline_is_link_bound_for_a_slow_link():
     s = synth.LLAMA_8B
     layer_b = 122.7e6
-    r = bench.step_roofline_ms(s, {"slot_bytes_layer": layer_b}, s.tokens, s.nseq, s.seq_len, "dpo",
-                               tflops=1e9, link_gbs=1.0)
-    vocab_b = s.vocab * s.hidden * 0.5625
-    # three sweeps of the layers, three reads of the vocabulary head, all at 1 GB/s
-    want = (3 * s.layers * layer_b + 3 * vocab_b) / 1e9 * 1e3
+    # two forward sweeps and the backward, every use a copy, all at 1 GB/s
+    r, vb = _roof(s, 3 * s.layers, 3 * 4, False, tflops=1e9, link=1.0, layer_b=layer_b)
+    want = (3 * s.layers * layer_b + 3 * 4 * vb) / 1e9 * 1e3
     assert r["ms"] == pytest.approx(want, rel=1e-9)
+    assert r["link_ms"] == pytest.approx(want, rel=1e-9)
 
 
 def test_step_roofline_shared_read_saves_one_sweep():
     s = synth.LLAMA_8B
     layer_b = 122.7e6
-    two = bench.step_roofline_ms(s, {"slot_bytes_layer": layer_b}, s.tokens, s.nseq, s.seq_len, "dpo", 1e9, 1.0)
-    one = bench.step_roofline_ms(s, {"slot_bytes_layer": layer_b}, s.tokens, s.nseq, s.seq_len, "dpo", 1e9, 1.0,
-                                 shared_read=True)
-    vocab_b = s.vocab * s.hidden * 0.5625
-    assert two["ms"] - one["ms"] == pytest.approx((s.layers * layer_b + vocab_b) / 1e9 * 1e3, rel=1e-9)
+    two, vb = _roof(s, 3 * s.layers, 12, False, 1e9, 1.0, layer_b=layer_b)
+    one, _ = _roof(s, 2 * s.layers, 8, True, 1e9, 1.0, layer_b=layer_b)
+    assert two["ms"] - one["ms"] == pytest.approx((s.layers * layer_b + 4 * vb) / 1e9 * 1e3, rel=1e-9)
     assert one["flop"] == pytest.approx(two["flop"], rel=1e-12)
 
 
+def test_step_roofline_reuse_saves_the_copy_not_the_compute():
+    """An item still in a slot at the turnaround costs its FLOPs, not its bytes."""
+    s = synth.LLAMA_8B
+    full, vb = _roof(s, 2 * s.layers, 8, True, 1000.0, 50.0)
+    reuse, _ = _roof(s, 2 * s.layers - 2, 6, True, 1000.0, 50.0)
+    saved = full["ms"] - reuse["ms"]
+    assert 0 < saved < (2 * 122.7e6 + 2 * vb) / 50e9 * 1e3
+    # and the bound never exceeds the bytes moved at the link rate plus all compute at peak
+    assert reuse["ms"] <= reuse["link_ms"] + reuse["compute_ms"]
+    assert reuse["ms"] >= max(reuse["link_ms"], reuse["compute_ms"]) - 1e-9
+
+
 def test_step_roofline_is_tensor_bound_for_an_infinite_link():
-    s = synth.QWEN_3B
-    r = bench.step_roofline_ms(s, {"slot_bytes_layer": 43.4e6}, s.tokens, s.nseq, s.seq_len, "sft",
-                               tflops=1000.0, link_gbs=1e12)
-    assert r["ms"] == pytest.approx(r["flop"] / 1e15 * 1e3, rel=1e-9)
+    s = synth.QWEN_3B.with_(method="sft")
+    nvch = 2
+    vb = s.vocab * s.hidden * 0.5625 / nvch
+    k = {"layer_reads": 2 * s.layers, "vocab_reads": 2 * nvch, "h2d_bytes": 0.0}
+    r = bench.link_roofline_ms(s, s.tokens, s.seq_len, s.nseq, k, 43.4e6, vb, nvch, 1000.0, 1e12, False)
+    assert r["ms"] == pytest.approx(r["flop"] / 1e15 * 1e3, rel=1e-6)
     # forward 2 T P per layer dominates: the step is at least 4 T P L FLOPs (fwd + dX)
     assert r["flop"] >= 4 * s.tokens * bench.layer_params(s) * s.layers
+
+
+def test_pcie_spec_rates():
+    assert bench.pcie_spec_gbs(5, 16) == pytest.approx(63.02, rel=1e-3)
+    assert bench.pcie_spec_gbs(6, 16) == pytest.approx(121.0, rel=1e-3)
+    assert bench.pcie_spec_gbs(4, 8) == pytest.approx(15.75, rel=1e-3)
 
 
 def test_layer_params_match_the_8b_shape():

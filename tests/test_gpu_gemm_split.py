@@ -10,6 +10,7 @@ multiple of the SM count (whole tiles only, persistent).  Tolerance as the other
 tests: normwise relative error <= 1e-2 against the fp64 oracle.
 """
 import ctypes
+import math
 
 import numpy as np
 import pytest
@@ -200,6 +201,44 @@ def test_paired_halves_round_identically(T, N, K, ext):
         lora = (om.t64(np.asarray(to_np(ext_a[:T]))), om.t64(np.asarray(to_np(ext_b))))
     want = om.linear(om.t64(x), om.t64(wd), lora=lora, residual=om.t64(res)).numpy()
     assert rel_err(to_np(out[:T]), want) <= TOL
+    _check_device_error()
+
+
+@pytest.mark.parametrize("T,N,K,ext", [(1024, 6144, 4096, 32), (1024, 28672, 4096, 0), (1024, 4096, 14336, 0),
+                                       (300, 640, 1024, 16)])
+def test_paired_halves_differ_and_match_whole_tiles(T, N, K, ext):
+    """A paired batch [X; Y] with different halves (the shared-read forward's policy and
+    reference rows once the adapter has moved them apart): each half must be its own
+    product.  Against whole tiles of the same batch the paired split differs only in
+    fp32 summation order; against the oracle each half is within the product bound."""
+    x = synth.gaussian((2 * T, K), 47, T, K)
+    w = _w(N, K, seed=48)
+    p, a, _, _ = nf4_dev(w)
+    wd = _deq(w)
+    xd = bf16_dev(x)
+    ext_a = ext_b = None
+    u = b = None
+    if ext:
+        u = synth.gaussian((2 * T, 64), 49, T) * (np.arange(64) < ext)
+        b = synth.gaussian((N, 64), 50, N) * (np.arange(64) < ext) * 0.05
+        ext_a, ext_b = bf16_dev(u), bf16_dev(b)
+    paired = torch.empty((2 * T, N), dtype=torch.float32, device=DEV)
+    whole = torch.empty((2 * T, N), dtype=torch.float32, device=DEV)
+    _sk(0, xd, 2 * T, p, a, N, K, ext_a, ext_b, ext, 1, paired, N, None, 1, pair_rows=T)
+    _sk(0, xd, 2 * T, p, a, N, K, ext_a, ext_b, ext, 1, whole, N, None, -1)
+    torch.cuda.synchronize()
+    ref = whole.double()
+    scale = ref.abs().max().item()
+    # two fp32 summation orders of K products: their difference walks like sqrt(K) unit
+    # roundoffs of the running sum (8x room)
+    assert (paired.double() - ref).abs().max().item() <= 8 * math.sqrt(K) * 2.0 ** -24 * scale
+    rows = np.array([0, 1, T - 1, T, T + 1, 2 * T - 1, T // 2, T + T // 2])
+    xr = bf16_dev(x[rows]).float().cpu().numpy()
+    lora = None
+    if ext:
+        lora = (om.t64(to_np(ext_a)[rows]), om.t64(to_np(ext_b)))
+    want = om.linear(om.t64(xr), om.t64(wd), lora=lora).numpy()
+    assert rel_err(to_np(paired)[rows], want) <= TOL
     _check_device_error()
 
 

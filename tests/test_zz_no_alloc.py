@@ -5,9 +5,10 @@ running inside another framework's memory pool, or on paths that must not take
 cudaMalloc's implicit synchronisation): it keeps its partial sums in a fixed array
 inside the library instead of caller scratch.  These tests call it through the C ABI
 and check it against the scratch-taking lsk_lora_outer on the same inputs, twice in a
-row with different inputs (the shared array keeps the previous call's contents), and
-check that an oversized request is refused before anything is launched.  This file is
-collected last so that a failure here cannot hide any other test.
+row with different inputs (the shared array keeps the previous call's contents).  Both
+run the same kernels over the same chunks in the same order, so the results must be
+equal bit for bit.  An oversized request must be refused before anything is launched.
+This file is collected last so that a failure here cannot hide any other test.
 """
 import math
 
@@ -46,14 +47,14 @@ def test_noalloc_outer_matches_scratch_version_two_calls_in_a_row():
     X1 = bf16_dev(synth.gaussian((T1, n1), 40, 1))
     U1 = torch.from_numpy(synth.gaussian_f32((T1, 32), 41, 1)).to(DEV)
     want1, got1 = _outer_both(X1, n1, U1, None, 32, r, T1, 1, 0, 128, 42)
-    assert rel_err(to_np(got1), to_np(want1)) <= TOL
+    assert torch.equal(got1, want1)
     # call 2 right after: dB shape (ncols x r) from bf16 u, ragged T, accumulate onto
     # existing values -- a smaller problem, so stale partials of call 1 sit beyond it
     T2, n2, r2 = 300, 1024, 8
     X2 = bf16_dev(synth.gaussian((T2, n2), 43, 2))
     U2 = bf16_dev(synth.gaussian((T2, 64), 44, 2))
     want2, got2 = _outer_both(X2, n2, None, U2, 64, r2, T2, 0, 1, 128, 45)
-    assert rel_err(to_np(got2), to_np(want2)) <= TOL
+    assert torch.equal(got2, want2)
     # and against a plain fp64 product, to be sure both are the real thing
     x = to_np(X2)
     u = to_np(U2)[:, :r2]
@@ -71,3 +72,13 @@ def test_noalloc_outer_refuses_sizes_beyond_its_array():
                                         out.data_ptr(), stream())
     assert rc == L.LS_ERR_ARG
     assert "more than the fixed" in L.last_error()
+
+
+def test_noalloc_outer_compact_u():
+    """U stored compactly ([T, r], ldu = r < 16): only its r columns are read."""
+    T, ncols, r = 200, 512, 8
+    X = bf16_dev(synth.gaussian((T, ncols), 46, 3))
+    U = torch.from_numpy(synth.gaussian_f32((T, r), 47, 3)).to(DEV)
+    want, got = _outer_both(X, ncols, U, None, r, r, T, 1, 0, 64, 48)
+    assert torch.equal(got, want)
+    assert rel_err(to_np(got), to_np(U).T @ to_np(X)) <= TOL
