@@ -161,6 +161,13 @@ struct GemmSched {
   }
 };
 
+// Dequant warps of the 256 x 256 tiles: 16, in two groups taking alternate k-steps, so
+// four of them share each scheduler and hide one another's latency (the dequant is the
+// kernel's bound: byte permutes and bit-selects on the integer pipe); 8 elsewhere.
+#ifndef LS_GEMM_DQ_WARPS_256
+#define LS_GEMM_DQ_WARPS_256 16
+#endif
+
 template <int NACC, int BN, int S, int SB>
 struct GemmCfg {
   static constexpr int BM = 128 * NACC;
@@ -169,8 +176,10 @@ struct GemmCfg {
   static constexpr int UNITS = BN;               // 64-element rows dequantised per k-step
   static constexpr int W_BYTES = UNITS * 32;
   static constexpr int ABS_PER_STAGE = UNITS;
-  static constexpr int NDQ_WARPS = 8;
+  static constexpr int NDQ_WARPS = (NACC == 2 && BN == 256) ? LS_GEMM_DQ_WARPS_256 : 8;
   static constexpr int NDQ = NDQ_WARPS * 32;
+  // the first 8 dequant warps also run the epilogue (two per TMEM lane quarter)
+  static constexpr int EPI_WARPS = 8;
   // dequant: one thread per 64-element row of the B tile (forward: output column;
   // input gradient: W row x 64-column block); when there are fewer rows than dequant
   // threads, groups of them take alternate k-steps (group g owns B buffer g)
@@ -189,6 +198,7 @@ struct GemmCfg {
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(FWD_GROUPS == 1 || (FWD_GROUPS == 2 && SB == 2), "dequant groups need one B buffer each");
+  static_assert(NDQ % UNITS == 0 && NDQ_WARPS >= EPI_WARPS, "dequant warp layout");
 };
 
 // -------------------------------------------------------------------------- dequantisers
@@ -216,17 +226,28 @@ __device__ __forceinline__ void nf4_byte_tab(float a, Nf4ByteTab& t) {
   }
 }
 
-// Four codes (16 bits: byte 0 = elements 0 (high nibble) and 1, byte 1 = elements 2, 3)
-// to two bf16x2 words (elements 0,1 and 2,3).
-__device__ __forceinline__ void nf4_lookup4(uint32_t v, const Nf4ByteTab& t, uint32_t& o01, uint32_t& o23) {
-  const uint32_t s7 = v & 0x7777u;
-  const uint32_t la = __byte_perm(t.lo[0], t.lo[1], s7), lb = __byte_perm(t.lo[2], t.lo[3], s7);
-  const uint32_t ha = __byte_perm(t.hi[0], t.hi[1], s7), hb = __byte_perm(t.hi[2], t.hi[3], s7);
-  const uint32_t m = __byte_perm(0x0000FF00u, 0u, (v >> 3) & 0x1111u);   // 0xFF where code >= 8
-  const uint32_t L = (la & ~m) | (lb & m), H = (ha & ~m) | (hb & m);
-  // bytes of L/H are in nibble order: element 1, 0, 3, 2
-  o01 = __byte_perm(L, H, 0x4051);
-  o23 = __byte_perm(L, H, 0x6273);
+// Eight codes (one 32-bit word: byte i holds elements 2i (high nibble) and 2i + 1) to
+// four bf16x2 words (elements 0,1 / 2,3 / 4,5 / 6,7).  Per half-word (four codes):
+//  - four byte permutes pick each code's low and high output byte from the tables of
+//    entries 0..7 and 8..15 (selectors = the codes' low three bits);
+//  - one sign-replicating byte permute forms the mask of the codes >= 8: each code's
+//    bit 3 is the top bit of a byte of w (even elements) or of w << 4 (odd elements),
+//    and a selector nibble with bit 3 set copies that top bit over the whole byte;
+//  - two bit-selects merge the halves of the tables, two permutes interleave the low
+//    and high bytes into bf16 pairs.
+__device__ __forceinline__ void nf4_lookup8(uint32_t w, const Nf4ByteTab& t, uint32_t (&o)[4]) {
+  const uint32_t u = w << 4;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t s7 = (h ? w >> 16 : w) & 0x7777u;
+    const uint32_t la = prmt(t.lo[0], t.lo[1], s7), lb = prmt(t.lo[2], t.lo[3], s7);
+    const uint32_t ha = prmt(t.hi[0], t.hi[1], s7), hb = prmt(t.hi[2], t.hi[3], s7);
+    // result bytes in nibble order of s7: elements 1, 0, 3, 2 of this half-word
+    const uint32_t m = prmt(w, u, h ? 0xBFAEu : 0x9D8Cu);
+    const uint32_t L = (la & ~m) | (lb & m), H = (ha & ~m) | (hb & m);
+    o[2 * h] = prmt(L, H, 0x4051u);
+    o[2 * h + 1] = prmt(L, H, 0x6273u);
+  }
 }
 
 // One 64-code row: codes at src (32 bytes, 16-byte aligned), one absmax, written as one
@@ -242,8 +263,7 @@ __device__ __forceinline__ void dequant_row(const uint8_t* src, float a, int h0,
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     uint32_t o[4];
-    nf4_lookup4(cw[c] & 0xFFFFu, t, o[0], o[1]);
-    nf4_lookup4(cw[c] >> 16, t, o[2], o[3]);
+    nf4_lookup8(cw[c], t, o);
     *reinterpret_cast<uint4*>(Bt + dst_off + ((c ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
@@ -285,17 +305,17 @@ __device__ __forceinline__ void copy_ext_rows(const __nv_bfloat16* ext_b, int n0
 
 // -------------------------------------------------------------------------- epilogue pieces
 
-__device__ __forceinline__ void store_bf16_32(__nv_bfloat16* dst, const float (&f)[32], int nvalid) {
-  if (nvalid >= 32) {
-    uint32_t p[16];
+__device__ __forceinline__ void store_bf16_16(__nv_bfloat16* dst, const float (&f)[16], int nvalid) {
+  if (nvalid >= 16) {
+    uint32_t p[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+    for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
     uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+    d[0] = make_uint4(p[0], p[1], p[2], p[3]);
+    d[1] = make_uint4(p[4], p[5], p[6], p[7]);
   } else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 16; ++i)
       if (i < nvalid) dst[i] = __float2bfloat16_rn(f[i]);
   }
 }
@@ -335,7 +355,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
       mbar_init(bempty(s), 1);
     }
     mbar_init(accfull, 1);
-    mbar_init(tmemfree, C::NDQ_WARPS);
+    mbar_init(tmemfree, C::EPI_WARPS);
     mbar_init(drained, 1);
     fence_barrier_init();
     s_abort = 0;
@@ -483,6 +503,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
     const int ew = warp - 2;   // epilogue warp: TMEM lane quarter wq, column half `half`
     const int wq = warp & 3;
     const int half = ew >> 2;
+    const bool epi = ew < C::EPI_WARPS;
     int gi = 0, pc = 0;
     while (sc.next(tile, k0, k1)) {
       int m0, n0;
@@ -511,6 +532,10 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
         if (lane == 0) mbar_arrive(bfull(b));
       }
       gi += n;
+      if (!epi) {   // dequant-only warps go straight on to the next piece's k-steps
+        if (stop || s_abort) break;
+        continue;
+      }
       if (stop || s_abort || !mbar_wait(accfull, pc & 1)) {
         s_abort = 1;
         break;
@@ -549,33 +574,33 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
             coef_r = g.coef[row];
           }
         }
-        for (int cc = 0; cc < BN / 64; ++cc) {
-          const int c0 = half * (BN / 2) + cc * 32;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * BN + c0), v);
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          const int c0 = half * (BN / 2) + cc * 16;
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * BN + c0), v);
           tmem_ld_wait();
-          // partial-slot position of this thread's 32 values: chunk (a, wq, c0 / 32),
-          // 8 float4 groups of 32 lanes
-          const size_t chunk = ((size_t)(a * 4 + wq) * (BN / 32) + c0 / 32) * 1024 + (size_t)lane * 4;
+          // partial-slot position of this thread's 16 values: chunk (a, wq, c0 / 16),
+          // 4 float4 groups of 32 lanes
+          const size_t chunk = ((size_t)(a * 4 + wq) * (BN / 16) + c0 / 16) * 512 + (size_t)lane * 4;
           if (partial) {
             float4* dst = reinterpret_cast<float4*>(g.sk_ws + (size_t)sc.c * kSkSlotFloats + chunk);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
+            for (int q = 0; q < 4; ++q)
               __stcg(dst + q * 32, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
             continue;
           }
           const int gc = n0 + c0;
-          const int nvalid = min(32, g.Nout - gc);
+          const int nvalid = min(16, g.Nout - gc);
           if (!rok || nvalid <= 0) continue;
-          float f[32];
+          float f[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
           if (finish) {
             for (int d = sc.c + 1; d <= dlast; ++d) {
               const float4* srcp = reinterpret_cast<const float4*>(g.sk_ws + (size_t)d * kSkSlotFloats + chunk);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
+              for (int q = 0; q < 4; ++q) {
                 const float4 p4 = __ldcg(srcp + q * 32);
                 f[4 * q] += p4.x;
                 f[4 * q + 1] += p4.y;
@@ -587,10 +612,10 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
           if (g.epi == EPI_BF16) {
             if (g.residual) {
               const __nv_bfloat16* rp = g.residual + (size_t)row * g.ldr + gc;
-              if (nvalid >= 32) {
+              if (nvalid >= 16) {
                 const uint4* r4 = reinterpret_cast<const uint4*>(rp);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                   const uint4 rv = r4[q];
                   const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
@@ -601,17 +626,17 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
                 }
               } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
+                for (int i = 0; i < 16; ++i)
                   if (i < nvalid) f[i] += bf2f(rp[i]);
               }
             }
-            store_bf16_32(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
+            store_bf16_16(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
           } else if (g.epi == EPI_F32 || g.epi == EPI_F32_ACC) {
             float* op = reinterpret_cast<float*>(g.out) + (size_t)row * g.ldo + gc;
-            if (nvalid >= 32) {
+            if (nvalid >= 16) {
               float4* o4 = reinterpret_cast<float4*>(op);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) {
+              for (int q = 0; q < 4; ++q) {
                 float4 x = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
                 if (g.epi == EPI_F32_ACC) {
                   const float4 y = o4[q];
@@ -621,13 +646,13 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
               }
             } else {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
+              for (int i = 0; i < 16; ++i)
                 if (i < nvalid) op[i] = (g.epi == EPI_F32_ACC ? op[i] : 0.f) + f[i];
             }
           } else if (g.epi == EPI_LOGPROB) {
             float cm = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
+            for (int i = 0; i < 16; ++i)
               if (i < nvalid) cm = fmaxf(cm, f[i]);
             if (cm > run_m) {
               run_s *= __expf(run_m - cm);
@@ -635,22 +660,22 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
             }
             float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
+            for (int i = 0; i < 16; ++i)
               if (i < nvalid) acc += __expf(f[i] - run_m);
             run_s += acc;
             const int rel = tgt - gc;
             if (rel >= 0 && rel < nvalid) {
               float t = 0.f;
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
+              for (int i = 0; i < 16; ++i)
                 if (i == rel) t = f[i];
               g.tgt_logit[row] = t;
             }
           } else {  // EPI_DLOGITS: coef * (onehot(target) - softmax)
             const int rel = tgt - gc;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = coef_r * ((i == rel ? 1.f : 0.f) - __expf(f[i] - lse_r));
-            store_bf16_32(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
+            for (int i = 0; i < 16; ++i) f[i] = coef_r * ((i == rel ? 1.f : 0.f) - __expf(f[i] - lse_r));
+            store_bf16_16(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
           }
         }
         if (!partial && g.epi == EPI_LOGPROB && rok && n0 + half * (BN / 2) < g.Nout) {

@@ -242,6 +242,29 @@ def test_paired_halves_differ_and_match_whole_tiles(T, N, K, ext):
     _check_device_error()
 
 
+@pytest.mark.parametrize("mode,split", [(0, 1), (0, -1), (1, 1), (1, -1)])
+def test_one_hot_rows_reproduce_the_dequant_exactly(mode, split):
+    """With one-hot activation rows every output of the fused product is a single
+    dequantised weight (times 1, plus exact zeros), so the GEMM's in-shared-memory dequant
+    must equal the definition bit for bit: forward out[m, n] = deq(W)[n, m], input
+    gradient out[m, k] = deq(W)[m, k].  N(0, 0.02) weights use all 16 codes, so both
+    halves of the byte tables and the >= 8 mask are exercised, on whole and split tiles."""
+    N, K = 512, 1024
+    w = _w(N, K, seed=51)
+    p, a, _, _ = nf4_dev(w)
+    wd = _deq(w)
+    M = K if mode == 0 else N
+    red = K if mode == 0 else N
+    x = torch.eye(M, red, dtype=torch.bfloat16, device=DEV).contiguous()
+    outc = N if mode == 0 else K
+    out = torch.empty((M, outc), dtype=torch.float32, device=DEV)
+    _sk(mode, x, M, p, a, N, K, None, None, 0, 1, out, outc, None, split)
+    torch.cuda.synchronize()
+    want = torch.from_numpy(np.ascontiguousarray(wd.T if mode == 0 else wd))
+    assert torch.equal(out.cpu(), want)
+    _check_device_error()
+
+
 def test_split_rejects_small_workspace():
     ws = _ws()
     x = torch.zeros((256, 256), dtype=torch.bfloat16, device=DEV)
