@@ -241,7 +241,14 @@ __global__ void attn_bwd_dot_kernel(const __nv_bfloat16* __restrict__ dout, cons
   const __nv_bfloat16* a = dout + (size_t)t * ld + (size_t)h * hd;
   const __nv_bfloat16* b = o + (size_t)t * ld + (size_t)h * hd;
   float acc = 0.f;
-  for (int d = lane; d < hd; d += 32) acc += bf2f(a[d]) * bf2f(b[d]);
+  // four consecutive elements per lane (8-byte reads; hd and ld are multiples of 4)
+  for (int d = lane * 4; d < hd; d += 128) {
+    const uint2 x = *reinterpret_cast<const uint2*>(a + d), y = *reinterpret_cast<const uint2*>(b + d);
+    acc += bf16lo(x.x) * bf16lo(y.x);
+    acc += bf16hi(x.x) * bf16hi(y.x);
+    acc += bf16lo(x.y) * bf16lo(y.y);
+    acc += bf16hi(x.y) * bf16hi(y.y);
+  }
   acc = warp_sum(acc);
   if (lane == 0) D[(size_t)h * T + t] = acc;
 }
@@ -496,15 +503,20 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(const __nv_bfloat16*
 }
 
 // dk / dv = sum over the head slices in slice order, into the k / v columns of dqkv.
+// Four consecutive columns per thread (float4): w = 2 nkv hd and ldg are multiples of 4.
 __global__ void attn_dkdv_reduce_kernel(const float* __restrict__ part, int hsplit, int nh, int nkv, int hd, int T,
                                         float* __restrict__ dqkv, long long ldg) {
-  const long long w = 2LL * nkv * hd;
-  const long long n = (long long)T * w;
-  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
-    const long long t = e / w, c = e % w;
-    float v = 0.f;
-    for (int k = 0; k < hsplit; ++k) v += part[(size_t)k * n + e];
-    dqkv[t * ldg + (long long)nh * hd + c] = v;
+  const long long w4 = (2LL * nkv * hd) >> 2;
+  const long long n4 = (long long)T * w4;
+  const float4* p4 = reinterpret_cast<const float4*>(part);
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n4; e += (long long)gridDim.x * blockDim.x) {
+    const long long t = e / w4, c = (e % w4) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < hsplit; ++k) {
+      const float4 x = p4[(size_t)k * n4 + e];
+      v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
+    }
+    *reinterpret_cast<float4*>(dqkv + t * ldg + (long long)nh * hd + c) = v;
   }
 }
 

@@ -147,7 +147,8 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
       return cudaErrorInvalidValue;
   } else {
     if (!make_map_2d(&tW, CU_TENSOR_MAP_DATA_TYPE_UINT8, c.Wp, (uint64_t)g.Kw / 2, (uint64_t)g.Nw,
-                     (uint64_t)g.Kw / 2, C::UNITS / 2, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+                     (uint64_t)g.Kw / 2, C::UNITS / 2, 64,
+                     C::DX_W_SWIZZLE ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
   if (g.ext_k > 0) {
@@ -157,6 +158,17 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   } else {
     tX = tA;
   }
+  // absmax [Nw, Kw / 64] fp32 by TMA when its row pitch is a multiple of 16 bytes (and, for
+  // the input gradient, a tile's 4 k-blocks make a 16-byte box row)
+  const int KBw = g.Kw / 64;
+  const bool abs_tma = KBw % 4 == 0 && (MODE == GEMM_FWD || C::UNITS == 256) &&
+                       (reinterpret_cast<uintptr_t>(g.absmax) & 15) == 0;
+  CUtensorMap tS = tA;
+  if (abs_tma &&
+      !make_map_2d(&tS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.absmax, (uint64_t)KBw, (uint64_t)g.Nw, (uint64_t)KBw * 4,
+                   MODE == GEMM_FWD ? 4u : (uint32_t)(C::UNITS / 64), MODE == GEMM_FWD ? (uint32_t)C::UNITS : 64u,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   // Tile order: consecutive CTAs (one wave) share the operand that is walked slowly.
   // M-fastest keeps each weight tile in L2 for all row tiles; when the activation
   // operand is the larger one (long reductions, e.g. the 32B down-projection's dX) the
@@ -169,6 +181,7 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   ga.sched_ctas = p.ctas;
   ga.sched_dp = p.whole_per_cta;
   ga.pair_rows = p.pair_rows;
+  ga.abs_tma = abs_tma ? 1 : 0;
   ga.sk_iters = 0;
   ga.sk_ws = nullptr;
   ga.sk_flags = nullptr;
@@ -183,9 +196,9 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   if (!kCanSplit && (ga.sched_dp != 1 || ga.sched_ctas != nt)) return cudaErrorInvalidValue;
   if (ga.sk_iters == 0) {
     if (ga.sched_dp == 1 && ga.sched_ctas == nt && !p.pair_rows)
-      kern_whole<<<(unsigned)nt, C::THREADS, C::SMEM, st>>>(tA, tW, tX, ga);
+      kern_whole<<<(unsigned)nt, C::THREADS, C::SMEM, st>>>(tA, tW, tX, tS, ga);
     else   // whole tiles, several per CTA, or paired rows
-      kern_split<<<(unsigned)ga.sched_ctas, C::THREADS, C::SMEM, st>>>(tA, tW, tX, ga);
+      kern_split<<<(unsigned)ga.sched_ctas, C::THREADS, C::SMEM, st>>>(tA, tW, tX, tS, ga);
     return cudaGetLastError();
   }
   // CTAs of a split schedule wait for one another's partial tiles: a cooperative launch
@@ -200,7 +213,7 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   at[0].val.cooperative = 1;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, kern_split, tA, tW, tX, ga);
+  return cudaLaunchKernelEx(&lc, kern_split, tA, tW, tX, tS, ga);
 }
 
 // Pick the tile shape by estimated time = waves x per-CTA time.  Per-CTA time per

@@ -47,7 +47,7 @@ int set_thread_err(int code, const std::string& m) {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-constexpr int kLoraSplitMax = 4;   // K slices of the LoRA projections (workspace scratch)
+constexpr int kLoraSplitMax = 8;   // K slices of the LoRA projections (workspace scratch)
 
 // ------------------------------------------------------------------ host NF4 quantiser
 // QLoRA's NormalFloat-4 code values (Dettmers et al. 2023, Appendix E).
@@ -624,8 +624,8 @@ cudaError_t attn_bwd_launch(const bf16* qkv, long long ld, const bf16* dout, con
   ls::attn_bwd_dkdv_kernel<HD><<<gk, 128, smem_k, st>>>(qkv, ld, dout, lddo, lse, D, cu, nh, nkv, scale, dqkv, ldg, T,
                                                         hsplit, part);
   if (hsplit > 1) {
-    const long long n = (long long)T * 2 * nkv * HD;
-    ls::attn_dkdv_reduce_kernel<<<grid1d(n, 256), 256, 0, st>>>(part, hsplit, nh, nkv, HD, T, dqkv, ldg);
+    const long long n4 = (long long)T * 2 * nkv * HD / 4;
+    ls::attn_dkdv_reduce_kernel<<<grid1d(n4, 256), 256, 0, st>>>(part, hsplit, nh, nkv, HD, T, dqkv, ldg);
   }
   return cudaGetLastError();
 }
@@ -662,7 +662,10 @@ cudaError_t lora_proj(const bf16* X, long long ldx, int T, ls::LoraProjHalf h0, 
                       float* out_f32, bf16* out_ext, float* scratch, cudaStream_t st) {
   const int ns = scratch ? kLoraSplit : 1;
   // 16-byte row reads when every half's columns allow them
-  auto v16 = [&](const ls::LoraProjHalf& h) { return !h.w || (h.xcol % 8 == 0 && h.K % 32 == 0); };
+  auto v16 = [&](const ls::LoraProjHalf& h) {
+    return !h.w || (h.xcol % 8 == 0 && h.K % 32 == 0 &&
+                    (h.trans || (h.ldw % 8 == 0 && (reinterpret_cast<uintptr_t>(h.w) & 15) == 0)));
+  };
   const dim3 grid((T + 15) / 16, ns);
   if (ldx % 8 == 0 && (reinterpret_cast<uintptr_t>(X) & 15) == 0 && v16(h0) && v16(h1))
     ls::lora_proj_kernel<true><<<grid, 256, 0, st>>>(X, ldx, T, h0, h1, r, s, out_f32, out_ext, scratch);
@@ -838,13 +841,21 @@ int run_items(ls_ctx* c, const std::vector<int>& items, const std::function<int(
   for (size_t j = 0; j < items.size(); ++j) {
     CK(cudaStreamWaitEvent(c->cs, c->ev_ready[s_cur], 0));
     int s_next = -1;
-    if (j + 1 < items.size()) {
+    // A RAM-backed next item is queued on the copy stream first, so the link starts at
+    // once.  A file-backed one is read on this host thread (pread): queue this item's
+    // kernels first, so the GPU computes while the disk read runs.
+    const bool next_file = j + 1 < items.size() && items[j + 1] < c->L && c->lf[items[j + 1]].fd >= 0;
+    if (j + 1 < items.size() && !next_file) {
       rc = prefetch(c, items[j + 1], s_cur, &s_next);
       if (rc) return rc;
     }
     c->slot_use[s_cur] = ++c->use_clock;
     rc = body(items[j], c->slot[s_cur]);
     if (rc) return rc;
+    if (next_file) {
+      rc = prefetch(c, items[j + 1], s_cur, &s_next);
+      if (rc) return rc;
+    }
     CK(cudaEventRecord(c->ev_free[s_cur], c->cs));
     c->free_rec[s_cur] = true;
     s_cur = s_next;

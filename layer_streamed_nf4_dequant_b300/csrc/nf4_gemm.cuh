@@ -80,6 +80,10 @@ struct GemmArgs {
   // always share a CTA, its k-ranges and its partial sums (identical inputs -> identical
   // outputs).  0: a tile's accumulators take consecutive 128-row blocks.
   int pair_rows;
+  // absmax by TMA (1) or 4-byte cp.async (0).  TMA: forward, a box of 4 consecutive k-blocks x
+  // UNITS rows each k-step (column it % 4 used); input gradient, the k-step's 64 rows x 4
+  // k-blocks.  Needs the absmax row pitch (K / 64 floats) to be a multiple of 16 bytes.
+  int abs_tma;
 };
 
 // Stream-K workspace: one 256 x 256 fp32 partial tile per CTA, at most kSkMaxCtas CTAs.
@@ -161,11 +165,54 @@ struct GemmSched {
   }
 };
 
-// Dequant warps of the 256 x 256 tiles: 16, in two groups taking alternate k-steps, so
-// four of them share each scheduler and hide one another's latency (the dequant is the
-// kernel's bound: byte permutes and bit-selects on the integer pipe); 8 elsewhere.
-#ifndef LS_GEMM_DQ_WARPS_256
-#define LS_GEMM_DQ_WARPS_256 16
+// A walk over a CTA's items (k-iterations of its pieces, in order), for roles that run
+// ahead of the others (the producer's two rings).
+template <bool SPLIT>
+struct ItemCursor {
+  GemmSched<SPLIT> sc;
+  int tile, k1, it, m0, n0, trows, bn;
+  __device__ __forceinline__ void init(const GemmArgs& g, int cta, int niter, int tile_rows, int bn_) {
+    sc.init(g, cta, niter);
+    tile = k1 = it = m0 = n0 = 0;
+    trows = tile_rows;
+    bn = bn_;
+  }
+  // advance to the next item; false once the CTA's work is done
+  __device__ __forceinline__ bool next() {
+    if (it + 1 < k1) {
+      ++it;
+      return true;
+    }
+    int k0;
+    if (!sc.next(tile, k0, k1)) {
+      it = k1 = 0;
+      return false;
+    }
+    it = k0;
+    sc.tile_origin(tile, trows, bn, m0, n0);
+    return true;
+  }
+};
+
+// Shared-memory rings of one CTA:
+//  - A ring (S stages): the activation tile of a k-step, filled by TMA, released by the
+//    MMAs that read it;
+//  - W ring (SW stages): the packed codes and absmax of a k-step, filled by TMA and
+//    cp.async, released by the dequant warps as soon as they have read them.  The
+//    producer keeps it LOOK k-steps ahead of the A ring, so a dequant never waits for an
+//    MMA to finish before its codes can be fetched;
+//  - B ring (SB stages): dequantised bf16 tiles, written by the dequant warps, released
+//    by the MMAs.
+// Dequant: TPU threads per 64-code row of the B tile (1: the whole row, 2: 32 codes
+// each), in NGRP groups taking alternate k-steps (group g owns B buffer g); the first 8
+// dequant warps also run the epilogue (two per TMEM lane quarter).  The 256-wide tiles
+// take their layout from LS_GEMM_TPU_256 / LS_GEMM_NGRP_256; the 128-wide ones use two
+// threads per row, one group.
+#ifndef LS_GEMM_TPU_256
+#define LS_GEMM_TPU_256 1
+#endif
+#ifndef LS_GEMM_NGRP_256
+#define LS_GEMM_NGRP_256 1
 #endif
 
 template <int NACC, int BN, int S, int SB>
@@ -175,30 +222,34 @@ struct GemmCfg {
   static constexpr int B_BYTES = BN * 128;
   static constexpr int UNITS = BN;               // 64-element rows dequantised per k-step
   static constexpr int W_BYTES = UNITS * 32;
-  static constexpr int ABS_PER_STAGE = UNITS;
-  static constexpr int NDQ_WARPS = (NACC == 2 && BN == 256) ? LS_GEMM_DQ_WARPS_256 : 8;
-  static constexpr int NDQ = NDQ_WARPS * 32;
-  // the first 8 dequant warps also run the epilogue (two per TMEM lane quarter)
+  static constexpr int ABS_PER_STAGE = UNITS * 4;   // floats (forward TMA box: 4 k-blocks per row)
+  static constexpr int SW = 5;
+  static constexpr int LOOK = 3;                 // W ring lead over the A ring (< SW)
+  static constexpr int TPU = BN == 256 ? LS_GEMM_TPU_256 : 2;
+  static constexpr int NGRP = BN == 256 ? LS_GEMM_NGRP_256 : 1;
+  static constexpr int GROUP_THREADS = TPU * UNITS;
+  static constexpr int NDQ = GROUP_THREADS * NGRP;
+  static constexpr int NDQ_WARPS = NDQ / 32;
+  static constexpr int GROUP_WARPS = NDQ_WARPS / NGRP;
   static constexpr int EPI_WARPS = 8;
-  // dequant: one thread per 64-element row of the B tile (forward: output column;
-  // input gradient: W row x 64-column block); when there are fewer rows than dequant
-  // threads, groups of them take alternate k-steps (group g owns B buffer g)
-  static constexpr int FWD_GROUPS = NDQ / UNITS;
-  static constexpr int FWD_GROUP_WARPS = NDQ_WARPS / FWD_GROUPS;
+  // input gradient: the code tile's rows are 128 bytes at BN = 256; TMA stores them with
+  // the 128-byte swizzle so that a row-per-lane read pattern meets no bank conflicts
+  static constexpr bool DX_W_SWIZZLE = UNITS == 256;
   static constexpr int THREADS = 64 + NDQ;
   static constexpr int TMEM_COLS = NACC * BN;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S * A_BYTES;
   static constexpr int OFF_W = OFF_B + SB * B_BYTES;
-  static constexpr int OFF_ABS = OFF_W + S * W_BYTES;
-  static constexpr int OFF_BAR = OFF_ABS + S * ABS_PER_STAGE * 4;
-  static constexpr int NBAR = 2 * S + 2 * SB + 3;   // + accumulator full / drained, TMEM free
+  static constexpr int OFF_ABS = OFF_W + SW * W_BYTES;
+  static constexpr int OFF_BAR = OFF_ABS + SW * ABS_PER_STAGE * 4;
+  static constexpr int NBAR = 2 * S + 2 * SW + 2 * SB + 3;   // + accumulator full / drained, TMEM free
   static constexpr int OFF_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_SLOT + 16 + 1024;   // + slack to align the base to 1024
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
   static_assert(BN == 128 || BN == 256, "BN");
-  static_assert(FWD_GROUPS == 1 || (FWD_GROUPS == 2 && SB == 2), "dequant groups need one B buffer each");
-  static_assert(NDQ % UNITS == 0 && NDQ_WARPS >= EPI_WARPS, "dequant warp layout");
+  static_assert(LOOK < SW && NDQ_WARPS >= EPI_WARPS, "ring / warp layout");
+  static_assert((TPU == 1 || TPU == 2) && (NGRP == 1 || (NGRP == 2 && SB == 2)), "dequant layout");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 // -------------------------------------------------------------------------- dequantisers
@@ -250,13 +301,30 @@ __device__ __forceinline__ void nf4_lookup8(uint32_t w, const Nf4ByteTab& t, uin
   }
 }
 
-// One 64-code row: codes at src (32 bytes, 16-byte aligned), one absmax, written as one
-// 128-byte row of the swizzled B tile (dst_off, swizzle phase sw).  h0 staggers the
-// order of the two 16-byte code reads across neighbouring rows (bank spread).
-__device__ __forceinline__ void dequant_row(const uint8_t* src, float a, int h0, uint8_t* Bt, int dst_off, int sw) {
-  const uint4 first = *reinterpret_cast<const uint4*>(src + h0 * 16);
-  const uint4 second = *reinterpret_cast<const uint4*>(src + (h0 ^ 1) * 16);
-  const uint4 w0 = h0 ? second : first, w1 = h0 ? first : second;
+// Half a 64-code row: 32 codes at src (16 bytes, 16-byte aligned), the row's absmax,
+// written as chunks 4 hf .. 4 hf + 3 of one 128-byte row of the swizzled B tile
+// (dst_off, swizzle phase sw).
+__device__ __forceinline__ void dequant_half(const uint8_t* src, float a, int hf, uint8_t* Bt, int dst_off, int sw) {
+  const uint4 w = *reinterpret_cast<const uint4*>(src);
+  Nf4ByteTab t;
+  nf4_byte_tab(a, t);
+  const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t o[4];
+    nf4_lookup8(cw[c], t, o);
+    *reinterpret_cast<uint4*>(Bt + dst_off + (((4 * hf + c) ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// A whole 64-code row: 32 code bytes as two 16-byte pieces at src0 / src1, one absmax,
+// written as the 8 chunks of one 128-byte row of the swizzled B tile.
+// swap_read: the pieces are read src1 first (bank spread), still fed in k order.
+__device__ __forceinline__ void dequant_full(const uint8_t* src0, const uint8_t* src1, float a, uint8_t* Bt,
+                                             int dst_off, int sw, int swap_read) {
+  const uint4 r0 = *reinterpret_cast<const uint4*>(swap_read ? src1 : src0);
+  const uint4 r1 = *reinterpret_cast<const uint4*>(swap_read ? src0 : src1);
+  const uint4 w0 = swap_read ? r1 : r0, w1 = swap_read ? r0 : r1;
   Nf4ByteTab t;
   nf4_byte_tab(a, t);
   const uint32_t cw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -268,27 +336,63 @@ __device__ __forceinline__ void dequant_row(const uint8_t* src, float a, int h0,
   }
 }
 
-// FWD: unit j = B-tile row base_row + j (output column n0 + base_row + j); its codes
-// are row j of this CTA's W tile (32 bytes per row), K-major SW128 destination.
-__device__ __forceinline__ void dequant_fwd_unit(const uint8_t* Wt, const float* absS, uint8_t* Bt, int j,
-                                                 int base_row) {
-  const int jb = base_row + j;
-  dequant_row(Wt + j * 32, absS[j], (j >> 2) & 1, Bt, jb * 128, jb & 7);
+// FWD, one group thread tg of a k-step.  B-tile row j (output column n0 + j) holds the
+// 64 codes of row j of this CTA's W tile (32 bytes), K-major SW128 destination.
+//  TPU 1: thread tg takes row j = tg; rows j and j ^ 4 read their two 16-byte pieces in
+//         opposite order, so the 8 lanes of a 16-byte access phase meet 8 bank groups;
+//  TPU 2: thread tg takes half hf = tg & 1 of row j = tg >> 1 (a warp reads 512
+//         contiguous bytes).
+// Row j's absmax is absS[j * astride + acol] (a k-block column of the TMA box, or one
+// float per row).
+template <int TPU>
+__device__ __forceinline__ void dequant_fwd_part(const uint8_t* Wt, const float* absS, int astride, int acol,
+                                                 uint8_t* Bt, int tg) {
+  if constexpr (TPU == 1) {
+    const int j = tg, h0 = (j >> 2) & 1;
+    const uint8_t* lo = Wt + j * 32;
+    const uint8_t* hi = lo + 16;
+    dequant_full(lo, hi, absS[j * astride + acol], Bt, j * 128, j & 7, h0);
+  } else {
+    const int j = tg >> 1, hf = tg & 1;
+    dequant_half(Wt + j * 32 + hf * 16, absS[j * astride + acol], hf, Bt, j * 128, j & 7);
+  }
 }
 
 // DX, MN-major B tile.  For dX = dY . deq(W) the MMA's reduction runs over W's rows n
 // and its output columns are W's columns k, so W's own row-major tile IS the B operand
-// in MN-major form: no transpose.  Unit j = (row n = j % 64, local 64-column block
-// j / 64) of this CTA's W tile (wbytes per row), one absmax; stored as one 128-byte
-// K-row of the canonical MN-major 128B-swizzled layout: atoms of 64 columns x 8 rows
-// (1 KB), 8 atoms down the 64 rows (8 KB per 64 columns):
-//   offset = kbl*8192 + (n/8)*1024 + (n%8)*128 + chunk,  kbl = base_kb + j / 64.
-__device__ __forceinline__ void dequant_dx_unit(const uint8_t* Wt, const float* absS, uint8_t* Bt, int j, int wbytes,
-                                                int base_kb) {
-  const int n = j & 63, kbl = j >> 6;
-  const int cb = wbytes / 32;   // 64-column blocks in the W tile
-  dequant_row(Wt + n * wbytes + kbl * 32, absS[n * cb + kbl], (n >> 1) & 1, Bt,
-              (base_kb + kbl) * 8192 + (n >> 3) * 1024 + (n & 7) * 128, n & 7);
+// in MN-major form: no transpose.  The W tile has 64 rows of UNITS / 2 bytes; a unit is
+// (row n, 64-column block kbl) with one absmax.  Stored as one 128-byte K-row of the
+// canonical MN-major 128B-swizzled layout: atoms of 64 columns x 8 rows (1 KB), 8 atoms
+// down the 64 rows (8 KB per 64 columns):
+//   offset = kbl*8192 + (n/8)*1024 + (n%8)*128 + chunk.
+// UNITS 256: the W tile itself arrived 128B-swizzled (16-byte piece q of row n at
+// q ^ (n & 7)), and unit u = (n = u % 64, kbl = u / 64) puts 8 different rows in every
+// 8-lane access phase, so reads and writes meet 8 bank groups.  TPU 1: thread tg takes
+// unit tg; TPU 2: half hf = tg & 1 of unit tg >> 1.
+// UNITS 128 (TPU 2, unswizzled 64-byte rows): thread tg takes piece tg % 4 of row tg / 4,
+// a warp reading whole contiguous rows.
+template <int UNITS, int TPU>
+__device__ __forceinline__ void dequant_dx_part(const uint8_t* Wt, const float* absS, uint8_t* Bt, int tg) {
+  constexpr int CB = UNITS / 64, WB = UNITS / 2;
+  if constexpr (UNITS == 256) {
+    const int u = TPU == 1 ? tg : tg >> 1;
+    const int n = u & 63, kbl = u >> 6, sw = n & 7;
+    const uint8_t* row = Wt + n * WB;
+    const int dst = kbl * 8192 + (n >> 3) * 1024 + sw * 128;
+    if constexpr (TPU == 1) {
+      dequant_full(row + (((2 * kbl) ^ sw) << 4), row + (((2 * kbl + 1) ^ sw) << 4), absS[n * CB + kbl], Bt, dst, sw,
+                   0);
+    } else {
+      const int hf = tg & 1;
+      dequant_half(row + (((2 * kbl + hf) ^ sw) << 4), absS[n * CB + kbl], hf, Bt, dst, sw);
+    }
+  } else {
+    static_assert(TPU == 2, "128-wide input-gradient tiles use two threads per unit");
+    constexpr int P = UNITS / 32;
+    const int n = tg / P, piece = tg % P, kbl = piece >> 1, hf = piece & 1;
+    dequant_half(Wt + n * WB + piece * 16, absS[n * CB + kbl], hf, Bt, kbl * 8192 + (n >> 3) * 1024 + (n & 7) * 128,
+                 n & 7);
+  }
 }
 
 // LoRA extra stage: B_ext rows [row0, row0 + rows) (K-major, 64 wide) into the B tile.
@@ -325,7 +429,8 @@ __device__ __forceinline__ void store_bf16_16(__nv_bfloat16* dst, const float (&
 template <int NACC, int BN, int S, int SB, int MODE, bool SPLIT>
 __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                    const __grid_constant__ CUtensorMap tmX, const GemmArgs g) {
+                    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
+                    const GemmArgs g) {
   using C = GemmCfg<NACC, BN, S, SB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -337,21 +442,29 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
   const int niter = KB + (g.ext_k > 0 ? 1 : 0);
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar0 = sb + C::OFF_BAR;
-  auto full = [&](int s) { return bar0 + s * 8; };
-  auto empty = [&](int s) { return bar0 + (S + s) * 8; };
-  auto bfull = [&](int s) { return bar0 + (2 * S + s) * 8; };
-  auto bempty = [&](int s) { return bar0 + (2 * S + SB + s) * 8; };
-  const uint32_t accfull = bar0 + (2 * S + 2 * SB) * 8;       // one phase per piece
-  const uint32_t tmemfree = bar0 + (2 * S + 2 * SB + 1) * 8;  // epilogue done reading TMEM
-  const uint32_t drained = bar0 + (2 * S + 2 * SB + 2) * 8;   // every MMA retired
+  constexpr int SW = C::SW;
+  auto afull = [&](int s) { return bar0 + s * 8; };
+  auto aempty = [&](int s) { return bar0 + (S + s) * 8; };
+  auto wfull = [&](int s) { return bar0 + (2 * S + s) * 8; };
+  auto wempty = [&](int s) { return bar0 + (2 * S + SW + s) * 8; };
+  auto bfull = [&](int s) { return bar0 + (2 * S + 2 * SW + s) * 8; };
+  auto bempty = [&](int s) { return bar0 + (2 * S + 2 * SW + SB + s) * 8; };
+  constexpr int BAR_END = 2 * S + 2 * SW + 2 * SB;
+  const uint32_t accfull = bar0 + BAR_END * 8;         // one phase per piece
+  const uint32_t tmemfree = bar0 + (BAR_END + 1) * 8;  // epilogue done reading TMEM
+  const uint32_t drained = bar0 + (BAR_END + 2) * 8;   // every MMA retired
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full(s), 1 + 32);
-      mbar_init(empty(s), 1);
+      mbar_init(afull(s), 1);
+      mbar_init(aempty(s), 1);
+    }
+    for (int s = 0; s < SW; ++s) {
+      mbar_init(wfull(s), 1 + 32);
+      mbar_init(wempty(s), C::GROUP_WARPS);
     }
     for (int s = 0; s < SB; ++s) {
-      mbar_init(bfull(s), C::FWD_GROUP_WARPS);
+      mbar_init(bfull(s), C::GROUP_WARPS);
       mbar_init(bempty(s), 1);
     }
     mbar_init(accfull, 1);
@@ -364,6 +477,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmW);
     if (g.ext_k > 0) prefetch_tensormap(&tmX);
+    if (g.abs_tma) prefetch_tensormap(&tmS);
   }
   if (warp == 1) {
     tmem_alloc(sb + C::OFF_SLOT, C::TMEM_COLS);
@@ -374,8 +488,8 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
 
-  // Every role walks the same piece sequence; gi counts k-iterations across pieces and
-  // drives the ring stages and their phases.
+  // Every role walks the same item sequence (the k-iterations of the CTA's pieces, in
+  // order); item counters drive the ring stages and their phases.
   GemmSched<SPLIT> sc;
   sc.init(g, blockIdx.x, niter);
   int tile, k0, k1;
@@ -387,65 +501,83 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int gi = 0;
-    bool stop = false;
-    while (!stop && sc.next(tile, k0, k1)) {
-      int m0, n0;
-      sc.tile_origin(tile, tile_rows, BN, m0, n0);
-      for (int it = k0; it < k1; ++it, ++gi) {
-        const int s = gi % S;
-        if (s_abort || !mbar_wait(empty(s), ((gi / S) & 1) ^ 1)) {
-          s_abort = 1;
-          stop = true;
-          break;
-        }
-        const uint32_t a_dst = sb + C::OFF_A + s * C::A_BYTES;
-        if (lane == 0) {
-          if (it < KB) {
-            mbar_arrive_expect_tx(full(s), C::A_BYTES + C::W_BYTES);
-            if (pair) {   // two 128-row boxes: this tile's rows of each half
-              tma_load_2d(a_dst, &tmA, it * 64, m0, full(s));
-              tma_load_2d(a_dst + 16384, &tmA, it * 64, m0 + pair, full(s));
-            } else {
-              tma_load_2d(a_dst, &tmA, it * 64, m0, full(s));
-            }
-            const uint32_t w_dst = sb + C::OFF_W + s * C::W_BYTES;
-            if (MODE == GEMM_FWD) tma_load_2d(w_dst, &tmW, it * 32, n0, full(s));
-            else tma_load_2d(w_dst, &tmW, n0 / 2, it * 64, full(s));
-          } else {
-            mbar_arrive_expect_tx(full(s), C::A_BYTES);
-            if (pair) {
-              tma_load_2d(a_dst, &tmX, 0, m0, full(s));
-              tma_load_2d(a_dst + 16384, &tmX, 0, m0 + pair, full(s));
-            } else {
-              tma_load_2d(a_dst, &tmX, 0, m0, full(s));
-            }
-          }
-        }
+    // Two cursors over the item sequence: W (codes + absmax) runs LOOK items ahead of A.
+    // Waits never depend on an item not yet issued: W item w needs the dequant of item
+    // w - SW, which needs A item w - SW - SB + 1 (< the A items issued) for its B buffer.
+    ItemCursor<SPLIT> cw, ca;
+    cw.init(g, blockIdx.x, niter, tile_rows, BN);
+    ca.init(g, blockIdx.x, niter, tile_rows, BN);
+    int nw = 0, na = 0;
+    auto issue_w = [&]() -> bool {
+      const int s = nw % SW, it = cw.it;
+      if (s_abort || !mbar_wait(wempty(s), ((nw / SW) & 1) ^ 1)) return false;
+      const uint32_t abs_dst = sb + C::OFF_ABS + s * C::ABS_PER_STAGE * 4;
+      if (lane == 0) {
         if (it < KB) {
-          const uint32_t abs_dst = sb + C::OFF_ABS + s * C::ABS_PER_STAGE * 4;
-          if (MODE == GEMM_FWD) {
-            for (int j = lane; j < C::UNITS; j += 32) {
-              const int n = n0 + j;
-              const float* src = n < g.Nw ? g.absmax + (size_t)n * KBw + it : g_zero_word;
-              cp_async_4(abs_dst + j * 4, src);
-            }
-          } else {
-            constexpr int CB = C::UNITS / 64;
-            for (int e = lane; e < 64 * CB; e += 32) {
-              const int r = e / CB, c = e % CB;
-              const int kb = n0 / 64 + c;
-              const float* src = kb < KBw ? g.absmax + (size_t)(it * 64 + r) * KBw + kb : g_zero_word;
-              cp_async_4(abs_dst + e * 4, src);
-            }
+          const int abs_bytes = !g.abs_tma ? 0 : MODE == GEMM_FWD ? C::UNITS * 16 : C::UNITS * 4;
+          mbar_arrive_expect_tx(wfull(s), C::W_BYTES + abs_bytes);
+          const uint32_t w_dst = sb + C::OFF_W + s * C::W_BYTES;
+          if (MODE == GEMM_FWD) tma_load_2d(w_dst, &tmW, it * 32, cw.n0, wfull(s));
+          else tma_load_2d(w_dst, &tmW, cw.n0 / 2, it * 64, wfull(s));
+          if (g.abs_tma) {
+            if (MODE == GEMM_FWD) tma_load_2d(abs_dst, &tmS, it & ~3, cw.n0, wfull(s));
+            else tma_load_2d(abs_dst, &tmS, cw.n0 / 64, it * 64, wfull(s));
+          }
+        } else {
+          mbar_arrive(wfull(s));   // the LoRA extra stage reads no codes
+        }
+      }
+      if (it < KB && !g.abs_tma) {
+        if (MODE == GEMM_FWD) {
+          for (int j = lane; j < C::UNITS; j += 32) {
+            const int n = cw.n0 + j;
+            const float* src = n < g.Nw ? g.absmax + (size_t)n * KBw + it : g_zero_word;
+            cp_async_4(abs_dst + j * 4, src);
+          }
+        } else {
+          constexpr int CB = C::UNITS / 64;
+          for (int e = lane; e < 64 * CB; e += 32) {
+            const int r = e / CB, c = e % CB;
+            const int kb = cw.n0 / 64 + c;
+            const float* src = kb < KBw ? g.absmax + (size_t)(it * 64 + r) * KBw + kb : g_zero_word;
+            cp_async_4(abs_dst + e * 4, src);
           }
         }
-        cp_async_mbar_arrive_noinc(full(s));
       }
+      cp_async_mbar_arrive_noinc(wfull(s));
+      ++nw;
+      return true;
+    };
+    auto issue_a = [&]() -> bool {
+      const int s = na % S, it = ca.it;
+      if (s_abort || !mbar_wait(aempty(s), ((na / S) & 1) ^ 1)) return false;
+      if (lane == 0) {
+        const uint32_t a_dst = sb + C::OFF_A + s * C::A_BYTES;
+        const CUtensorMap* map = it < KB ? &tmA : &tmX;
+        const int x = it < KB ? it * 64 : 0;
+        mbar_arrive_expect_tx(afull(s), C::A_BYTES);
+        if (pair) {   // two 128-row boxes: this tile's rows of each half
+          tma_load_2d(a_dst, map, x, ca.m0, afull(s));
+          tma_load_2d(a_dst + 16384, map, x, ca.m0 + pair, afull(s));
+        } else {
+          tma_load_2d(a_dst, map, x, ca.m0, afull(s));
+        }
+      }
+      ++na;
+      return true;
+    };
+    bool ok = true;
+    for (int i = 0; ok && i < C::LOOK && cw.next(); ++i) ok = issue_w();
+    while (ok) {
+      if (cw.next()) ok = issue_w();
+      if (!ok || !ca.next()) break;
+      ok = issue_a();
     }
-    if (s_abort) {
+    if (!ok) {
+      s_abort = 1;
       // let copies already in flight land before the CTA's shared memory goes away
-      for (int j = gi - S < 0 ? 0 : gi - S; j < gi; ++j) mbar_wait(full(j % S), (j / S) & 1);
+      for (int j = nw - SW < 0 ? 0 : nw - SW; j < nw; ++j) mbar_wait(wfull(j % SW), (j / SW) & 1);
+      for (int j = na - S < 0 ? 0 : na - S; j < na; ++j) mbar_wait(afull(j % S), (j / S) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -461,7 +593,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
         }
         for (int it = k0; it < k1; ++it, ++gi) {
           const int s = gi % S, b = gi % SB;
-          if (s_abort || !mbar_wait(full(s), (gi / S) & 1) || !mbar_wait(bfull(b), (gi / SB) & 1)) {
+          if (s_abort || !mbar_wait(afull(s), (gi / S) & 1) || !mbar_wait(bfull(b), (gi / SB) & 1)) {
             s_abort = 1;
             stop = true;
             break;
@@ -482,7 +614,7 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
               tc_mma_bf16(tmem + a * BN, ad, bd, idesc, (it > k0 || k > 0) ? 1u : 0u);
             }
           }
-          tc_commit(empty(s));
+          tc_commit(aempty(s));
           tc_commit(bempty(b));
         }
         if (stop) break;
@@ -496,10 +628,8 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
   } else {
     // ------------------------------------------------------------ dequant warps
     const int tq = threadIdx.x - 64;
-    // group grp takes the k-iterations gi = grp (mod FWD_GROUPS); its threads one unit each
-    const int grp = tq / C::UNITS;
-    const int step = C::FWD_GROUPS;
-    const int tg = tq - grp * C::UNITS;
+    // group grp takes the items gi = grp (mod NGRP); tg = the thread's index in it
+    const int grp = tq / C::GROUP_THREADS, tg = tq % C::GROUP_THREADS;
     const int ew = warp - 2;   // epilogue warp: TMEM lane quarter wq, column half `half`
     const int wq = warp & 3;
     const int half = ew >> 2;
@@ -508,30 +638,31 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
     while (sc.next(tile, k0, k1)) {
       int m0, n0;
       sc.tile_origin(tile, tile_rows, BN, m0, n0);
-      const int n = k1 - k0;
       bool stop = false;
-      for (int gj = gi + ((grp - gi % step) + step) % step; gj < gi + n; gj += step) {
-        const int it = k0 + (gj - gi);
-        const int s = gj % S, b = gj % SB;
-        if (s_abort || !mbar_wait(full(s), (gj / S) & 1) || !mbar_wait(bempty(b), ((gj / SB) & 1) ^ 1)) {
+      for (int it = k0; it < k1; ++it, ++gi) {
+        if (C::NGRP > 1 && gi % C::NGRP != grp) continue;
+        const int sw = gi % SW, b = gi % SB;
+        if (s_abort || !mbar_wait(wfull(sw), (gi / SW) & 1) || !mbar_wait(bempty(b), ((gi / SB) & 1) ^ 1)) {
           s_abort = 1;
           stop = true;
           break;
         }
         uint8_t* Bt = smem + C::OFF_B + b * C::B_BYTES;
         if (it < KB) {
-          const uint8_t* Wt = smem + C::OFF_W + s * C::W_BYTES;
-          const float* absS = reinterpret_cast<const float*>(smem + C::OFF_ABS + s * C::ABS_PER_STAGE * 4);
-          if (MODE == GEMM_FWD) dequant_fwd_unit(Wt, absS, Bt, tg, 0);
-          else dequant_dx_unit(Wt, absS, Bt, tg, C::W_BYTES / 64, 0);
+          const uint8_t* Wt = smem + C::OFF_W + sw * C::W_BYTES;
+          const float* absS = reinterpret_cast<const float*>(smem + C::OFF_ABS + sw * C::ABS_PER_STAGE * 4);
+          if (MODE == GEMM_FWD) dequant_fwd_part<C::TPU>(Wt, absS, g.abs_tma ? 4 : 1, g.abs_tma ? (it & 3) : 0, Bt, tg);
+          else dequant_dx_part<C::UNITS, C::TPU>(Wt, absS, Bt, tg);
         } else {
-          copy_ext_rows(g.ext_b, n0, g.Nout, Bt, 0, C::UNITS, tg, C::UNITS);
+          copy_ext_rows(g.ext_b, n0, g.Nout, Bt, 0, C::UNITS, tg, C::GROUP_THREADS);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bfull(b));
+        if (lane == 0) {
+          mbar_arrive(wempty(sw));
+          mbar_arrive(bfull(b));
+        }
       }
-      gi += n;
       if (!epi) {   // dequant-only warps go straight on to the next piece's k-steps
         if (stop || s_abort) break;
         continue;

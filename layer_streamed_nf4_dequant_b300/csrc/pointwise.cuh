@@ -445,8 +445,18 @@ __global__ void pair_setup_kernel(const int* __restrict__ tokens, const int* __r
   if (i <= 2 * nseq) cu2[i] = i <= nseq ? cu[i] : T + cu[i - nseq];
 }
 
-// lse[t] = log sum_v exp(logit) from per-column-group (max, sum-exp) partials, in
-// partial order; lp[t] = logit[t, target] - lse[t] (0 without a target).
+// lse[t] = log sum_v exp(logit) from per-column-group (max, sum-exp) partials;
+// lp[t] = logit[t, target] - lse[t] (0 without a target).  One pass over the partials:
+// lane i keeps four running (max, sum) pairs over the partials p = i + 32 (4j + c)
+// (c = 0..3, independent chains), merges them in order c = 0..3, then the lanes merge
+// by a butterfly: a fixed order, so the result does not depend on scheduling.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  const float mx = fmaxf(m, m2);
+  if (mx == -INFINITY) return;   // both empty
+  s = s * __expf(m - mx) + s2 * __expf(m2 - mx);
+  m = mx;
+}
+
 __global__ void logprob_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum, int P,
                                        int ld, const float* __restrict__ tgt_logit, const int* __restrict__ tgt,
                                        float* __restrict__ lse, float* __restrict__ lp, int T) {
@@ -455,14 +465,23 @@ __global__ void logprob_combine_kernel(const float* __restrict__ pmax, const flo
   if (row >= T) return;
   const float* pm = pmax + (size_t)row * ld;
   const float* ps = psum + (size_t)row * ld;
-  float m = -INFINITY;
-  for (int p = lane; p < P; p += 32) m = fmaxf(m, pm[p]);
-  m = warp_max(m);
-  float s = 0.f;
-  for (int p = lane; p < P; p += 32) s += ps[p] * __expf(pm[p] - m);
-  s = warp_sum(s);
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, sm[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int p0 = lane; p0 < P; p0 += 128) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int p = p0 + 32 * c;
+      if (p < P) lse_merge(m[c], sm[c], pm[p], ps[p]);
+    }
+  }
+#pragma unroll
+  for (int c = 1; c < 4; ++c) lse_merge(m[0], sm[0], m[c], sm[c]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m[0], o), s2 = __shfl_xor_sync(0xffffffffu, sm[0], o);
+    lse_merge(m[0], sm[0], m2, s2);
+  }
   if (lane == 0) {
-    const float l = m + logf(s);
+    const float l = m[0] + logf(sm[0]);
     lse[row] = l;
     lp[row] = tgt[row] >= 0 ? tgt_logit[row] - l : 0.f;
   }
@@ -653,11 +672,12 @@ __device__ __forceinline__ uint32_t lora_w_pair(const LoraProjHalf& h, int n, in
 // blockIdx.y / gridDim.y selects a slice of K (fixed split); with gridDim.y > 1 the
 // block writes its unscaled partial sums to part [gridDim.y][T][32] for
 // lora_proj_reduce_kernel instead of the outputs.
-// V16: rows are read 16 bytes per lane (X 16-byte aligned, ldx and the column offsets
-// multiples of 8, K a multiple of 32): lane (g, q) loads columns 8q .. 8q+7 of a 32-wide
+// V16: rows are read 16 bytes per lane (X and W 16-byte aligned, ldx, ldw and the column
+// offsets multiples of 8, K a multiple of 32): lane (g, q) loads columns 8q .. 8q+7 of a 32-wide
 // step for rows g and g + 8, and the two m16n8k16 MMAs of the step take them as their
 // k positions in the order (8q, 8q+1 | 8q+2, 8q+3) and (8q+4, 8q+5 | 8q+6, 8q+7); B is
-// read with the same assignment, so each MMA still sums matching X and W columns.
+// read with the same assignment (for a row-major W, one 16-byte read of row n), so each
+// MMA still sums matching X and W columns.
 template <bool V16>
 __global__ void __launch_bounds__(256) lora_proj_kernel(const __nv_bfloat16* __restrict__ X, long long ldx, int T,
                                                         LoraProjHalf h0, LoraProjHalf h1, int r, float s,
@@ -692,8 +712,14 @@ __global__ void __launch_bounds__(256) lora_proj_kernel(const __nv_bfloat16* __r
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const int n = nt * 8 + g;
-          mma_16816_bf16(acc[hh][nt], a0, lora_w_pair(h, n, kc, r), lora_w_pair(h, n, kc + 2, r));
-          mma_16816_bf16(acc[hh][nt], a1, lora_w_pair(h, n, kc + 4, r), lora_w_pair(h, n, kc + 6, r));
+          if (!h.trans) {   // W row n, columns kc .. kc+7: one 16-byte read for both MMAs
+            const uint4 b = n < r ? *reinterpret_cast<const uint4*>(h.w + (size_t)n * h.ldw + kc) : make_uint4(0, 0, 0, 0);
+            mma_16816_bf16(acc[hh][nt], a0, b.x, b.y);
+            mma_16816_bf16(acc[hh][nt], a1, b.z, b.w);
+          } else {
+            mma_16816_bf16(acc[hh][nt], a0, lora_w_pair(h, n, kc, r), lora_w_pair(h, n, kc + 2, r));
+            mma_16816_bf16(acc[hh][nt], a1, lora_w_pair(h, n, kc + 4, r), lora_w_pair(h, n, kc + 6, r));
+          }
         }
       }
     } else {
@@ -772,37 +798,44 @@ __global__ void lora_proj_reduce_kernel(const float* __restrict__ part, int nspl
 //   part[chunk][c][j] = sum_{t in chunk} X[t, c] * U[t, j]     (c < ncols, j < 16)
 // X bf16 [T, ldx] (16-byte aligned rows, ncols % 8 == 0); U fp32 or bf16 [T, ldu], of
 // which only the first r columns are read (the sums of columns r..15 are zero).
-// A block takes a 64-column strip of one chunk of rows, in sub-tiles of up to 128 rows:
-// all of a sub-tile's loads (16 KB of X in 16-byte pieces, its U rows) are issued before
-// any is used, then staged in shared memory; thread (column, j-quarter) adds its 4 sums
-// in row order.  The many small blocks (64 columns x 128 rows each) keep every SM's
-// memory pipe busy; each sum is still a fixed-order walk over the chunk's rows.
+// As a matrix product out = X^T U over the chunk's rows, on the tensor cores (mma.sync
+// m16n8k16, fp32 accumulation): a block takes a 64-column strip of one chunk, in
+// sub-tiles of up to 128 rows staged in shared memory (X as [t][c], read transposed by
+// ldmatrix as the A operand; U transposed to [j][t] as the B operand).  A bf16 U is
+// exact; an fp32 U is split into u_hi = bf16(u) and u_lo = bf16(u - u_hi), two MMAs, so
+// about 16 of its mantissa bits take part (the products themselves are exact in fp32).
+// Warp w takes columns 16 (w & 3) .. + 15 and j = 8 (w >> 2) .. + 7; every sum runs
+// over the chunk's rows in a fixed order.
 __global__ void __launch_bounds__(256) lora_outer_partial_kernel(const __nv_bfloat16* __restrict__ X, long long ldx,
                                                                  int ncols, const float* __restrict__ Uf,
                                                                  const __nv_bfloat16* __restrict__ Ub, int ldu, int r,
                                                                  int T, int rows_per_chunk, float* __restrict__ part) {
-  __shared__ __align__(16) __nv_bfloat16 xs[128][64];
-  __shared__ __align__(16) float us[128][16];
+  constexpr int XS = 64 + 8, US = 128 + 8;   // padded row pitches (conflict-free ldmatrix)
+  __shared__ __align__(16) __nv_bfloat16 xs[128][XS];
+  __shared__ __align__(16) __nv_bfloat16 uh[16][US];
+  __shared__ __align__(16) __nv_bfloat16 ul[16][US];
   const int c0 = blockIdx.x * 64;
   const int chunk = blockIdx.y;
   const int t0 = chunk * rows_per_chunk, t1 = min(T, t0 + rows_per_chunk);
-  const int cl = threadIdx.x & 63, jq = threadIdx.x >> 6;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = warp & 3, nt = warp >> 2;
+  const bool split = Uf != nullptr;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int tb = t0; tb < t1; tb += 128) {
-    const int nt = min(128, t1 - tb);
+    const int nrow = min(128, t1 - tb);
     uint4 xv[4];
     float uv[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int e = threadIdx.x + i * 256, tt = e >> 3, col = c0 + (e & 7) * 8;
-      xv[i] = (tt < nt && col < ncols) ? *reinterpret_cast<const uint4*>(X + (size_t)(tb + tt) * ldx + col)
-                                       : make_uint4(0, 0, 0, 0);
+      xv[i] = (tt < nrow && col < ncols) ? *reinterpret_cast<const uint4*>(X + (size_t)(tb + tt) * ldx + col)
+                                         : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = threadIdx.x + i * 256, tt = e >> 4, j = e & 15;
       uv[i] = 0.f;
-      if (tt < nt && j < r) uv[i] = Uf ? Uf[(size_t)(tb + tt) * ldu + j] : bf2f(Ub[(size_t)(tb + tt) * ldu + j]);
+      if (tt < nrow && j < r) uv[i] = split ? Uf[(size_t)(tb + tt) * ldu + j] : bf2f(Ub[(size_t)(tb + tt) * ldu + j]);
     }
     __syncthreads();   // the previous sub-tile's readers are done
 #pragma unroll
@@ -812,24 +845,48 @@ __global__ void __launch_bounds__(256) lora_outer_partial_kernel(const __nv_bflo
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int e = threadIdx.x + i * 256;
-      us[e >> 4][e & 15] = uv[i];
+      const int e = threadIdx.x + i * 256, tt = e >> 4, j = e & 15;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(uv[i]);
+      uh[j][tt] = hi;
+      ul[j][tt] = __float2bfloat16_rn(uv[i] - __bfloat162float(hi));
     }
     __syncthreads();
-#pragma unroll 8
-    for (int tt = 0; tt < nt; ++tt) {
-      const float x = bf2f(xs[tt][cl]);
-      const float4 u = *reinterpret_cast<const float4*>(&us[tt][jq * 4]);
-      acc[0] += x * u.x;
-      acc[1] += x * u.y;
-      acc[2] += x * u.z;
-      acc[3] += x * u.w;
+    const int ksteps = (nrow + 15) >> 4;   // rows past nrow are zero in both operands
+    for (int ks = 0; ks < ksteps; ++ks) {
+      const int k0 = ks * 16;
+      // A = X^T (16 columns x 16 rows): four 8 x 8 blocks read transposed from [t][c]
+      uint32_t a[4];
+      {
+        const int mm = ((lane >> 3) & 1) * 8, kk = (lane >> 4) * 8;
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                     : "r"(smem_u32(&xs[k0 + kk + (lane & 7)][mt * 16 + mm])));
+      }
+      // B = U (16 rows x 8 j), stored [j][t]: two 8 x 8 blocks (k 0-7, 8-15)
+      uint32_t bh[2], bl[2];
+      {
+        const __nv_bfloat16* ph = &uh[nt * 8 + (lane & 7)][k0 + ((lane >> 3) & 1) * 8];
+        asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                     : "=r"(bh[0]), "=r"(bh[1]) : "r"(smem_u32(ph)));
+      }
+      mma_16816_bf16(acc, a, bh[0], bh[1]);
+      if (split) {
+        const __nv_bfloat16* pl = &ul[nt * 8 + (lane & 7)][k0 + ((lane >> 3) & 1) * 8];
+        asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                     : "=r"(bl[0]), "=r"(bl[1]) : "r"(smem_u32(pl)));
+        mma_16816_bf16(acc, a, bl[0], bl[1]);
+      }
     }
   }
-  const int c = c0 + cl;
-  if (c < ncols)
-    *reinterpret_cast<float4*>(part + ((size_t)chunk * ncols + c) * 16 + jq * 4) =
-        make_float4(acc[0], acc[1], acc[2], acc[3]);
+  // accumulator (16 columns x 8 j): thread (g, q) holds columns g, g + 8 and j 2q, 2q+1
+  const int g = lane >> 2, q = lane & 3;
+  const int j = nt * 8 + 2 * q;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = c0 + mt * 16 + g + 8 * h;
+    if (c < ncols)
+      *reinterpret_cast<float2*>(part + ((size_t)chunk * ncols + c) * 16 + j) = make_float2(acc[2 * h], acc[2 * h + 1]);
+  }
 }
 
 // out (+)= sum over chunks, in chunk order.  layout 0: out[c * r + j] (B-shaped [ncols, r]);
