@@ -445,18 +445,10 @@ __global__ void pair_setup_kernel(const int* __restrict__ tokens, const int* __r
   if (i <= 2 * nseq) cu2[i] = i <= nseq ? cu[i] : T + cu[i - nseq];
 }
 
-// lse[t] = log sum_v exp(logit) from per-column-group (max, sum-exp) partials;
-// lp[t] = logit[t, target] - lse[t] (0 without a target).  One pass over the partials:
-// lane i keeps four running (max, sum) pairs over the partials p = i + 32 (4j + c)
-// (c = 0..3, independent chains), merges them in order c = 0..3, then the lanes merge
-// by a butterfly: a fixed order, so the result does not depend on scheduling.
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
-  const float mx = fmaxf(m, m2);
-  if (mx == -INFINITY) return;   // both empty
-  s = s * __expf(m - mx) + s2 * __expf(m2 - mx);
-  m = mx;
-}
-
+// lse[t] = log sum_v exp(logit) from per-column-group (max, sum-exp) partials, in
+// partial order; lp[t] = logit[t, target] - lse[t] (0 without a target).  Two passes
+// over the row's partials (max, then the rescaled sum): every load of a pass is
+// independent, and each partial costs one exp.
 __global__ void logprob_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum, int P,
                                        int ld, const float* __restrict__ tgt_logit, const int* __restrict__ tgt,
                                        float* __restrict__ lse, float* __restrict__ lp, int T) {
@@ -465,23 +457,14 @@ __global__ void logprob_combine_kernel(const float* __restrict__ pmax, const flo
   if (row >= T) return;
   const float* pm = pmax + (size_t)row * ld;
   const float* ps = psum + (size_t)row * ld;
-  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, sm[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int p0 = lane; p0 < P; p0 += 128) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int p = p0 + 32 * c;
-      if (p < P) lse_merge(m[c], sm[c], pm[p], ps[p]);
-    }
-  }
-#pragma unroll
-  for (int c = 1; c < 4; ++c) lse_merge(m[0], sm[0], m[c], sm[c]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m[0], o), s2 = __shfl_xor_sync(0xffffffffu, sm[0], o);
-    lse_merge(m[0], sm[0], m2, s2);
-  }
+  float m = -INFINITY;
+  for (int p = lane; p < P; p += 32) m = fmaxf(m, pm[p]);
+  m = warp_max(m);
+  float s = 0.f;
+  for (int p = lane; p < P; p += 32) s += ps[p] * __expf(pm[p] - m);
+  s = warp_sum(s);
   if (lane == 0) {
-    const float l = m[0] + logf(sm[0]);
+    const float l = m + logf(s);
     lse[row] = l;
     lp[row] = tgt[row] >= 0 ? tgt_logit[row] - l : 0.f;
   }
