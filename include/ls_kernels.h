@@ -109,16 +109,22 @@ int lsk_rope_bwd_cast(const float* g, uint16_t* out, int64_t ld, const int32_t* 
 
 /* Causal GQA attention forward.  qkv bf16 [T, ld] holds q heads (nh*hd columns),
  * then k heads, then v heads (kv*hd each); sequences by cu int32 [nseq+1];
- * max_len = longest sequence.  out bf16 [T, ldo] (nh*hd columns); lse fp32 [nh, T]. */
+ * max_len = longest sequence.  out bf16 [T, ldo] (nh*hd columns); lse fp32 [nh, T].
+ * qkv and out 16-byte aligned, ld and ldo multiples of 8 (else LS_ERR_ARG). */
 int lsk_attn_fwd(const uint16_t* qkv, int64_t ld, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh,
                  int32_t nkv, int32_t head_dim, uint16_t* out, int64_t ldo, float* lse, int32_t T, void* stream);
 
 /* Causal GQA attention backward: from dout bf16 [T, lddo] and the forward's out and
  * lse, writes dq, dk, dv (fp32) into the q/k/v columns of dqkv [T, ldg].
- * d_scratch: fp32 [nh, T]. */
+ * d_scratch: fp32 [nh, T].  part: NULL, or fp32 scratch of (nh / nkv) * T * 2 * nkv *
+ * head_dim floats (16-byte aligned): dk / dv are then computed per query head by separate
+ * CTAs and summed in head order by a second kernel (more CTAs in flight; the same result
+ * to fp32 reassociation, and deterministic either way).  qkv, dout and dqkv 16-byte
+ * aligned; ld, lddo multiples of 8, ldg of 4. */
 int lsk_attn_bwd(const uint16_t* qkv, int64_t ld, const uint16_t* dout, const uint16_t* out, int64_t lddo,
                  const float* lse, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh, int32_t nkv,
-                 int32_t head_dim, float* d_scratch, float* dqkv, int64_t ldg, int32_t T, void* stream);
+                 int32_t head_dim, float* d_scratch, float* dqkv, int64_t ldg, int32_t T, float* part,
+                 void* stream);
 
 /* SwiGLU: h = bf16(silu(gate) * up) with gu = [gate | up] bf16 [T, 2I]; backward
  * from dh fp32 [T, I] to dgu bf16 [T, 2I]. */
@@ -209,6 +215,14 @@ int lsk_vocab_logprob(const uint16_t* h, int32_t T, int32_t H, const uint8_t* w_
 int lsk_vocab_bwd(const uint16_t* h, int32_t T, int32_t H, const uint8_t* w_packed, const float* w_absmax,
                   int32_t v0, int32_t n, const int32_t* targets, const float* lse, const float* coef,
                   uint16_t* dlogits, float* dh, int32_t accumulate, void* stream);
+
+/* The bounded device wait every cross-CTA handshake of these kernels uses (the split
+ * GEMM's partial tiles), on its own: one thread waits until the uint32 at flag equals
+ * value or limit_ns nanoseconds (device %globaltimer) have passed, then writes status
+ * (int32, device): 0 = seen, 1 = the limit ran out, in which case the device error word
+ * (lsk_device_error) is also raised.  The kernel returns either way; the context stays
+ * usable.  Lets a caller check the failure path of a wait with a flag nothing sets. */
+int lsk_wait_flag(const uint32_t* flag, uint32_t value, int64_t limit_ns, int32_t* status, void* stream);
 
 /* Device error flag raised by kernels whose bounded waits ran out (0 = none). */
 int lsk_device_error(int32_t* h_out, int32_t reset);

@@ -120,7 +120,7 @@ _SIGS = {
     "lsk_rope_fwd": [P, I64, P, P, P, I32, I32, I32, P],
     "lsk_rope_bwd_cast": [P, P, I64, P, P, P, I32, I32, I32, I32, P],
     "lsk_attn_fwd": [P, I64, P, I32, I32, I32, I32, I32, P, I64, P, I32, P],
-    "lsk_attn_bwd": [P, I64, P, P, I64, P, P, I32, I32, I32, I32, I32, P, P, I64, I32, P],
+    "lsk_attn_bwd": [P, I64, P, P, I64, P, P, I32, I32, I32, I32, I32, P, P, I64, I32, P, P],
     "lsk_swiglu_fwd": [P, P, I32, I32, P],
     "lsk_swiglu_bwd": [P, P, P, I32, I32, P],
     "lsk_lora_down": [P, I64, P, P, I32, I32, F32, P, I32, P],
@@ -132,6 +132,7 @@ _SIGS = {
     "lsk_embed_gather": [P, P, P, I32, P, I32, I32, P],
     "lsk_vocab_logprob": [P, I32, I32, P, P, I32, P, P, P, P, P, P],
     "lsk_vocab_bwd": [P, I32, I32, P, P, I32, I32, P, P, P, P, P, I32, P],
+    "lsk_wait_flag": [P, C.c_uint32, I64, P, P],
     "lsk_device_error": [C.POINTER(I32), I32],
 }
 

@@ -29,6 +29,7 @@
 #include "gemm_host.cuh"
 #include "pointwise.cuh"
 #include "attention.cuh"
+#include "attention_tc.cuh"
 #include "ls.h"
 #include "ls_kernels.h"
 
@@ -583,46 +584,62 @@ cudaError_t gemm(int mode, const bf16* A, long long lda, int M, const uint8_t* W
   return ls::launch_nf4_gemm(c, st);
 }
 
+// The tensor-core forward: qkv and out 16-byte aligned, ld and ldo multiples of 8.
 template <int HD>
-cudaError_t attn_fwd_launch(const bf16* qkv, long long ld, const int* cu, int nseq, int maxlen, int nh, int nkv,
-                            bf16* out, long long ldo, float* lse, int T, cudaStream_t st) {
-  const int smem = 5 * 64 * (HD + 8) * 2;   // Q + two (K, V) buffers
+cudaError_t attn_fwd_tc_launch(const bf16* qkv, long long ld, const int* cu, int nseq, int maxlen, int nh, int nkv,
+                               bf16* out, long long ldo, float* lse, int T, cudaStream_t st) {
+  using C = ls::AttnTcCfg<HD>;
+  if (T <= 0) return cudaSuccess;
   static std::atomic<uint64_t> attr{0};
   {
-    const cudaError_t e = ls::ensure_smem_attr(ls::attn_fwd_kernel<HD>, smem, attr);
+    const cudaError_t e = ls::ensure_smem_attr(ls::attn_fwd_tc_kernel<HD>, C::SMEM, attr);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid((maxlen + 63) / 64, nh, nseq);
-  ls::attn_fwd_kernel<HD><<<grid, 128, smem, st>>>(qkv, ld, cu, nh, nkv, 1.0f / sqrtf((float)HD), out, ldo, lse, T);
+  CUtensorMap tm;
+  if (!ls::make_map_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)ld, (uint64_t)T, (uint64_t)ld * 2, 64,
+                       64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const int ntq = (maxlen + C::BM - 1) / C::BM;
+  dim3 grid((unsigned)nh, (unsigned)nseq, (unsigned)ntq);
+  ls::attn_fwd_tc_kernel<HD><<<grid, C::THREADS, C::SMEM, st>>>(tm, cu, nh, nkv, 1.0f / sqrtf((float)HD), out, ldo,
+                                                                 lse, T, ntq);
   return cudaGetLastError();
 }
 
-// part (fp32, >= (nh / nkv) * T * 2 * nkv * HD): split each KV group's query heads
-// over CTAs (one head each) and sum the per-head dk / dv in head order; without it
-// one CTA loops over the whole group.
+// The tensor-core backward: qkv, dout and dqkv 16-byte aligned; ld, lddo multiples of 8,
+// ldg of 4.  part (fp32, >= (nh / nkv) * T * 2 * nkv * HD): dK / dV per query head in
+// separate CTAs, summed in head order by a second kernel; without it one CTA takes the
+// whole key/value group.
 template <int HD>
-cudaError_t attn_bwd_launch(const bf16* qkv, long long ld, const bf16* dout, const bf16* o, long long lddo,
-                            const float* lse, const int* cu, int nseq, int maxlen, int nh, int nkv, float* D,
-                            float* dqkv, long long ldg, int T, cudaStream_t st, float* part = nullptr) {
-  const int smem_q = 6 * 64 * (HD + 8) * 2;                  // Q, dO + two (K, V) buffers
-  const int smem_k = 6 * 64 * (HD + 8) * 2 + 4 * 64 * 4;     // K, V + two (Q, dO, lse, D) buffers
+cudaError_t attn_bwd_tc_launch(const bf16* qkv, long long ld, const bf16* dout, const bf16* o, long long lddo,
+                               const float* lse, const int* cu, int nseq, int maxlen, int nh, int nkv, float* D,
+                               float* dqkv, long long ldg, int T, cudaStream_t st, float* part) {
+  using C = ls::AttnBwdTcCfg<HD>;
+  if (T <= 0) return cudaSuccess;
   static std::atomic<uint64_t> attr_q{0}, attr_k{0};
   {
-    cudaError_t e = ls::ensure_smem_attr(ls::attn_bwd_dq_kernel<HD>, smem_q, attr_q);
-    if (e == cudaSuccess) e = ls::ensure_smem_attr(ls::attn_bwd_dkdv_kernel<HD>, smem_k, attr_k);
+    cudaError_t e = ls::ensure_smem_attr(ls::attn_bwd_dq_tc_kernel<HD>, C::SMEM_Q, attr_q);
+    if (e == cudaSuccess) e = ls::ensure_smem_attr(ls::attn_bwd_dkdv_tc_kernel<HD>, C::SMEM_K, attr_k);
     if (e != cudaSuccess) return e;
   }
+  CUtensorMap tq, td;
+  if (!ls::make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)ld, (uint64_t)T, (uint64_t)ld * 2, 64,
+                       64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !ls::make_map_2d(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dout, (uint64_t)lddo, (uint64_t)T, (uint64_t)lddo * 2,
+                       64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   const float scale = 1.0f / sqrtf((float)HD);
   {
     const long long w = (long long)T * nh;
     ls::attn_bwd_dot_kernel<<<(unsigned)((w + 7) / 8), 256, 0, st>>>(dout, o, lddo, nh, HD, D, T);
   }
-  dim3 gq((maxlen + 63) / 64, nh, nseq);
-  ls::attn_bwd_dq_kernel<HD><<<gq, 128, smem_q, st>>>(qkv, ld, dout, lddo, lse, D, cu, nh, nkv, scale, dqkv, ldg, T);
+  const int nt = (maxlen + 127) / 128;
+  ls::attn_bwd_dq_tc_kernel<HD><<<dim3((unsigned)nh, (unsigned)nseq, (unsigned)nt), C::THREADS, C::SMEM_Q, st>>>(
+      tq, td, lse, D, cu, nh, nkv, scale, dqkv, ldg, T, nt);
   const int hsplit = part ? nh / nkv : 1;
-  dim3 gk((maxlen + 63) / 64, nkv * hsplit, nseq);
-  ls::attn_bwd_dkdv_kernel<HD><<<gk, 128, smem_k, st>>>(qkv, ld, dout, lddo, lse, D, cu, nh, nkv, scale, dqkv, ldg, T,
-                                                        hsplit, part);
+  ls::attn_bwd_dkdv_tc_kernel<HD>
+      <<<dim3((unsigned)(nkv * hsplit), (unsigned)nseq, (unsigned)nt), C::THREADS, C::SMEM_K, st>>>(
+          tq, td, lse, D, cu, nh, nkv, scale, dqkv, ldg, T, hsplit, part);
   if (hsplit > 1) {
     const long long n4 = (long long)T * 2 * nkv * HD / 4;
     ls::attn_dkdv_reduce_kernel<<<grid1d(n4, 256), 256, 0, st>>>(part, hsplit, nh, nkv, HD, T, dqkv, ldg);
@@ -632,15 +649,16 @@ cudaError_t attn_bwd_launch(const bf16* qkv, long long ld, const bf16* dout, con
 
 cudaError_t attn_fwd(int hd, const bf16* qkv, long long ld, const int* cu, int nseq, int maxlen, int nh, int nkv,
                      bf16* out, long long ldo, float* lse, int T, cudaStream_t st) {
-  return hd == 64 ? attn_fwd_launch<64>(qkv, ld, cu, nseq, maxlen, nh, nkv, out, ldo, lse, T, st)
-                  : attn_fwd_launch<128>(qkv, ld, cu, nseq, maxlen, nh, nkv, out, ldo, lse, T, st);
+  return hd == 64 ? attn_fwd_tc_launch<64>(qkv, ld, cu, nseq, maxlen, nh, nkv, out, ldo, lse, T, st)
+                  : attn_fwd_tc_launch<128>(qkv, ld, cu, nseq, maxlen, nh, nkv, out, ldo, lse, T, st);
 }
 cudaError_t attn_bwd(int hd, const bf16* qkv, long long ld, const bf16* dout, const bf16* o, long long lddo,
                      const float* lse, const int* cu, int nseq, int maxlen, int nh, int nkv, float* D, float* dqkv,
                      long long ldg, int T, cudaStream_t st, float* part = nullptr) {
   return hd == 64
-             ? attn_bwd_launch<64>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st, part)
-             : attn_bwd_launch<128>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st, part);
+             ? attn_bwd_tc_launch<64>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st, part)
+             : attn_bwd_tc_launch<128>(qkv, ld, dout, o, lddo, lse, cu, nseq, maxlen, nh, nkv, D, dqkv, ldg, T, st,
+                                       part);
 }
 
 cudaError_t lora_outer(const bf16* X, long long ldx, int ncols, const float* Uf, const bf16* Ub, int ldu, int r, int T,
@@ -1922,7 +1940,8 @@ int lsk_rope_bwd_cast(const float* g, uint16_t* out, int64_t ld, const int32_t* 
 int lsk_attn_fwd(const uint16_t* qkv, int64_t ld, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh,
                  int32_t nkv, int32_t hd, uint16_t* out, int64_t ldo, float* lse, int32_t T, void* s) {
   if (!qkv || !cu || !out || !lse || nseq < 1 || max_len < 1 || nh < 1 || nkv < 1 || nh % nkv ||
-      (hd != 64 && hd != 128) || ld < (int64_t)(nh + 2 * nkv) * hd || ld % 8 || ldo % 8)
+      (hd != 64 && hd != 128) || ld < (int64_t)(nh + 2 * nkv) * hd || ld % 8 || ldo % 8 ||
+      (reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
     return set_thread_err(LS_ERR_ARG, "lsk_attn_fwd: bad args");
   KCK(attn_fwd(hd, reinterpret_cast<const bf16*>(qkv), ld, cu, nseq, max_len, nh, nkv, reinterpret_cast<bf16*>(out),
                ldo, lse, T, STREAM(s)));
@@ -1931,12 +1950,15 @@ int lsk_attn_fwd(const uint16_t* qkv, int64_t ld, const int32_t* cu, int32_t nse
 
 int lsk_attn_bwd(const uint16_t* qkv, int64_t ld, const uint16_t* dout, const uint16_t* o, int64_t lddo,
                  const float* lse, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh, int32_t nkv,
-                 int32_t hd, float* D, float* dqkv, int64_t ldg, int32_t T, void* s) {
-  if (!qkv || !dout || !o || !lse || !cu || !D || !dqkv || nseq < 1 || max_len < 1 || nh % nkv ||
-      (hd != 64 && hd != 128) || ld % 8 || lddo % 8 || ldg % 2)
+                 int32_t hd, float* D, float* dqkv, int64_t ldg, int32_t T, float* part, void* s) {
+  if (!qkv || !dout || !o || !lse || !cu || !D || !dqkv || nseq < 1 || max_len < 1 || nh < 1 || nkv < 1 || nh % nkv ||
+      (hd != 64 && hd != 128) || ld % 8 || lddo % 8 || ldg % 4 ||
+      ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv) |
+        reinterpret_cast<uintptr_t>(part)) & 15))
     return set_thread_err(LS_ERR_ARG, "lsk_attn_bwd: bad args");
   KCK(attn_bwd(hd, reinterpret_cast<const bf16*>(qkv), ld, reinterpret_cast<const bf16*>(dout),
-               reinterpret_cast<const bf16*>(o), lddo, lse, cu, nseq, max_len, nh, nkv, D, dqkv, ldg, T, STREAM(s)));
+               reinterpret_cast<const bf16*>(o), lddo, lse, cu, nseq, max_len, nh, nkv, D, dqkv, ldg, T, STREAM(s),
+               nh > nkv ? part : nullptr));
   return LS_OK;
 }
 
@@ -2120,6 +2142,14 @@ int lsk_vocab_bwd(const uint16_t* h, int32_t T, int32_t H, const uint8_t* wp, co
   KCK(ls::launch_nf4_gemm(g, STREAM(s)));
   KCK(gemm(ls::GEMM_DX, reinterpret_cast<const bf16*>(dlogits), n, T, wp, wa, n, H, nullptr, nullptr, 0,
            accumulate ? ls::EPI_F32_ACC : ls::EPI_F32, dh, H, nullptr, 0, STREAM(s)));
+  return LS_OK;
+}
+
+int lsk_wait_flag(const uint32_t* flag, uint32_t value, int64_t limit_ns, int32_t* status, void* s) {
+  if (!flag || !status || limit_ns < 0 || (reinterpret_cast<uintptr_t>(flag) & 3))
+    return set_thread_err(LS_ERR_ARG, "lsk_wait_flag: bad args");
+  ls::wait_flag_kernel<<<1, 32, 0, STREAM(s)>>>(flag, value, (unsigned long long)limit_ns, status);
+  KLAUNCH();
   return LS_OK;
 }
 

@@ -10,6 +10,14 @@
 
 namespace ls {
 
+// ------------------------------------------------------------------ bounded waits
+// One thread waits, through the same bounded loop as the split GEMM's partial-tile
+// exchange, until *flag == value or limit_ns has passed; status 0 = seen, 1 = ran out.
+__global__ void wait_flag_kernel(const unsigned* flag, unsigned value, unsigned long long limit_ns, int* status) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  *status = flag_wait_eq(flag, value, limit_ns) ? 0 : 1;
+}
+
 // ------------------------------------------------------------------ RMSNorm
 // y = bf16(w * bf16(x * rstd)), rstd = 1 / sqrt(mean(x^2) + eps)   (x bf16 [T, H])
 __global__ void rmsnorm_fwd_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,

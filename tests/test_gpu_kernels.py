@@ -184,6 +184,31 @@ def test_embed_gather_rows_and_out_of_range_ids():
     assert L.lib().lsk_device_error(ctypes.byref(e), 1) == 0 and e.value == 0
 
 
+# ------------------------------------------------------------------ bounded waits
+
+def test_bounded_wait_runs_out_and_context_stays_usable():
+    """A wait on a flag that nothing sets ends after its limit with status 1 and the
+    device error word 1 (wait timeout); a flag already set is seen at once (status 0,
+    no error); later kernels run normally on the same context."""
+    flag = torch.zeros(4, dtype=torch.int32, device=DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    e = ctypes.c_int32(0)
+    assert L.lib().lsk_device_error(ctypes.byref(e), 1) == 0
+    k("lsk_wait_flag", flag, 1, 20_000_000, status)          # 20 ms, nobody sets it
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    assert L.lib().lsk_device_error(ctypes.byref(e), 1) == 0 and e.value == 1
+    flag.fill_(7)
+    status.fill_(-1)
+    k("lsk_wait_flag", flag, 7, 20_000_000, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert L.lib().lsk_device_error(ctypes.byref(e), 1) == 0 and e.value == 0
+    assert L.lib().lsk_wait_flag(flag.data_ptr() + 2, 0, 1000, status.data_ptr(), stream()) == L.LS_ERR_ARG
+    x = torch.ones(1024, device=DEV)
+    assert float((x * 2).sum()) == 2048.0
+
+
 # ------------------------------------------------------------------ norms, rope, swiglu
 
 @pytest.mark.parametrize("T,H", [(5, 64), (512, 896), (1024, 4096), (37, 5120)])
@@ -275,6 +300,8 @@ ATT_CASES = [
     (128, 32, 8, [0, 512, 1024]),
     (128, 4, 1, [0, 1, 66, 200]),     # length-1 sequence, ragged tiles
     (64, 4, 4, [0, 130]),
+    (128, 40, 8, [0, 1000, 2048]),    # 32B head layout, the longest sequence, ragged 128-row tiles
+    (64, 16, 2, [0, 0, 300, 1000]),   # an empty sequence among ragged ones
 ]
 
 
@@ -299,23 +326,80 @@ def test_attention_fwd_bwd(hd, nh, nkv, cu):
     dscr = torch.empty((nh, T), dtype=torch.float32, device=DEV)
     dq = torch.zeros((T, ncols), dtype=torch.float32, device=DEV)
     dod = bf16_dev(do)
-    k("lsk_attn_bwd", qd, ncols, dod, o, nh * hd, lse, cud, len(cu) - 1, maxlen, nh, nkv, hd, dscr, dq, ncols, T)
+    k("lsk_attn_bwd", qd, ncols, dod, o, nh * hd, lse, cud, len(cu) - 1, maxlen, nh, nkv, hd, dscr, dq, ncols, T,
+      None)
+    grads = [dq]
+    if nh > nkv:
+        # dk / dv per query head in separate CTAs, summed in head order by a second kernel
+        part = torch.empty((nh // nkv) * T * 2 * nkv * hd, dtype=torch.float32, device=DEV)
+        dq2 = torch.zeros((T, ncols), dtype=torch.float32, device=DEV)
+        k("lsk_attn_bwd", qd, ncols, dod, o, nh * hd, lse, cud, len(cu) - 1, maxlen, nh, nkv, hd, dscr, dq2, ncols,
+          T, part)
+        grads.append(dq2)
     torch.cuda.synchronize()
     assert rel_err(to_np(o), ref.detach().reshape(T, -1).numpy()) <= TOL
-    g = to_np(dq)
-    assert rel_err(g[:, :nh * hd], Q.grad.reshape(T, -1).numpy()) <= TOL
-    assert rel_err(g[:, nh * hd:(nh + nkv) * hd], K_.grad.reshape(T, -1).numpy()) <= TOL
-    assert rel_err(g[:, (nh + nkv) * hd:], V.grad.reshape(T, -1).numpy()) <= TOL
+    for gd in grads:
+        g = to_np(gd)
+        assert rel_err(g[:, :nh * hd], Q.grad.reshape(T, -1).numpy()) <= TOL
+        assert rel_err(g[:, nh * hd:(nh + nkv) * hd], K_.grad.reshape(T, -1).numpy()) <= TOL
+        assert rel_err(g[:, (nh + nkv) * hd:], V.grad.reshape(T, -1).numpy()) <= TOL
+    if len(grads) == 2:
+        # dq is the same kernel either way; dk / dv differ only in summation order
+        a_, b_ = to_np(grads[0]), to_np(grads[1])
+        assert np.array_equal(a_[:, :nh * hd], b_[:, :nh * hd])
+        assert rel_err(b_[:, nh * hd:], a_[:, nh * hd:]) <= 1e-5
     # log-sum-exp of the scaled scores
     lo = to_np(lse)
     for si in range(len(cu) - 1):
         a, b = cu[si], cu[si + 1]
+        if b == a:
+            continue
         qs = om.t64(qkv[a:b, :nh * hd]).view(b - a, nh, hd).transpose(0, 1)
         ks = om.t64(qkv[a:b, nh * hd:(nh + nkv) * hd]).view(b - a, nkv, hd).transpose(0, 1).repeat_interleave(nh // nkv, 0)
         sc = qs @ ks.transpose(1, 2) / math.sqrt(hd)
         sc = sc.masked_fill(torch.triu(torch.ones(b - a, b - a, dtype=torch.bool), 1), float("-inf"))
         want = torch.logsumexp(sc, -1).numpy()
         assert np.abs(lo[:, a:b] - want).max() <= 1e-3
+
+
+def test_attention_masks_and_head_groups_exactly():
+    """With q = 0 every score is exactly 0, so each row averages the values of exactly the
+    keys it may see (causal, inside its own sequence) with weight 1 / (r + 1), and
+    lse = ln(r + 1).  The log-sum-exp pins how many keys each row saw to fp32 precision;
+    value columns holding the bits of the key's position pin which keys they were; a
+    value column holding the key/value head index pins the query-head grouping (exact).
+    Ragged sequences, a length-1 one and a 512-long one (four 128-row query tiles)."""
+    hd, nh, nkv = 128, 8, 2
+    cu = [0, 1, 66, 200, 712]
+    T = cu[-1]
+    ncols = (nh + 2 * nkv) * hd
+    pos = np.concatenate([np.arange(b - a) for a, b in zip(cu[:-1], cu[1:])])
+    qkv = np.zeros((T, ncols), np.float32)
+    qkv[:, nh * hd:(nh + nkv) * hd] = synth.gaussian((T, nkv * hd), 60, T)   # any keys: q = 0
+    for g in range(nkv):
+        vc = (nh + nkv + g) * hd
+        for b in range(9):
+            qkv[:, vc + b] = (pos >> b) & 1
+        qkv[:, vc + hd - 1] = g
+    qd = bf16_dev(qkv)
+    cud = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    o = torch.empty((T, nh * hd), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((nh, T), dtype=torch.float32, device=DEV)
+    k("lsk_attn_fwd", qd, ncols, cud, len(cu) - 1, 512, nh, nkv, hd, o, nh * hd, lse, T)
+    torch.cuda.synchronize()
+    got = to_np(o).reshape(T, nh, hd)
+    lo = to_np(lse)
+    np.testing.assert_allclose(lo, np.broadcast_to(np.log(pos + 1.0), (nh, T)), rtol=0, atol=2e-5)
+    for b in range(9):
+        # fraction of positions 0..r with bit b set
+        bits = (pos >> b) & 1
+        want = np.empty(T)
+        for a, e in zip(cu[:-1], cu[1:]):
+            want[a:e] = np.cumsum(bits[a:e]) / (pos[a:e] + 1.0)
+        for h in range(nh):
+            assert np.abs(got[:, h, b] - want).max() <= 2.0 ** -8 * np.abs(want).max() + 1e-6, (b, h)
+    for h in range(nh):
+        assert (got[:, h, hd - 1] == h // (nh // nkv)).all()
 
 
 # ------------------------------------------------------------------ vocabulary logprobs
