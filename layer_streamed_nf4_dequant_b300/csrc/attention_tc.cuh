@@ -51,6 +51,8 @@ struct AttnTcCfg {
   // column offsets: O, then two S buffers (P_j, bf16 pairs, over the first BN / 2 columns)
   static constexpr int T_O = 0, T_S = HD;
   static constexpr int THREADS = 192;
+  // epilogue staging: four warps x 32 padded bf16 rows over the idle Q and K space
+  static_assert(4 * 32 * (HD * 2 + 16) <= OFF_V, "output staging");
 };
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -286,25 +288,35 @@ __global__ void __launch_bounds__(192, 2)
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
-      __nv_bfloat16* orow = out + (size_t)(a + row) * ldo + (size_t)h * HD;
+      // O / l as bf16 rows, staged in this warp's part of the (now idle) Q / K space, then
+      // written out a row at a time by the whole warp (coalesced)
+      constexpr int RS = HD * 2 + 16;   // padded row: consecutive lanes hit different banks
+      uint8_t* stg = base + C::OFF_Q + q * 32 * RS;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t o[32];
         tmem_ld_32x32b_x32(tl + C::T_O + c * 32, o);
         tmem_ld_wait();
-        if (row < L) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = w;
-          }
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+          *reinterpret_cast<uint4*>(stg + lane * RS + c * 64 + v * 16) = w;
         }
       }
       if (row < L) lse[(size_t)h * T + a + row] = (m_used + log2f(l)) * 0.6931471805599453f;
+      __syncwarp();
+      const int rlast = min(32, L - (q0 + q * 32));   // rows of this warp inside the sequence
+      for (int i = 0; i < rlast; ++i) {
+        __nv_bfloat16* orow = out + (size_t)(a + q0 + q * 32 + i) * ldo + (size_t)h * HD;
+        if constexpr (HD == 128)
+          *reinterpret_cast<uint2*>(orow + lane * 4) = *reinterpret_cast<const uint2*>(stg + i * RS + lane * 8);
+        else
+          *reinterpret_cast<uint32_t*>(orow + lane * 2) = *reinterpret_cast<const uint32_t*>(stg + i * RS + lane * 4);
+      }
     } else {
       s_abort = 1;
     }
@@ -354,6 +366,8 @@ struct AttnBwdTcCfg {
   // 64 columns, so that every SM sub-partition runs two of them
   static constexpr int THREADS = 64 + 256;
   static constexpr int NSOFT = 8;
+  // epilogue staging: eight warps x 32 padded rows over the idle operand space
+  static_assert(8 * 32 * (HD * 2 + 16) <= Q_OFF_BAR && 8 * 32 * (128 + 16) <= K_OFF_BAR, "output staging");
 };
 
 template <int HD>
@@ -548,19 +562,30 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
     if (ok) ok = wwait(ds_done((nkt - 1) & 1), ((nkt - 1) >> 1) & 1);
     if (ok) {
       tc_fence_after();
-      float* grow = dqkv + (size_t)(a + row) * ldg + (size_t)h * HD;
+      // this warp's half of its 32 dQ rows, staged in the idle Q / dO / K / V space, then
+      // written out a row at a time by the whole warp (coalesced)
+      constexpr int HB = HD * 2;        // bytes of a half row (HD / 2 fp32)
+      constexpr int RS = HB + 16;
+      uint8_t* stg = base + (warp - 2) * 32 * RS;
 #pragma unroll
-      for (int c = hf * (HD / 64); c < (hf + 1) * (HD / 64); ++c) {
+      for (int c = 0; c < HD / 64; ++c) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(tl + C::DQ_ACC + c * 32, o);
+        tmem_ld_32x32b_x32(tl + C::DQ_ACC + hf * (HD / 2) + c * 32, o);
         tmem_ld_wait();
-        if (row < L) {
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            *reinterpret_cast<float4*>(grow + c * 32 + v * 4) =
-                make_float4(__uint_as_float(o[4 * v]) * scale, __uint_as_float(o[4 * v + 1]) * scale,
-                            __uint_as_float(o[4 * v + 2]) * scale, __uint_as_float(o[4 * v + 3]) * scale);
-        }
+        for (int v = 0; v < 8; ++v)
+          *reinterpret_cast<float4*>(stg + lane * RS + c * 128 + v * 16) =
+              make_float4(__uint_as_float(o[4 * v]) * scale, __uint_as_float(o[4 * v + 1]) * scale,
+                          __uint_as_float(o[4 * v + 2]) * scale, __uint_as_float(o[4 * v + 3]) * scale);
+      }
+      __syncwarp();
+      const int rlast = min(32, L - (q0 + qw * 32));
+      for (int i = 0; i < rlast; ++i) {
+        float* grow = dqkv + (size_t)(a + q0 + qw * 32 + i) * ldg + (size_t)h * HD + hf * (HD / 2);
+        if constexpr (HD == 128)
+          *reinterpret_cast<float2*>(grow + lane * 2) = *reinterpret_cast<const float2*>(stg + i * RS + lane * 8);
+        else
+          grow[lane] = *reinterpret_cast<const float*>(stg + i * RS + lane * 4);
       }
     } else {
       s_abort = 1;
@@ -803,14 +828,15 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
     if (ok && nit > 0) ok = wwait(pd_done((nit - 1) & 1), ((nit - 1) >> 1) & 1);
     if (ok) {
       if (nit > 0) tc_fence_after();
-      float* krow = hsplit > 1 ? part + ((size_t)hs * T + a + key) * (2 * nkv * HD) + (size_t)g * HD
-                               : dqkv + (size_t)(a + key) * ldg + (size_t)(nh + g) * HD;
-      float* vrow = hsplit > 1 ? krow + (size_t)nkv * HD : dqkv + (size_t)(a + key) * ldg + (size_t)(nh + nkv + g) * HD;
-      // half 0 writes dK, half 1 dV
+      // half 0 writes dK, half 1 dV: HD / 64 passes of 32 columns per row, each staged in
+      // this warp's part of the idle K / V / Q / dO space and written out a row at a time
+      // by the whole warp (coalesced)
       {
         const int w = hf;
-        float* dst = w == 0 ? krow : vrow;
         const float f = w == 0 ? scale : 1.f;
+        constexpr int RS = 128 + 16;
+        uint8_t* stg = base + (warp - 2) * 32 * RS;
+        const int rlast = min(32, L - (k0 + qw * 32));
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t o[32];
@@ -821,12 +847,19 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
 #pragma unroll
             for (int v = 0; v < 32; ++v) o[v] = 0u;
           }
-          if (key < L) {
+          __syncwarp();   // the previous pass's rows have been read out
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              *reinterpret_cast<float4*>(dst + c * 32 + v * 4) =
-                  make_float4(__uint_as_float(o[4 * v]) * f, __uint_as_float(o[4 * v + 1]) * f,
-                              __uint_as_float(o[4 * v + 2]) * f, __uint_as_float(o[4 * v + 3]) * f);
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(stg + lane * RS + v * 16) =
+                make_float4(__uint_as_float(o[4 * v]) * f, __uint_as_float(o[4 * v + 1]) * f,
+                            __uint_as_float(o[4 * v + 2]) * f, __uint_as_float(o[4 * v + 3]) * f);
+          __syncwarp();
+          for (int i = 0; i < rlast; ++i) {
+            const int kr = k0 + qw * 32 + i;
+            float* dst = hsplit > 1
+                             ? part + ((size_t)hs * T + a + kr) * (2 * nkv * HD) + (size_t)(w * nkv + g) * HD
+                             : dqkv + (size_t)(a + kr) * ldg + (size_t)(nh + w * nkv + g) * HD;
+            dst[c * 32 + lane] = *reinterpret_cast<const float*>(stg + i * RS + lane * 4);
           }
         }
       }
