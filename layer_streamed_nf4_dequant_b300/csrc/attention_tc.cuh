@@ -9,22 +9,24 @@
 // One CTA owns 128 query rows of one head and walks the key tiles (64 keys each) up to
 // the diagonal.  Per key tile j:
 //   S_j = Q K_j^T      tcgen05.mma, Q and K_j in shared memory (TMA, 128-byte swizzle),
-//                      S_j (128 x 64 fp32) in tensor-memory buffer j % 2;
+//                      S_j (128 x 64 fp32) in tensor memory;
 //   P_j = exp2(S_j c - m)  the softmax warps read S_j row by row (thread = row) and write
-//                      P_j as bf16 over the first half of the same buffer;
+//                      P_j as bf16 into one of two tensor-memory P buffers;
 //   O += P_j V_j       tcgen05.mma with A = P_j from tensor memory, B = V_j MN-major in
 //                      shared memory, O (128 x hd fp32) in tensor memory.
-// S_{j+2} is issued into buffer j % 2 once P_j V_j has finished, so the tensor core
-// computes the next scores while the softmax warps work on this tile, and the softmax
-// warps never wait for a P V product except to rescale O.  The running maximum m is moved
-// only when a row's maximum grows by more than 8 (a factor 256 in the exponentials): O
-// and the row sum l are then rescaled together, otherwise both keep the stale m, which
-// changes no result since o = O / l and lse = m + log2 l use the same m.  K and V have
-// rings of their own (K_j is free once S_j is done, V_j once P_j V_j is).
+// S_{j+1} is issued as soon as the softmax warps have read S_j out, so the tensor core
+// computes the next scores while they work on this tile; with two P buffers they wait
+// for a P V product only to rescale O or to reuse its buffer two tiles later.  K and V
+// have rings of their own, each fed by its own producer lane: K_{j+2} needs only S_j to
+// be done, V_{j+2} only P_j V_j.  The running maximum m is moved only when a row's
+// maximum grows by more than 8 (a factor 256 in the exponentials): O and the row sum l
+// are then rescaled together, otherwise both keep the stale m, which changes no result
+// since o = O / l and lse = m + log2 l use the same m.
 //
-// Warps: 0 = TMA producer, 1 = tensor-memory owner and MMA issuer, 2..5 = softmax and
-// epilogue (warp w reads tensor-memory lanes 32 (w % 4) .. + 31).  Every wait is
-// bounded; a timeout raises the device error word and the CTA winds down.
+// Warps: 0 = TMA producers (lane 0: Q and K, lane 1: V), 1 = tensor-memory owner and MMA
+// issuer, 2..5 = softmax and epilogue (warp w reads tensor-memory lanes 32 (w % 4) ..
+// + 31).  Every wait is bounded; a timeout raises the device error word and the CTA
+// winds down.
 #pragma once
 #include "attention.cuh"
 #include "common.cuh"
@@ -48,9 +50,10 @@ struct AttnTcCfg {
   // at most two CTAs per SM, so that two tensor-memory allocations always fit
   static constexpr int SMEM = USED < 80 * 1024 ? 80 * 1024 : USED;
   static constexpr int TMEM_COLS = 256;
-  // column offsets: O, then two S buffers (P_j, bf16 pairs, over the first BN / 2 columns)
-  static constexpr int T_O = 0, T_S = HD;
+  // column offsets: O, S, two P buffers (bf16 pairs, BN / 2 columns each)
+  static constexpr int T_O = 0, T_S = HD, T_P = HD + BN;
   static constexpr int THREADS = 192;
+  static_assert(T_P + BN <= TMEM_COLS, "tensor-memory columns");
   // epilogue staging: four warps x 32 padded bf16 rows over the idle Q and K space
   static_assert(4 * 32 * (HD * 2 + 16) <= OFF_V, "output staging");
 };
@@ -86,12 +89,11 @@ __global__ void __launch_bounds__(192, 2)
   // Barriers come in pairs (index b = tile % 2) wherever one side may run a whole tile
   // ahead of the other, so that no waiter can find its phase overtaken by the next one.
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
-  const uint32_t q_full = bar(0), drain = bar(15);
+  const uint32_t q_full = bar(0), s_full = bar(9), s_cons = bar(10), drain = bar(15);
   auto k_full = [&](int b) -> uint32_t { return bar(1 + b); };
   auto k_empty = [&](int b) -> uint32_t { return bar(3 + b); };
   auto v_full = [&](int b) -> uint32_t { return bar(5 + b); };
   auto v_empty = [&](int b) -> uint32_t { return bar(7 + b); };
-  auto s_full = [&](int b) -> uint32_t { return bar(9 + b); };     // S_j computed
   auto p_full = [&](int b) -> uint32_t { return bar(11 + b); };    // P_j written
   auto pv_done = [&](int b) -> uint32_t { return bar(13 + b); };   // P_j V_j finished
 
@@ -102,10 +104,11 @@ __global__ void __launch_bounds__(192, 2)
       mbar_init(k_empty(b), 1);
       mbar_init(v_full(b), 1);
       mbar_init(v_empty(b), 1);
-      mbar_init(s_full(b), 1);
       mbar_init(p_full(b), 4);
       mbar_init(pv_done(b), 1);
     }
+    mbar_init(s_full, 1);
+    mbar_init(s_cons, 4);
     mbar_init(drain, 1);
     fence_barrier_init();
     s_abort = 0;
@@ -121,51 +124,48 @@ __global__ void __launch_bounds__(192, 2)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + C::OFF_SLOT);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ TMA producers
+    // lane 0: Q, then the K ring; lane 1: the V ring.  K_j goes into slot j % 2 once S_{j-2}
+    // is done, V_j once P_{j-2} V_{j-2} is.
+    if (lane < 2) {
       const int xq = h * HD, xk = (nh + g) * HD, xv = (nh + nkv + g) * HD;
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      const bool isv = lane == 1;
+      if (!isv) {
+        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
-      for (int p = 0; p < C::PANELS; ++p)
+        for (int p = 0; p < C::PANELS; ++p)
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_2d(sb + C::OFF_Q + p * 16384 + hf * 8192, &tm_qkv, xq + p * 64, a + q0 + hf * 64, q_full);
-      int nk = 0, nv = 0;   // tiles issued
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_2d(sb + C::OFF_Q + p * 16384 + hf * 8192, &tm_qkv, xq + p * 64, a + q0 + hf * 64, q_full);
+      }
+      const uint32_t ring = sb + (isv ? C::OFF_V : C::OFF_K);
+      const int x = isv ? xv : xk;
+      int n = 0;   // tiles issued
       bool ok = true;
-      for (int j = 0; ok && j < nkt; ++j) {
+      for (int j = 0; j < nkt; ++j) {
         const int b = j & 1;
-        // K_j into slot b once S_{j-2} is done, V_j once P_{j-2} V_{j-2} is
-        if (j >= 2 && (s_abort || !mbar_wait(k_empty(b), ((j - 2) >> 1) & 1))) {
+        if (j >= 2 && (s_abort || !mbar_wait(isv ? v_empty(b) : k_empty(b), ((j - 2) >> 1) & 1))) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(k_full(b), C::KV_BYTES);
+        const uint32_t fb = isv ? v_full(b) : k_full(b);
+        mbar_arrive_expect_tx(fb, C::KV_BYTES);
 #pragma unroll
         for (int p = 0; p < C::PANELS; ++p)
-          tma_load_2d(sb + C::OFF_K + b * C::KV_BYTES + p * 8192, &tm_qkv, xk + p * 64, a + j * C::BN, k_full(b));
-        ++nk;
-        if (j >= 2 && (s_abort || !mbar_wait(v_empty(b), ((j - 2) >> 1) & 1))) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(v_full(b), C::KV_BYTES);
-#pragma unroll
-        for (int p = 0; p < C::PANELS; ++p)
-          tma_load_2d(sb + C::OFF_V + b * C::KV_BYTES + p * 8192, &tm_qkv, xv + p * 64, a + j * C::BN, v_full(b));
-        ++nv;
+          tma_load_2d(ring + b * C::KV_BYTES + p * 8192, &tm_qkv, x + p * 64, a + j * C::BN, fb);
+        ++n;
       }
       if (!ok) s_abort = 1;
       // every copy issued has landed before the CTA's shared memory goes away
-      mbar_wait(q_full, 0);
-      for (int i = nk - 2 < 0 ? 0 : nk - 2; i < nk; ++i) mbar_wait(k_full(i & 1), (i >> 1) & 1);
-      for (int i = nv - 2 < 0 ? 0 : nv - 2; i < nv; ++i) mbar_wait(v_full(i & 1), (i >> 1) & 1);
+      if (!isv) mbar_wait(q_full, 0);
+      for (int i = n - 2 < 0 ? 0 : n - 2; i < n; ++i) mbar_wait(isv ? v_full(i & 1) : k_full(i & 1), (i >> 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc_bf16_f32(128, C::BN);
       constexpr uint32_t ID_O = idesc_bf16_f32(128, HD) | (1u << 16);   // B (= V) MN-major
-      // S_j = Q K_j^T into buffer j % 2, then release K slot j % 2
+      // S_j = Q K_j^T, then release K slot j % 2
       auto qk = [&](int j) -> bool {
         const int b = j & 1;
         if (s_abort || !mbar_wait(k_full(b), (j >> 1) & 1)) return false;
@@ -173,16 +173,18 @@ __global__ void __launch_bounds__(192, 2)
         const uint32_t kb = sb + C::OFF_K + b * C::KV_BYTES;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          tc_mma_bf16(tmem + C::T_S + b * C::BN, sw128_kmajor_desc(sb + C::OFF_Q + (kk >> 2) * 16384 + (kk & 3) * 32),
+          tc_mma_bf16(tmem + C::T_S, sw128_kmajor_desc(sb + C::OFF_Q + (kk >> 2) * 16384 + (kk & 3) * 32),
                       sw128_kmajor_desc(kb + (kk >> 2) * 8192 + (kk & 3) * 32), ID_S, kk > 0 ? 1u : 0u);
-        tc_commit(s_full(b));
+        tc_commit(s_full);
         tc_commit(k_empty(b));
         return true;
       };
-      bool ok = mbar_wait(q_full, 0) && qk(0) && (nkt < 2 || qk(1));
+      bool ok = mbar_wait(q_full, 0) && qk(0);
       for (int j = 0; ok && j < nkt; ++j) {
         const int b = j & 1;
-        if (s_abort || !mbar_wait(p_full(b), (j >> 1) & 1) || !mbar_wait(v_full(b), (j >> 1) & 1)) {
+        // S_{j+1} overwrites S_j once the softmax warps have read it out
+        if (j + 1 < nkt) ok = !s_abort && mbar_wait(s_cons, j & 1) && qk(j + 1);
+        if (!ok || s_abort || !mbar_wait(p_full(b), (j >> 1) & 1) || !mbar_wait(v_full(b), (j >> 1) & 1)) {
           ok = false;
           break;
         }
@@ -190,12 +192,10 @@ __global__ void __launch_bounds__(192, 2)
         const uint32_t vb = sb + C::OFF_V + b * C::KV_BYTES;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          tc_mma_bf16_ts(tmem + C::T_O, tmem + C::T_S + b * C::BN + kk * 8, sw128_mnmajor_desc(vb + kk * 2048, 8192),
-                         ID_O, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_bf16_ts(tmem + C::T_O, tmem + C::T_P + b * (C::BN / 2) + kk * 8,
+                         sw128_mnmajor_desc(vb + kk * 2048, 8192), ID_O, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(pv_done(b));
         tc_commit(v_empty(b));
-        // S_{j+2} overwrites P_j: only once P_j V_j has read it
-        if (j + 2 < nkt) ok = !s_abort && mbar_wait(pv_done(b), (j >> 1) & 1) && qk(j + 2);
       }
       if (!ok) s_abort = 1;
       // every MMA issued has completed before tensor memory is freed
@@ -218,15 +218,18 @@ __global__ void __launch_bounds__(192, 2)
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
       const int b = j & 1;
-      if (!wwait(s_full(b), (j >> 1) & 1)) {
+      if (!wwait(s_full, j & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sv[64];
-      tmem_ld_32x32b_x32(tl + C::T_S + b * C::BN, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld_32x32b_x32(tl + C::T_S + b * C::BN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld_32x32b_x32(tl + C::T_S, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld_32x32b_x32(tl + C::T_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_cons);
       const int k0 = j * C::BN;
       float x[64];
       float tmax = -INFINITY;
@@ -261,6 +264,14 @@ __global__ void __launch_bounds__(192, 2)
         pk[i] = pack_bf16x2(p0, p1);
       }
       l = l * alpha + sum;
+      // P buffer j % 2 was last read by P_{j-2} V_{j-2}
+      if (j >= 2) {
+        if (!wwait(pv_done(b), ((j - 2) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
       // O is rescaled once it holds P_{j-1} V_{j-1}
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         if (!wwait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1)) {
@@ -278,7 +289,7 @@ __global__ void __launch_bounds__(192, 2)
           tmem_st_32x32b_x32(tl + C::T_O + c * 32, o);
         }
       }
-      tmem_st_32x32b_x32(tl + C::T_S + b * C::BN, pk);
+      tmem_st_32x32b_x32(tl + C::T_P + b * (C::BN / 2), pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -346,12 +357,13 @@ struct AttnBwdTcCfg {
   static constexpr int T128 = 128 * HD * 2;   // 128 rows x HD (PANELS x [128 rows x 128 B])
   static constexpr int T64 = 64 * HD * 2;     // 64 rows x HD  (PANELS x [64 rows x 128 B])
   // dQ kernel: Q, dO (128 query rows); stages of (K, V) (64 keys)
+  static constexpr int NST = 3;               // stages of the streamed operand ring
   static constexpr int Q_OFF_Q = 0, Q_OFF_DO = T128, Q_OFF_KV = 2 * T128;
-  static constexpr int Q_OFF_BAR = Q_OFF_KV + 4 * T64;
+  static constexpr int Q_OFF_BAR = Q_OFF_KV + NST * 2 * T64;
   // dK/dV kernel: K, V (128 keys); stages of (Q, dO) (64 query rows), then lse / D rows
   static constexpr int K_OFF_K = 0, K_OFF_V = T128, K_OFF_QD = 2 * T128;
-  static constexpr int K_OFF_BAR = K_OFF_QD + 4 * T64;
-  static constexpr int OFF_SLOT = 128;                 // tensor-memory address, after the barriers
+  static constexpr int K_OFF_BAR = K_OFF_QD + NST * 2 * T64;
+  static constexpr int OFF_SLOT = 192;                 // tensor-memory address, after the barriers
   static constexpr int BAR_BYTES = 256;
   // one CTA per SM: each takes all 512 tensor-memory columns
   static constexpr int SMEM_Q = (Q_OFF_BAR + BAR_BYTES + 1024) < 116 * 1024 ? 116 * 1024 : Q_OFF_BAR + BAR_BYTES + 1024;
@@ -394,19 +406,22 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
 
   const uint32_t bars = sb + C::Q_OFF_BAR;
   auto bar = [&](int i) -> uint32_t { return bars + 8 * i; };
-  const uint32_t q_full = bar(0), drain = bar(13);
-  auto kv_full = [&](int b) -> uint32_t { return bar(1 + b); };
-  auto kv_empty = [&](int b) -> uint32_t { return bar(3 + b); };
-  auto sd_full = [&](int b) -> uint32_t { return bar(5 + b); };    // S_j, dP_j computed, j % 2 = b
-  auto sd_free = [&](int b) -> uint32_t { return bar(7 + b); };    // ... and read out
-  auto ds_full = [&](int b) -> uint32_t { return bar(9 + b); };    // dS_j written
-  auto ds_done = [&](int b) -> uint32_t { return bar(11 + b); };   // dQ += dS_j K_j finished
+  constexpr int NST = C::NST;
+  const uint32_t q_full = bar(0), drain = bar(15);
+  auto kv_full = [&](int st) -> uint32_t { return bar(1 + st); };    // K_j, V_j in stage j % NST
+  auto kv_empty = [&](int st) -> uint32_t { return bar(4 + st); };
+  auto sd_full = [&](int b) -> uint32_t { return bar(7 + b); };    // S_j, dP_j computed, j % 2 = b
+  auto sd_free = [&](int b) -> uint32_t { return bar(9 + b); };    // ... and read out
+  auto ds_full = [&](int b) -> uint32_t { return bar(11 + b); };   // dS_j written
+  auto ds_done = [&](int b) -> uint32_t { return bar(13 + b); };   // dQ += dS_j K_j finished
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(kv_full(st), 1);
+      mbar_init(kv_empty(st), 1);
+    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(kv_full(b), 1);
-      mbar_init(kv_empty(b), 1);
       mbar_init(sd_full(b), 1);
       mbar_init(sd_free(b), C::NSOFT);
       mbar_init(ds_full(b), C::NSOFT);
@@ -442,22 +457,22 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
       int j = 0;
       bool ok = true;
       for (; j < nkt; ++j) {
-        const int b = j & 1;
-        if (j >= 2 && (s_abort || !mbar_wait(kv_empty(b), ((j >> 1) - 1) & 1))) {
+        const int st = j % NST;
+        if (j >= NST && (s_abort || !mbar_wait(kv_empty(st), ((j / NST) - 1) & 1))) {
           ok = false;
           break;
         }
-        const uint32_t kb = sb + C::Q_OFF_KV + b * 2 * C::T64, vb = kb + C::T64;
-        mbar_arrive_expect_tx(kv_full(b), 2 * C::T64);
+        const uint32_t kb = sb + C::Q_OFF_KV + st * 2 * C::T64, vb = kb + C::T64;
+        mbar_arrive_expect_tx(kv_full(st), 2 * C::T64);
 #pragma unroll
         for (int p = 0; p < C::PANELS; ++p) {
-          tma_load_2d(kb + p * 8192, &tm_qkv, xk + p * 64, a + j * 64, kv_full(b));
-          tma_load_2d(vb + p * 8192, &tm_qkv, xv + p * 64, a + j * 64, kv_full(b));
+          tma_load_2d(kb + p * 8192, &tm_qkv, xk + p * 64, a + j * 64, kv_full(st));
+          tma_load_2d(vb + p * 8192, &tm_qkv, xv + p * 64, a + j * 64, kv_full(st));
         }
       }
       if (!ok) s_abort = 1;
       mbar_wait(q_full, 0);
-      for (int i = j - 2 < 0 ? 0 : j - 2; i < j; ++i) mbar_wait(kv_full(i & 1), (i >> 1) & 1);
+      for (int i = j - NST < 0 ? 0 : j - NST; i < j; ++i) mbar_wait(kv_full(i % NST), (i / NST) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -468,24 +483,25 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
       auto dq = [&](int i) -> bool {
         if (s_abort || !mbar_wait(ds_full(i & 1), (i >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t kb = sb + C::Q_OFF_KV + (i & 1) * 2 * C::T64;
+        const uint32_t kb = sb + C::Q_OFF_KV + (i % NST) * 2 * C::T64;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_bf16_ts(tmem + C::DQ_ACC, tmem + C::DQ_DS + (i & 1) * 32 + kk * 8,
                          sw128_mnmajor_desc(kb + kk * 2048, 8192), ID_Q, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(ds_done(i & 1));
-        tc_commit(kv_empty(i & 1));
+        tc_commit(kv_empty(i % NST));
         return true;
       };
       bool ok = mbar_wait(q_full, 0);
       for (int j = 0; ok && j < nkt; ++j) {
         const int b = j & 1;
-        if (s_abort || !mbar_wait(kv_full(b), (j >> 1) & 1) || (j >= 2 && !mbar_wait(sd_free(b), ((j - 2) >> 1) & 1))) {
+        if (s_abort || !mbar_wait(kv_full(j % NST), (j / NST) & 1) ||
+            (j >= 2 && !mbar_wait(sd_free(b), ((j - 2) >> 1) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t kb = sb + C::Q_OFF_KV + b * 2 * C::T64, vb = kb + C::T64;
+        const uint32_t kb = sb + C::Q_OFF_KV + (j % NST) * 2 * C::T64, vb = kb + C::T64;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32, koff = (kk >> 2) * 8192 + (kk & 3) * 32;
@@ -616,7 +632,7 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(attn_tc_smem) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(base);
   __shared__ volatile int s_abort;
-  __shared__ __align__(16) float s_ld[2][2][64];   // per query-tile stage: lse (log2 units), D
+  __shared__ __align__(16) float s_ld[C::NST][2][64];   // per query-tile stage: lse (log2 units), D
 
   const int s = blockIdx.y, g = blockIdx.x / hsplit, hs = blockIdx.x % hsplit;
   int a, L;
@@ -633,17 +649,20 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
 
   const uint32_t bars = sb + C::K_OFF_BAR;
   auto bar = [&](int i) -> uint32_t { return bars + 8 * i; };
-  const uint32_t kv_full = bar(0), st_full = bar(5), st_free = bar(6), drain = bar(11);
-  auto qd_full = [&](int b) -> uint32_t { return bar(1 + b); };
-  auto qd_empty = [&](int b) -> uint32_t { return bar(3 + b); };
-  auto pd_full = [&](int b) -> uint32_t { return bar(7 + b); };    // P^T_i, dS^T_i written, i % 2 = b
-  auto pd_done = [&](int b) -> uint32_t { return bar(9 + b); };    // dV, dK products of tile i finished
+  constexpr int NST = C::NST;
+  const uint32_t kv_full = bar(0), st_full = bar(7), st_free = bar(8), drain = bar(13);
+  auto qd_full = [&](int st) -> uint32_t { return bar(1 + st); };   // Q_i, dO_i (+ lse, D) in stage i % NST
+  auto qd_empty = [&](int st) -> uint32_t { return bar(4 + st); };
+  auto pd_full = [&](int b) -> uint32_t { return bar(9 + b); };    // P^T_i, dS^T_i written, i % 2 = b
+  auto pd_done = [&](int b) -> uint32_t { return bar(11 + b); };   // dV, dK products of tile i finished
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(qd_full(st), 1 + 32);   // the TMA bytes, and the producer lanes' lse / D stores
+      mbar_init(qd_empty(st), 1);
+    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(qd_full(b), 1 + 32);   // the TMA bytes, and the producer lanes' lse / D stores
-      mbar_init(qd_empty(b), 1);
       mbar_init(pd_full(b), C::NSOFT);
       mbar_init(pd_done(b), 1);
     }
@@ -681,9 +700,9 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
       int i = 0;
       bool ok = true;
       for (; i < nit; ++i) {
-        const int b = i & 1;
+        const int b = i % NST;
         bool good = true;
-        if (i >= 2) good = !s_abort && mbar_wait(qd_empty(b), ((i >> 1) - 1) & 1);
+        if (i >= NST) good = !s_abort && mbar_wait(qd_empty(b), ((i / NST) - 1) & 1);
         if (!__all_sync(0xffffffffu, good)) {
           ok = false;
           break;
@@ -710,7 +729,7 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
       if (lane == 0) {
         if (!ok) s_abort = 1;
         mbar_wait(kv_full, 0);
-        for (int j = i - 2 < 0 ? 0 : i - 2; j < i; ++j) mbar_wait(qd_full(j & 1), (j >> 1) & 1);
+        for (int j = i - NST < 0 ? 0 : i - NST; j < i; ++j) mbar_wait(qd_full(j % NST), (j / NST) & 1);
       }
     }
   } else if (warp == 1) {
@@ -722,7 +741,7 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
       auto kv = [&](int i) -> bool {
         if (s_abort || !mbar_wait(pd_full(i & 1), (i >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t qb = sb + C::K_OFF_QD + (i & 1) * 2 * C::T64, ob = qb + C::T64;
+        const uint32_t qb = sb + C::K_OFF_QD + (i % NST) * 2 * C::T64, ob = qb + C::T64;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           tc_mma_bf16_ts(tmem + C::KV_DV, tmem + C::KV_P + (i & 1) * 32 + kk * 8,
@@ -731,19 +750,18 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
                          sw128_mnmajor_desc(qb + kk * 2048, 8192), ID_O, (i > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(pd_done(i & 1));
-        tc_commit(qd_empty(i & 1));
+        tc_commit(qd_empty(i % NST));
         return true;
       };
       bool ok = mbar_wait(kv_full, 0);
       for (int i = 0; ok && i < nit; ++i) {
-        const int b = i & 1;
         // S^T, dP^T of tile i overwrite tile i-1's: the softmax warps must have read them
-        if (s_abort || !mbar_wait(qd_full(b), (i >> 1) & 1) || (i > 0 && !mbar_wait(st_free, (i - 1) & 1))) {
+        if (s_abort || !mbar_wait(qd_full(i % NST), (i / NST) & 1) || (i > 0 && !mbar_wait(st_free, (i - 1) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t qb = sb + C::K_OFF_QD + b * 2 * C::T64, ob = qb + C::T64;
+        const uint32_t qb = sb + C::K_OFF_QD + (i % NST) * 2 * C::T64, ob = qb + C::T64;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32, qoff = (kk >> 2) * 8192 + (kk & 3) * 32;
@@ -774,7 +792,7 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
     for (int i = 0; i < nit; ++i) {
       const int b = i & 1;
       // the tile's lse / D rows are in shared memory once its stage is full
-      if (!wwait(qd_full(b), (i >> 1) & 1) || !wwait(st_full, i & 1)) {
+      if (!wwait(qd_full(i % NST), (i / NST) & 1) || !wwait(st_full, i & 1)) {
         ok = false;
         break;
       }
@@ -788,8 +806,8 @@ __global__ void __launch_bounds__(AttnBwdTcCfg<HD>::THREADS, 1)
       if (lane == 0) mbar_arrive(st_free);
       const int q0 = k0 + (i % nqt) * 64 + hf * 32;   // first query of this thread's half
       const bool diag = q0 < k0 + 128;                // the half crosses the diagonal
-      const float* sl = s_ld[b][0] + hf * 32;
-      const float* sd = s_ld[b][1] + hf * 32;
+      const float* sl = s_ld[i % NST][0] + hf * 32;
+      const float* sd = s_ld[i % NST][1] + hf * 32;
       uint32_t pp[16], pd[16];
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
