@@ -114,3 +114,31 @@ def test_binding_signatures_match_header_declarations():
         else:
             assert name in B._SIGS, f"{name} has no ctypes signature"
             assert len(B._SIGS[name]) == n, f"{name}: header {n} parameters, binding {len(B._SIGS[name])}"
+
+
+def test_attention_and_wait_entry_points_refuse_bad_arguments_on_the_host():
+    """Argument checks that run before anything touches the device (so no GPU is needed):
+    the tensor-core attention kernels need 16-byte aligned operands (TMA, 16-byte
+    stores), a head dimension of 64 or 128 and a whole number of query heads per
+    key/value head; the bounded wait needs a 4-byte aligned flag and a limit >= 0."""
+    lib = L.lib()
+    A, B, C_, D = 0x10000, 0x20000, 0x30000, 0x40000       # 16-byte aligned stand-ins
+    # forward: qkv not 16-byte aligned; head_dim 96; 5 query heads on 2 kv heads
+    assert lib.lsk_attn_fwd(A + 8, 768, B, 1, 64, 4, 1, 128, C_, 512, D, 64, None) == L.LS_ERR_ARG
+    assert lib.lsk_attn_fwd(A, 768, B, 1, 64, 4, 1, 96, C_, 512, D, 64, None) == L.LS_ERR_ARG
+    assert lib.lsk_attn_fwd(A, 1152, B, 1, 64, 5, 2, 128, C_, 640, D, 64, None) == L.LS_ERR_ARG
+    assert "lsk_attn_fwd" in L.last_error()
+    # backward: no kv heads; dqkv row pitch not a multiple of 4; head-split scratch misaligned
+    args = [A, 768, B, C_, 512, D, B, 1, 64, 4, 1, 128, C_, D, 768, 64]
+    bad_kv = list(args)
+    bad_kv[10] = 0
+    assert lib.lsk_attn_bwd(*bad_kv, None, None) == L.LS_ERR_ARG
+    bad_ldg = list(args)
+    bad_ldg[14] = 770
+    assert lib.lsk_attn_bwd(*bad_ldg, None, None) == L.LS_ERR_ARG
+    assert lib.lsk_attn_bwd(*args, D + 4, None) == L.LS_ERR_ARG
+    assert "lsk_attn_bwd" in L.last_error()
+    # bounded wait: misaligned flag; negative limit; no status
+    assert lib.lsk_wait_flag(A + 2, 0, 1000, B, None) == L.LS_ERR_ARG
+    assert lib.lsk_wait_flag(A, 0, -1, B, None) == L.LS_ERR_ARG
+    assert lib.lsk_wait_flag(A, 0, 1000, None, None) == L.LS_ERR_ARG
