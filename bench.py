@@ -672,6 +672,58 @@ def gemm_microbench(spec: str, reps: int = 10) -> dict:
             "peak_source": peaks["source"]}
 
 
+def attn_microbench(spec: str, reps: int = 10) -> dict:
+    """Causal GQA attention forward and backward through the C ABI (lsk_attn_fwd /
+    lsk_attn_bwd, the tcgen05 kernels the training step runs), timed with CUDA events after
+    warm-up: spec = "T,nseq,nh,nkv,hd" (nseq equal sequences of T / nseq tokens; q/k/v and dO
+    drawn N(0, 1) in bf16; the backward takes the per-query-head split the step uses when
+    nh > nkv).  FLOPs: forward 4 hd nh sum L(L+1)/2, backward 2.5x that."""
+    import layer_streamed_nf4_dequant_b300 as L
+    T, nseq, nh, nkv, hd = [int(x) for x in spec.split(",")]
+    if nseq < 1 or T % nseq or nh % nkv:
+        raise ValueError("attn spec: T,nseq,nh,nkv,hd with T a multiple of nseq and nh of nkv")
+    Ls = T // nseq
+    cu = list(range(0, T + 1, Ls))
+    dev = torch.device("cuda:0")
+    ncols = (nh + 2 * nkv) * hd
+    g = torch.Generator().manual_seed(0)
+    qkv = torch.randn(T, ncols, generator=g).to(torch.bfloat16).to(dev)
+    dout = torch.randn(T, nh * hd, generator=g).to(torch.bfloat16).to(dev)
+    cud = torch.tensor(cu, dtype=torch.int32, device=dev)
+    o = torch.empty((T, nh * hd), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((nh, T), dtype=torch.float32, device=dev)
+    dsc = torch.empty((nh, T), dtype=torch.float32, device=dev)
+    dq = torch.zeros((T, ncols), dtype=torch.float32, device=dev)
+    part = torch.empty((nh // nkv) * T * 2 * nkv * hd, dtype=torch.float32, device=dev) if nh > nkv else None
+    st = torch.cuda.current_stream().cuda_stream
+
+    def fwd():
+        L.call("lsk_attn_fwd", qkv, ncols, cud, nseq, Ls, nh, nkv, hd, o, nh * hd, lse, T, st)
+
+    def bwd():
+        L.call("lsk_attn_bwd", qkv, ncols, dout, o, nh * hd, lse, cud, nseq, Ls, nh, nkv, hd, dsc, dq, ncols, T, part,
+               st)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3
+
+    fus = timed(fwd)
+    bus = timed(bwd)
+    flop = 4.0 * hd * nh * nseq * Ls * (Ls + 1) / 2
+    return {"kernel": "attention", "T": T, "nseq": nseq, "nh": nh, "nkv": nkv, "hd": hd,
+            "fwd_us": round(fus, 2), "fwd_tflops": round(flop / (fus * 1e-6) / 1e12, 1),
+            "bwd_us": round(bus, 2), "bwd_tflops": round(2.5 * flop / (bus * 1e-6) / 1e12, 1)}
+
+
 def cpu_baseline(s, seconds_budget: float = 20.0):
     tok, cu, mask = synth.tokens(s), synth.seq_offsets(s), synth.loss_mask(s)
     _, prep = oracle_sample(s, 0, 0, tok, cu, mask, None)   # warm-up (and weight preparation)
@@ -698,6 +750,8 @@ def main():
                     help="training method on the config's pairs (default: the config's own)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm", default=None, help="micro-benchmark one NF4 GEMM: mode,M,N,K[,bn,nacc[,split[,pair_rows]]] (split: 0 cost model, 1 split tiles, -1 whole tiles)")
+    ap.add_argument("--attn", default=None,
+                    help="micro-benchmark causal GQA attention fwd + bwd: T,nseq,nh,nkv,hd (e.g. 1024,2,32,8,128)")
     ap.add_argument("--stream-source", default="ram", choices=["ram", "file"],
                     help="where the streamed decoder layers live: pinned host RAM, or a file (NVMe tier)")
     ap.add_argument("--file-dir", default=None, help="directory of the layer file (default: the temp dir)")
@@ -709,6 +763,9 @@ def main():
     args = ap.parse_args()
     if args.gemm:
         print(json.dumps(gemm_microbench(args.gemm, max(1, args.steps))), flush=True)
+        return
+    if args.attn:
+        print(json.dumps(attn_microbench(args.attn, max(1, args.steps))), flush=True)
         return
     if args.warmup < 3:
         args.warmup = 3
