@@ -169,11 +169,19 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
                    MODE == GEMM_FWD ? 4u : (uint32_t)(C::UNITS / 64), MODE == GEMM_FWD ? (uint32_t)C::UNITS : 64u,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
+  // bf16 outputs with no residual leave through a tensor map (32-row x 64-column boxes)
+  CUtensorMap tO = tA;
+  const bool out_tma = C::NDQ_WARPS == C::EPI_WARPS && g.epi == EPI_BF16 && !g.residual && g.M > 0 && g.Nout > 0 && g.ldo % 8 == 0 &&
+                       (reinterpret_cast<uintptr_t>(g.out) & 15) == 0 &&
+                       make_map_2d(&tO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.out, (uint64_t)g.Nout, (uint64_t)g.M,
+                                   (uint64_t)g.ldo * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!out_tma) tO = tA;
   // Tile order: consecutive CTAs (one wave) share the operand that is walked slowly.
   // M-fastest keeps each weight tile in L2 for all row tiles; when the activation
   // operand is the larger one (long reductions, e.g. the 32B down-projection's dX) the
   // N-fastest order lets a wave share activation tiles instead.
   GemmArgs ga = g;
+  ga.out_tma = out_tma ? 1 : 0;
   ga.n_fast = (double)g.M * g.Kred * 2.0 > (double)g.Nw * g.Kw * 0.5625;
   const long long nt = (long long)p.tiles_m * p.tiles_n;
   ga.tiles_m = p.tiles_m;
@@ -196,9 +204,9 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   if (!kCanSplit && (ga.sched_dp != 1 || ga.sched_ctas != nt)) return cudaErrorInvalidValue;
   if (ga.sk_iters == 0) {
     if (ga.sched_dp == 1 && ga.sched_ctas == nt && !p.pair_rows)
-      kern_whole<<<(unsigned)nt, C::THREADS, C::SMEM, st>>>(tA, tW, tX, tS, ga);
+      kern_whole<<<(unsigned)nt, C::THREADS, C::SMEM, st>>>(tA, tW, tX, tS, tO, ga);
     else   // whole tiles, several per CTA, or paired rows
-      kern_split<<<(unsigned)ga.sched_ctas, C::THREADS, C::SMEM, st>>>(tA, tW, tX, tS, ga);
+      kern_split<<<(unsigned)ga.sched_ctas, C::THREADS, C::SMEM, st>>>(tA, tW, tX, tS, tO, ga);
     return cudaGetLastError();
   }
   // CTAs of a split schedule wait for one another's partial tiles: a cooperative launch
@@ -213,7 +221,7 @@ static cudaError_t launch_cfg(const GemmCall& c, const GemmPlan& p, cudaStream_t
   at[0].val.cooperative = 1;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, kern_split, tA, tW, tX, tS, ga);
+  return cudaLaunchKernelEx(&lc, kern_split, tA, tW, tX, tS, tO, ga);
 }
 
 // Pick the tile shape by estimated time = waves x per-CTA time.  Per-CTA time per

@@ -84,6 +84,10 @@ struct GemmArgs {
   // UNITS rows each k-step (column it % 4 used); input gradient, the k-step's 64 rows x 4
   // k-blocks.  Needs the absmax row pitch (K / 64 floats) to be a multiple of 16 bytes.
   int abs_tma;
+  // EPI_BF16 without residual: 1 = each epilogue warp stages its rows in its slice of the
+  // (then idle) B ring in the 128-byte-swizzled box layout and the output tensor map stores
+  // them (32 rows x 64 columns per box); 0 = direct row stores
+  int out_tma;
 };
 
 // Stream-K workspace: one 256 x 256 fp32 partial tile per CTA, at most kSkMaxCtas CTAs.
@@ -430,7 +434,7 @@ template <int NACC, int BN, int S, int SB, int MODE, bool SPLIT>
 __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
-                    const GemmArgs g) {
+                    const __grid_constant__ CUtensorMap tmO, const GemmArgs g) {
   using C = GemmCfg<NACC, BN, S, SB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -634,6 +638,8 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
     const int wq = warp & 3;
     const int half = ew >> 2;
     const bool epi = ew < C::EPI_WARPS;
+    // staged output boxes borrow the B ring, which only the epilogue warps write
+    const bool kOutTma = C::NDQ_WARPS == C::EPI_WARPS && SB * C::B_BYTES >= C::EPI_WARPS * 32 * BN && g.out_tma;
     int gi = 0, pc = 0;
     while (sc.next(tile, k0, k1)) {
       int m0, n0;
@@ -695,6 +701,10 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
       for (int a = 0; a < NACC; ++a) {
         const int row = m0 + a * (pair ? pair : 128) + wq * 32 + lane;
         const bool rok = row < g.M && (!pair || m0 + wq * 32 + lane < pair);
+        // the tensor store writes whole 32-row boxes: only where every row of the warp's box
+        // belongs to this tile (rows past M are clipped by the map)
+        const bool tstore = kOutTma && !partial && (!pair || m0 + wq * 32 + 32 <= pair);
+        uint8_t* ostg = smem + C::OFF_B + ew * (32 * BN);   // this warp's 32 x BN / 2 bf16 boxes
         float run_m = -INFINITY, run_s = 0.f;
         int tgt = -1;
         float lse_r = 0.f, coef_r = 0.f;
@@ -740,7 +750,16 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
               }
             }
           }
-          if (g.epi == EPI_BF16) {
+          if (g.epi == EPI_BF16 && tstore) {
+            // 16 values = chunks ch, ch + 1 of the 64-column box bx, 128-byte swizzle
+            const int lc = c0 - half * (BN / 2), bx = lc >> 6, ch = (lc & 63) >> 3;
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+            uint8_t* rowp = ostg + bx * 4096 + lane * 128;
+            *reinterpret_cast<uint4*>(rowp + ((ch ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(rowp + (((ch + 1) ^ (lane & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else if (g.epi == EPI_BF16) {
             if (g.residual) {
               const __nv_bfloat16* rp = g.residual + (size_t)row * g.ldr + gc;
               if (nvalid >= 16) {
@@ -809,6 +828,23 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
             store_bf16_16(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
           }
         }
+        if (tstore) {
+          // the warp's boxes to global memory; their shared-memory reads finish before the
+          // next accumulator is staged over them
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int rowb = m0 + a * (pair ? pair : 128) + wq * 32;
+#pragma unroll
+            for (int bx = 0; bx < BN / 128; ++bx) {
+              const int x = n0 + half * (BN / 2) + bx * 64;
+              if (x < g.Nout && rowb < g.M) tma_store_2d(&tmO, x, rowb, smem_u32(ostg) + bx * 4096);
+            }
+            bulk_commit();
+            bulk_wait_read0();
+          }
+          __syncwarp();
+        }
         if (!partial && g.epi == EPI_LOGPROB && rok && n0 + half * (BN / 2) < g.Nout) {
           const int p = (g.vocab_off + n0 + half * (BN / 2)) / (BN / 2);
           g.part_max[(size_t)row * g.part_ld + p] = run_m;
@@ -826,10 +862,16 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmemfree);
+      // the B ring held staged output boxes: refill it only once every epilogue warp is done
+      if (kOutTma && (s_abort || !mbar_wait(tmemfree, pc & 1))) {
+        s_abort = 1;
+        break;
+      }
       ++pc;
     }
   }
 
+  if (g.out_tma && lane == 0) bulk_wait0();   // this warp's tensor stores have completed
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
