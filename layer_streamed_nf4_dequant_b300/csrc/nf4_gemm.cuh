@@ -715,117 +715,128 @@ __global__ void __launch_bounds__(GemmCfg<NACC, BN, S, SB>::THREADS, 1)
             coef_r = g.coef[row];
           }
         }
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          const int c0 = half * (BN / 2) + cc * 16;
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * BN + c0), v);
+        for (int cp = 0; cp < BN / 64; ++cp) {
+          // 32 columns per TMEM load, and the peers' partials of both 16-column chunks are
+          // all in flight before the first is added: the epilogue is latency-bound
+          const int cb = half * (BN / 2) + cp * 32;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(a * BN + cb), v);
           tmem_ld_wait();
-          // partial-slot position of this thread's 16 values: chunk (a, wq, c0 / 16),
-          // 4 float4 groups of 32 lanes
-          const size_t chunk = ((size_t)(a * 4 + wq) * (BN / 16) + c0 / 16) * 512 + (size_t)lane * 4;
+          // partial-slot position of this thread's values: chunks (a, wq, cb / 16) and the next
+          // one (512 floats on), each 4 float4 groups of 32 lanes
+          const size_t chunk = ((size_t)(a * 4 + wq) * (BN / 16) + cb / 16) * 512 + (size_t)lane * 4;
           if (partial) {
             float4* dst = reinterpret_cast<float4*>(g.sk_ws + (size_t)sc.c * kSkSlotFloats + chunk);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 8; ++q)
               __stcg(dst + q * 32, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
             continue;
           }
-          const int gc = n0 + c0;
-          const int nvalid = min(16, g.Nout - gc);
-          if (!rok || nvalid <= 0) continue;
-          float f[16];
+          float fa[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 32; ++i) fa[i] = __uint_as_float(v[i]);
           if (finish) {
             for (int d = sc.c + 1; d <= dlast; ++d) {
               const float4* srcp = reinterpret_cast<const float4*>(g.sk_ws + (size_t)d * kSkSlotFloats + chunk);
+              float4 p4[8];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float4 p4 = __ldcg(srcp + q * 32);
-                f[4 * q] += p4.x;
-                f[4 * q + 1] += p4.y;
-                f[4 * q + 2] += p4.z;
-                f[4 * q + 3] += p4.w;
+              for (int q = 0; q < 8; ++q) p4[q] = __ldcg(srcp + q * 32);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                fa[4 * q] += p4[q].x;
+                fa[4 * q + 1] += p4[q].y;
+                fa[4 * q + 2] += p4[q].z;
+                fa[4 * q + 3] += p4[q].w;
               }
             }
           }
-          if (g.epi == EPI_BF16 && tstore) {
-            // 16 values = chunks ch, ch + 1 of the 64-column box bx, 128-byte swizzle
-            const int lc = c0 - half * (BN / 2), bx = lc >> 6, ch = (lc & 63) >> 3;
-            uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-            uint8_t* rowp = ostg + bx * 4096 + lane * 128;
-            *reinterpret_cast<uint4*>(rowp + ((ch ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4*>(rowp + (((ch + 1) ^ (lane & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          } else if (g.epi == EPI_BF16) {
-            if (g.residual) {
-              const __nv_bfloat16* rp = g.residual + (size_t)row * g.ldr + gc;
-              if (nvalid >= 16) {
-                const uint4* r4 = reinterpret_cast<const uint4*>(rp);
+          for (int u = 0; u < 2; ++u) {
+            const int c0 = cb + u * 16;
+            const int gc = n0 + c0;
+            const int nvalid = min(16, g.Nout - gc);
+            if (!rok || nvalid <= 0) continue;
+            float f[16];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                  const uint4 rv = r4[q];
-                  const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
+            for (int i = 0; i < 16; ++i) f[i] = fa[16 * u + i];
+            if (g.epi == EPI_BF16 && tstore) {
+              // 16 values = chunks ch, ch + 1 of the 64-column box bx, 128-byte swizzle
+              const int lc = c0 - half * (BN / 2), bx = lc >> 6, ch = (lc & 63) >> 3;
+              uint32_t pk[8];
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    f[8 * q + 2 * e] += bf16lo(w4[e]);
-                    f[8 * q + 2 * e + 1] += bf16hi(w4[e]);
+              for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+              uint8_t* rowp = ostg + bx * 4096 + lane * 128;
+              *reinterpret_cast<uint4*>(rowp + ((ch ^ (lane & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              *reinterpret_cast<uint4*>(rowp + (((ch + 1) ^ (lane & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            } else if (g.epi == EPI_BF16) {
+              if (g.residual) {
+                const __nv_bfloat16* rp = g.residual + (size_t)row * g.ldr + gc;
+                if (nvalid >= 16) {
+                  const uint4* r4 = reinterpret_cast<const uint4*>(rp);
+#pragma unroll
+                  for (int q = 0; q < 2; ++q) {
+                    const uint4 rv = r4[q];
+                    const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      f[8 * q + 2 * e] += bf16lo(w4[e]);
+                      f[8 * q + 2 * e + 1] += bf16hi(w4[e]);
+                    }
                   }
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    if (i < nvalid) f[i] += bf2f(rp[i]);
+                }
+              }
+              store_bf16_16(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
+            } else if (g.epi == EPI_F32 || g.epi == EPI_F32_ACC) {
+              float* op = reinterpret_cast<float*>(g.out) + (size_t)row * g.ldo + gc;
+              if (nvalid >= 16) {
+                float4* o4 = reinterpret_cast<float4*>(op);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  float4 x = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                  if (g.epi == EPI_F32_ACC) {
+                    const float4 y = o4[q];
+                    x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+                  }
+                  o4[q] = x;
                 }
               } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                  if (i < nvalid) f[i] += bf2f(rp[i]);
+                  if (i < nvalid) op[i] = (g.epi == EPI_F32_ACC ? op[i] : 0.f) + f[i];
               }
-            }
-            store_bf16_16(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
-          } else if (g.epi == EPI_F32 || g.epi == EPI_F32_ACC) {
-            float* op = reinterpret_cast<float*>(g.out) + (size_t)row * g.ldo + gc;
-            if (nvalid >= 16) {
-              float4* o4 = reinterpret_cast<float4*>(op);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                float4 x = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
-                if (g.epi == EPI_F32_ACC) {
-                  const float4 y = o4[q];
-                  x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-                }
-                o4[q] = x;
-              }
-            } else {
+            } else if (g.epi == EPI_LOGPROB) {
+              float cm = -INFINITY;
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                if (i < nvalid) op[i] = (g.epi == EPI_F32_ACC ? op[i] : 0.f) + f[i];
-            }
-          } else if (g.epi == EPI_LOGPROB) {
-            float cm = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (i < nvalid) cm = fmaxf(cm, f[i]);
-            if (cm > run_m) {
-              run_s *= __expf(run_m - cm);
-              run_m = cm;
-            }
-            float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (i < nvalid) acc += __expf(f[i] - run_m);
-            run_s += acc;
-            const int rel = tgt - gc;
-            if (rel >= 0 && rel < nvalid) {
-              float t = 0.f;
+                if (i < nvalid) cm = fmaxf(cm, f[i]);
+              if (cm > run_m) {
+                run_s *= __expf(run_m - cm);
+                run_m = cm;
+              }
+              float acc = 0.f;
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                if (i == rel) t = f[i];
-              g.tgt_logit[row] = t;
-            }
-          } else {  // EPI_DLOGITS: coef * (onehot(target) - softmax)
-            const int rel = tgt - gc;
+                if (i < nvalid) acc += __expf(f[i] - run_m);
+              run_s += acc;
+              const int rel = tgt - gc;
+              if (rel >= 0 && rel < nvalid) {
+                float t = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) f[i] = coef_r * ((i == rel ? 1.f : 0.f) - __expf(f[i] - lse_r));
-            store_bf16_16(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
+                for (int i = 0; i < 16; ++i)
+                  if (i == rel) t = f[i];
+                g.tgt_logit[row] = t;
+              }
+            } else {  // EPI_DLOGITS: coef * (onehot(target) - softmax)
+              const int rel = tgt - gc;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) f[i] = coef_r * ((i == rel ? 1.f : 0.f) - __expf(f[i] - lse_r));
+              store_bf16_16(reinterpret_cast<__nv_bfloat16*>(g.out) + (size_t)row * g.ldo + gc, f, nvalid);
+            }
           }
         }
         if (tstore) {
