@@ -52,8 +52,8 @@ METRIC = "train tokens/s streamed NF4 LoRA (8B shape, SFT+DPO); H2D GB/s; % roof
 # on paired split tiles, input gradient 1024 rows on the split schedule), in the build the
 # step runs.  It scales the class's algorithmic bytes per launch to the reported traffic;
 # None whenever that kernel has changed since the capture (the traffic is then null).
-GEMM_TRAFFIC_PER_ALG_BYTE = {"gemm_fwd": None,    # epilogue changed since the last capture
-                             "gemm_dx": None}
+GEMM_TRAFFIC_PER_ALG_BYTE = {"gemm_fwd": (85.9 + 105.9) / 200.3,    # gate|up forward, 2048 rows, paired split
+                             "gemm_dx": (449.1 + 17.8) / 141.6}     # gate|up input gradient, 1024 rows, split
 UNIT = "tokens/s"
 NF4_BYTES_PER_PARAM = 0.5625
 
