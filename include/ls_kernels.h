@@ -110,7 +110,10 @@ int lsk_rope_bwd_cast(const float* g, uint16_t* out, int64_t ld, const int32_t* 
 /* Causal GQA attention forward.  qkv bf16 [T, ld] holds q heads (nh*hd columns),
  * then k heads, then v heads (kv*hd each); sequences by cu int32 [nseq+1];
  * max_len = longest sequence.  out bf16 [T, ldo] (nh*hd columns); lse fp32 [nh, T].
- * qkv and out 16-byte aligned, ld and ldo multiples of 8 (else LS_ERR_ARG). */
+ * qkv and out 16-byte aligned, ld >= (nh + 2 nkv) head_dim and ldo >= nh head_dim, both
+ * multiples of 8, 1 <= nseq <= 65535, ceil(max_len / 128) <= 65535 (else LS_ERR_ARG).
+ * max_len must not be below any sequence's length (cu lives on the device and is not
+ * checked): query tiles past ceil(max_len / 128) are not computed. */
 int lsk_attn_fwd(const uint16_t* qkv, int64_t ld, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh,
                  int32_t nkv, int32_t head_dim, uint16_t* out, int64_t ldo, float* lse, int32_t T, void* stream);
 
@@ -119,8 +122,9 @@ int lsk_attn_fwd(const uint16_t* qkv, int64_t ld, const int32_t* cu, int32_t nse
  * d_scratch: fp32 [nh, T].  part: NULL, or fp32 scratch of (nh / nkv) * T * 2 * nkv *
  * head_dim floats (16-byte aligned): dk / dv are then computed per query head by separate
  * CTAs and summed in head order by a second kernel (more CTAs in flight; the same result
- * to fp32 reassociation, and deterministic either way).  qkv, dout and dqkv 16-byte
- * aligned; ld, lddo multiples of 8, ldg of 4. */
+ * to fp32 reassociation, and deterministic either way).  qkv, dout, out and dqkv 16-byte
+ * aligned; ld and ldg >= (nh + 2 nkv) head_dim, lddo >= nh head_dim; ld, lddo multiples of
+ * 8, ldg of 4; nseq and max_len as for lsk_attn_fwd (else LS_ERR_ARG). */
 int lsk_attn_bwd(const uint16_t* qkv, int64_t ld, const uint16_t* dout, const uint16_t* out, int64_t lddo,
                  const float* lse, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh, int32_t nkv,
                  int32_t head_dim, float* d_scratch, float* dqkv, int64_t ldg, int32_t T, float* part,

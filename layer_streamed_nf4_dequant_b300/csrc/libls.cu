@@ -1939,9 +1939,11 @@ int lsk_rope_bwd_cast(const float* g, uint16_t* out, int64_t ld, const int32_t* 
 
 int lsk_attn_fwd(const uint16_t* qkv, int64_t ld, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh,
                  int32_t nkv, int32_t hd, uint16_t* out, int64_t ldo, float* lse, int32_t T, void* s) {
-  if (!qkv || !cu || !out || !lse || nseq < 1 || max_len < 1 || nh < 1 || nkv < 1 || nh % nkv ||
-      (hd != 64 && hd != 128) || ld < (int64_t)(nh + 2 * nkv) * hd || ld % 8 || ldo % 8 ||
-      (reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+  // grid: (query heads, sequences, 128-row query tiles); the last two are limited to 65535
+  if (!qkv || !cu || !out || !lse || nseq < 1 || nseq > 65535 || max_len < 1 || (max_len + 127) / 128 > 65535 ||
+      nh < 1 || nkv < 1 || nh % nkv || (hd != 64 && hd != 128) || ld < (int64_t)(nh + 2 * nkv) * hd || ld % 8 ||
+      ldo < (int64_t)nh * hd || ldo % 8 || (reinterpret_cast<uintptr_t>(qkv) & 15) ||
+      (reinterpret_cast<uintptr_t>(out) & 15))
     return set_thread_err(LS_ERR_ARG, "lsk_attn_fwd: bad args");
   KCK(attn_fwd(hd, reinterpret_cast<const bf16*>(qkv), ld, cu, nseq, max_len, nh, nkv, reinterpret_cast<bf16*>(out),
                ldo, lse, T, STREAM(s)));
@@ -1951,10 +1953,12 @@ int lsk_attn_fwd(const uint16_t* qkv, int64_t ld, const int32_t* cu, int32_t nse
 int lsk_attn_bwd(const uint16_t* qkv, int64_t ld, const uint16_t* dout, const uint16_t* o, int64_t lddo,
                  const float* lse, const int32_t* cu, int32_t nseq, int32_t max_len, int32_t nh, int32_t nkv,
                  int32_t hd, float* D, float* dqkv, int64_t ldg, int32_t T, float* part, void* s) {
-  if (!qkv || !dout || !o || !lse || !cu || !D || !dqkv || nseq < 1 || max_len < 1 || nh < 1 || nkv < 1 || nh % nkv ||
-      (hd != 64 && hd != 128) || ld % 8 || lddo % 8 || ldg % 4 ||
-      ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv) |
-        reinterpret_cast<uintptr_t>(part)) & 15))
+  const int64_t w = (int64_t)(nh + 2 * nkv) * hd;   // q | k | v columns
+  if (!qkv || !dout || !o || !lse || !cu || !D || !dqkv || nseq < 1 || nseq > 65535 || max_len < 1 ||
+      (max_len + 127) / 128 > 65535 || nh < 1 || nkv < 1 || nh % nkv || (hd != 64 && hd != 128) || ld < w ||
+      ld % 8 || lddo < (int64_t)nh * hd || lddo % 8 || ldg < w || ldg % 4 ||
+      ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(o) |
+        reinterpret_cast<uintptr_t>(dqkv) | reinterpret_cast<uintptr_t>(part)) & 15))
     return set_thread_err(LS_ERR_ARG, "lsk_attn_bwd: bad args");
   KCK(attn_bwd(hd, reinterpret_cast<const bf16*>(qkv), ld, reinterpret_cast<const bf16*>(dout),
                reinterpret_cast<const bf16*>(o), lddo, lse, cu, nseq, max_len, nh, nkv, D, dqkv, ldg, T, STREAM(s),

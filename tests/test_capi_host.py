@@ -119,8 +119,9 @@ def test_binding_signatures_match_header_declarations():
 def test_attention_and_wait_entry_points_refuse_bad_arguments_on_the_host():
     """Argument checks that run before anything touches the device (so no GPU is needed):
     the tensor-core attention kernels need 16-byte aligned operands (TMA, 16-byte
-    stores), a head dimension of 64 or 128 and a whole number of query heads per
-    key/value head; the bounded wait needs a 4-byte aligned flag and a limit >= 0."""
+    stores), a head dimension of 64 or 128, a whole number of query heads per
+    key/value head, row pitches that hold a whole row and a grid within CUDA's limits; the
+    bounded wait needs a 4-byte aligned flag and a limit >= 0."""
     lib = L.lib()
     A, B, C_, D = 0x10000, 0x20000, 0x30000, 0x40000       # 16-byte aligned stand-ins
     # forward: qkv not 16-byte aligned; head_dim 96; 5 query heads on 2 kv heads
@@ -137,7 +138,26 @@ def test_attention_and_wait_entry_points_refuse_bad_arguments_on_the_host():
     bad_ldg[14] = 770
     assert lib.lsk_attn_bwd(*bad_ldg, None, None) == L.LS_ERR_ARG
     assert lib.lsk_attn_bwd(*args, D + 4, None) == L.LS_ERR_ARG
+    # ... forward output misaligned (8-byte reads of it); row pitches narrower than a row
+    bad_o = list(args)
+    bad_o[3] = C_ + 4
+    assert lib.lsk_attn_bwd(*bad_o, None, None) == L.LS_ERR_ARG
+    for i, v in ((1, 760), (4, 504), (14, 764)):      # ld, lddo, ldg one step short
+        narrow = list(args)
+        narrow[i] = v
+        assert lib.lsk_attn_bwd(*narrow, None, None) == L.LS_ERR_ARG
+    # ... grid limits: 65536 sequences; 65536 query tiles
+    many = list(args)
+    many[7] = 65536
+    assert lib.lsk_attn_bwd(*many, None, None) == L.LS_ERR_ARG
+    long_ = list(args)
+    long_[8] = 65536 * 128 + 1
+    assert lib.lsk_attn_bwd(*long_, None, None) == L.LS_ERR_ARG
     assert "lsk_attn_bwd" in L.last_error()
+    # forward: output pitch narrower than nh * head_dim; grid limits
+    assert lib.lsk_attn_fwd(A, 768, B, 1, 64, 4, 1, 128, C_, 504, D, 64, None) == L.LS_ERR_ARG
+    assert lib.lsk_attn_fwd(A, 768, B, 65536, 64, 4, 1, 128, C_, 512, D, 64, None) == L.LS_ERR_ARG
+    assert lib.lsk_attn_fwd(A, 768, B, 1, 65536 * 128 + 1, 4, 1, 128, C_, 512, D, 64, None) == L.LS_ERR_ARG
     # bounded wait: misaligned flag; negative limit; no status
     assert lib.lsk_wait_flag(A + 2, 0, 1000, B, None) == L.LS_ERR_ARG
     assert lib.lsk_wait_flag(A, 0, -1, B, None) == L.LS_ERR_ARG
