@@ -7,6 +7,14 @@
  * caller-owned memory unless named h_*.  bf16 travels as uint16_t; matrices are
  * dense row-major with the given leading dimension (elements).  Shapes: T tokens,
  * H hidden, NF4 matrices W [N, K] in nn.Linear order with K % 64 == 0.
+ *
+ * Alignment: the kernels move whole 4-, 8- and 16-byte words.  Unless a call says
+ * otherwise, bf16 matrices and packed NF4 codes are 16-byte aligned, fp32 matrices
+ * 16-byte aligned, absmax and index arrays 4-byte aligned; the narrower cases are
+ * listed per call (rmsnorm and SwiGLU backward: bf16 operands 8-byte; LoRA down / du
+ * inputs 4-byte; embedding and dequant codes 4-byte; RoPE takes any alignment).
+ * A pointer below its call's alignment is refused with LS_ERR_ARG before anything is
+ * launched.  Allocations from cudaMalloc or PyTorch are 256-byte aligned.
  */
 #ifndef LS_KERNELS_H_
 #define LS_KERNELS_H_

@@ -19,6 +19,7 @@
 #include <fcntl.h>
 #include <unistd.h>
 #include <cerrno>
+#include <climits>
 #include <mutex>
 #include <string>
 #include <thread>
@@ -47,6 +48,10 @@ int set_thread_err(int code, const std::string& m) {
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// A pointer that is given and not a multiple of a bytes (a power of two): the kernels read
+// and write whole 4-, 8- or 16-byte words, and a misaligned word access faults.
+inline bool misaligned(const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
 
 constexpr int kLoraSplitMax = 8;   // K slices of the LoRA projections (workspace scratch)
 
@@ -1793,7 +1798,8 @@ int ls_debug_copy_delay(ls_ctx* c, int32_t ms) {
 #define STREAM(s) reinterpret_cast<cudaStream_t>(s)
 
 int lsk_nf4_dequant(const uint8_t* packed, const float* absmax, int64_t rows, int32_t cols, uint16_t* out, void* s) {
-  if (!packed || !absmax || !out || rows < 0 || cols <= 0 || cols % 64) return set_thread_err(LS_ERR_ARG, "lsk_nf4_dequant: bad args");
+  if (!packed || !absmax || !out || rows < 0 || cols <= 0 || cols % 64 || misaligned(packed, 4) || misaligned(out, 16))
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_dequant: bad args");
   const long long n = rows * (cols / 8);
   if (n == 0) return LS_OK;
   ls::nf4_dequant_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(packed, absmax, reinterpret_cast<bf16*>(out), rows, cols);
@@ -1818,6 +1824,10 @@ int lsk_nf4_gemm(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, const 
   if (force_bn != 0 && force_bn != 128 && force_bn != 256) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: force_bn");
   if (force_nacc < 0 || force_nacc > 2) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: force_nacc");
   if (residual && epi != 0) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: residual only with bf16 output");
+  if (misaligned(A, 16) || misaligned(wp, 16) || misaligned(wa, 4) || misaligned(out, 16) || misaligned(residual, 16) ||
+      misaligned(ext_a, 16) || misaligned(ext_b, 16))
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm: A, w_packed, ext_a, ext_b, out, residual must be 16-byte aligned, "
+                                      "absmax 4-byte");
   KCK(gemm(mode, reinterpret_cast<const bf16*>(A), lda, M, wp, wa, N, K, reinterpret_cast<const bf16*>(ext_a),
            reinterpret_cast<const bf16*>(ext_b), ext_k, epi, out, ldo, reinterpret_cast<const bf16*>(residual), ldr,
            STREAM(s), ls::SkWorkspace{}, force_bn, force_nacc));
@@ -1881,6 +1891,10 @@ int lsk_nf4_gemm_sk(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, con
     return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: force_bn");
   if (force_nacc < 0 || force_nacc > 2) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: force_nacc");
   if (residual && epi != 0) return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: residual only with bf16 output");
+  if (misaligned(A, 16) || misaligned(wp, 16) || misaligned(wa, 4) || misaligned(out, 16) || misaligned(residual, 16) ||
+      misaligned(ext_a, 16) || misaligned(ext_b, 16))
+    return set_thread_err(LS_ERR_ARG, "lsk_nf4_gemm_sk: A, w_packed, ext_a, ext_b, out, residual must be 16-byte aligned, "
+                                      "absmax 4-byte");
   KCK(gemm(mode, reinterpret_cast<const bf16*>(A), lda, M, wp, wa, N, K, reinterpret_cast<const bf16*>(ext_a),
            reinterpret_cast<const bf16*>(ext_b), ext_k, epi, out, ldo, reinterpret_cast<const bf16*>(residual), ldr,
            STREAM(s), paired_ws(workspace, pair_rows), force_bn, force_nacc, split));
@@ -1889,7 +1903,8 @@ int lsk_nf4_gemm_sk(int32_t mode, const uint16_t* A, int64_t lda, int32_t M, con
 
 int lsk_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, float* rstd, int32_t T, int32_t H, float eps,
                     void* s) {
-  if (!x || !w || !y || T < 0 || H <= 0 || H % 8) return set_thread_err(LS_ERR_ARG, "lsk_rmsnorm_fwd: bad args");
+  if (!x || !w || !y || T < 0 || H <= 0 || H % 8 || misaligned(x, 16) || misaligned(w, 16) || misaligned(y, 16))
+    return set_thread_err(LS_ERR_ARG, "lsk_rmsnorm_fwd: bad args");
   if (T == 0) return LS_OK;
   KCK(rmsnorm_fwd(reinterpret_cast<const bf16*>(x), reinterpret_cast<const bf16*>(w), reinterpret_cast<bf16*>(y),
                   rstd, T, H, eps, STREAM(s)));
@@ -1898,7 +1913,9 @@ int lsk_rmsnorm_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, float* rs
 
 int lsk_rmsnorm_bwd(const float* dy, const uint16_t* x, const float* rstd, const uint16_t* w, float* dx,
                     uint16_t* dx_bf16, int32_t T, int32_t H, int32_t accumulate, void* s) {
-  if (!dy || !x || !rstd || !w || !dx || T < 0 || H <= 0 || H % 4) return set_thread_err(LS_ERR_ARG, "lsk_rmsnorm_bwd: bad args");
+  if (!dy || !x || !rstd || !w || !dx || T < 0 || H <= 0 || H % 4 || misaligned(dy, 16) || misaligned(dx, 16) ||
+      misaligned(x, 8) || misaligned(w, 8) || misaligned(dx_bf16, 8))
+    return set_thread_err(LS_ERR_ARG, "lsk_rmsnorm_bwd: bad args");
   if (T == 0) return LS_OK;
   KCK(rmsnorm_bwd(dy, reinterpret_cast<const bf16*>(x), rstd, reinterpret_cast<const bf16*>(w), dx,
                   reinterpret_cast<bf16*>(dx_bf16), T, H, accumulate, STREAM(s)));
@@ -1967,7 +1984,8 @@ int lsk_attn_bwd(const uint16_t* qkv, int64_t ld, const uint16_t* dout, const ui
 }
 
 int lsk_swiglu_fwd(const uint16_t* gu, uint16_t* h, int32_t T, int32_t I, void* s) {
-  if (!gu || !h || T < 0 || I <= 0 || I % 8) return set_thread_err(LS_ERR_ARG, "lsk_swiglu_fwd: bad args");
+  if (!gu || !h || T < 0 || I <= 0 || I % 8 || misaligned(gu, 16) || misaligned(h, 16))
+    return set_thread_err(LS_ERR_ARG, "lsk_swiglu_fwd: bad args");
   const long long n = (long long)T * (I / 8);
   if (n == 0) return LS_OK;
   ls::swiglu_fwd_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(gu), reinterpret_cast<bf16*>(h), T, I);
@@ -1976,7 +1994,8 @@ int lsk_swiglu_fwd(const uint16_t* gu, uint16_t* h, int32_t T, int32_t I, void* 
 }
 
 int lsk_swiglu_bwd(const float* dh, const uint16_t* gu, uint16_t* dgu, int32_t T, int32_t I, void* s) {
-  if (!dh || !gu || !dgu || T < 0 || I <= 0 || I % 4) return set_thread_err(LS_ERR_ARG, "lsk_swiglu_bwd: bad args");
+  if (!dh || !gu || !dgu || T < 0 || I <= 0 || I % 4 || misaligned(dh, 16) || misaligned(gu, 8) || misaligned(dgu, 8))
+    return set_thread_err(LS_ERR_ARG, "lsk_swiglu_bwd: bad args");
   const long long n = (long long)T * (I / 4);
   if (n == 0) return LS_OK;
   ls::swiglu_bwd_kernel<<<grid1d(n, 256), 256, 0, STREAM(s)>>>(dh, reinterpret_cast<const bf16*>(gu), reinterpret_cast<bf16*>(dgu), T, I);
@@ -1986,7 +2005,8 @@ int lsk_swiglu_bwd(const float* dh, const uint16_t* gu, uint16_t* dgu, int32_t T
 
 int lsk_lora_down(const uint16_t* x, int64_t ldx, const uint16_t* aq, const uint16_t* av, int32_t r, int32_t K,
                   float sc, uint16_t* u_ext, int32_t T, void* s) {
-  if (!x || !u_ext || r < 1 || r > 16 || K <= 0 || K % 8 || ldx < K || ldx % 8 || T < 0)
+  if (!x || !u_ext || r < 1 || r > 16 || K <= 0 || K % 8 || ldx < K || ldx % 8 || T < 0 || misaligned(x, 4) ||
+      misaligned(aq, 4) || misaligned(av, 4))
     return set_thread_err(LS_ERR_ARG, "lsk_lora_down: bad args");
   if (K % 16) return set_thread_err(LS_ERR_ARG, "lsk_lora_down: K must be a multiple of 16");
   if (T == 0) return LS_OK;
@@ -1997,7 +2017,7 @@ int lsk_lora_down(const uint16_t* x, int64_t ldx, const uint16_t* aq, const uint
 
 int lsk_lora_du(const uint16_t* dy, int64_t ldy, int32_t col_q, int32_t nq, const uint16_t* bq, int32_t col_v,
                 int32_t nv, const uint16_t* bv, int32_t r, float sc, float* du, uint16_t* du_ext, int32_t T, void* s) {
-  if (!dy || !du || !du_ext || r < 1 || r > 16 || T < 0 || ldy % 2 || col_q % 2 || col_v % 2 ||
+  if (!dy || !du || !du_ext || r < 1 || r > 16 || T < 0 || ldy % 2 || col_q % 2 || col_v % 2 || misaligned(dy, 4) ||
       (bq && (nq < 16 || nq % 16)) || (bv && (nv < 16 || nv % 16)))
     return set_thread_err(LS_ERR_ARG, "lsk_lora_du: bad args (even pitch/offsets, widths multiples of 16)");
   if (T == 0) return LS_OK;
@@ -2010,7 +2030,7 @@ int lsk_lora_outer(const uint16_t* X, int64_t ldx, int32_t ncols, const float* u
                    int32_t r, int32_t T, int32_t layout, int32_t accumulate, float* scratch, int32_t rpc, float* out,
                    void* s) {
   if (!X || (!uf && !ub) || !scratch || !out || r < 1 || r > 16 || ncols < 1 || ncols % 8 || ldx % 8 ||
-      ldx < ncols || ldu < r || (reinterpret_cast<uintptr_t>(X) & 15) || T < 1 || rpc < 1 ||
+      ldx < ncols || ldu < r || (reinterpret_cast<uintptr_t>(X) & 15) || misaligned(scratch, 8) || T < 1 || rpc < 1 ||
       (layout != 0 && layout != 1) || ((long long)T + rpc - 1) / rpc > 65535)
     return set_thread_err(LS_ERR_ARG, "lsk_lora_outer: bad args");
   KCK(lora_outer(reinterpret_cast<const bf16*>(X), ldx, ncols, uf, reinterpret_cast<const bf16*>(ub), ldu, r, T,
@@ -2070,7 +2090,7 @@ int lsk_lora_outer_noalloc(const uint16_t* X, int64_t ldx, int32_t ncols, const 
 
 int lsk_build_ext_fwd(const uint16_t* bq, int32_t q0, int32_t nq, const uint16_t* bv, int32_t v0, int32_t nv,
                       int32_t r, int32_t N, uint16_t* ext, void* s) {
-  if (!ext || N < 1 || r < 1 || r > 16) return set_thread_err(LS_ERR_ARG, "lsk_build_ext_fwd: bad args");
+  if (!ext || N < 1 || N > INT_MAX / 64 || r < 1 || r > 16) return set_thread_err(LS_ERR_ARG, "lsk_build_ext_fwd: bad args");
   const int n = N * 64;
   ls::build_ext_fwd_kernel<<<(n + 255) / 256, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(bq), q0, nq,
                                                                   reinterpret_cast<const bf16*>(bv), v0, nv, r, N,
@@ -2080,7 +2100,7 @@ int lsk_build_ext_fwd(const uint16_t* bq, int32_t q0, int32_t nq, const uint16_t
 }
 
 int lsk_build_ext_bwd(const uint16_t* aq, const uint16_t* av, int32_t r, int32_t K, uint16_t* ext, void* s) {
-  if (!ext || K < 1 || r < 1 || r > 16) return set_thread_err(LS_ERR_ARG, "lsk_build_ext_bwd: bad args");
+  if (!ext || K < 1 || K > INT_MAX / 64 || r < 1 || r > 16) return set_thread_err(LS_ERR_ARG, "lsk_build_ext_bwd: bad args");
   const int n = K * 64;
   ls::build_ext_bwd_kernel<<<(n + 255) / 256, 256, 0, STREAM(s)>>>(reinterpret_cast<const bf16*>(aq),
                                                                   reinterpret_cast<const bf16*>(av), r, K,
@@ -2091,7 +2111,7 @@ int lsk_build_ext_bwd(const uint16_t* aq, const uint16_t* av, int32_t r, int32_t
 
 int lsk_embed_gather(const int32_t* tokens, const uint8_t* packed, const float* absmax, int32_t V, uint16_t* x,
                      int32_t T, int32_t H, void* s) {
-  if (!tokens || !packed || !absmax || !x || V < 1 || T < 0 || H % 64)
+  if (!tokens || !packed || !absmax || !x || V < 1 || T < 0 || H % 64 || misaligned(packed, 4) || misaligned(x, 16))
     return set_thread_err(LS_ERR_ARG, "lsk_embed_gather: bad args");
   const long long n = (long long)T * (H / 8);
   if (n == 0) return LS_OK;
@@ -2103,7 +2123,8 @@ int lsk_embed_gather(const int32_t* tokens, const uint8_t* packed, const float* 
 
 int lsk_vocab_logprob(const uint16_t* h, int32_t T, int32_t H, const uint8_t* wp, const float* wa, int32_t V,
                       const int32_t* targets, float* scratch, float* tgt_logit, float* lse, float* lp, void* s) {
-  if (!h || !wp || !wa || !targets || !scratch || !tgt_logit || !lse || !lp || T < 1 || H % 64 || V % 64 || V < 64)
+  if (!h || !wp || !wa || !targets || !scratch || !tgt_logit || !lse || !lp || T < 1 || H % 64 || V % 64 || V < 64 ||
+      misaligned(h, 16) || misaligned(wp, 16) || misaligned(wa, 4))
     return set_thread_err(LS_ERR_ARG, "lsk_vocab_logprob: bad args");
   const int P = (V + 127) / 128;
   float* pmax = scratch;
@@ -2129,7 +2150,8 @@ int lsk_vocab_logprob(const uint16_t* h, int32_t T, int32_t H, const uint8_t* wp
 int lsk_vocab_bwd(const uint16_t* h, int32_t T, int32_t H, const uint8_t* wp, const float* wa, int32_t v0, int32_t n,
                   const int32_t* targets, const float* lse, const float* coef, uint16_t* dlogits, float* dh,
                   int32_t accumulate, void* s) {
-  if (!h || !wp || !wa || !targets || !lse || !coef || !dlogits || !dh || T < 1 || H % 64 || n % 64 || n < 64)
+  if (!h || !wp || !wa || !targets || !lse || !coef || !dlogits || !dh || T < 1 || H % 64 || n % 64 || n < 64 ||
+      misaligned(h, 16) || misaligned(wp, 16) || misaligned(wa, 4) || misaligned(dlogits, 16) || misaligned(dh, 16))
     return set_thread_err(LS_ERR_ARG, "lsk_vocab_bwd: bad args");
   GemmCall g{};
   g.mode = ls::GEMM_FWD;

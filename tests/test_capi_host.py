@@ -162,3 +162,52 @@ def test_attention_and_wait_entry_points_refuse_bad_arguments_on_the_host():
     assert lib.lsk_wait_flag(A + 2, 0, 1000, B, None) == L.LS_ERR_ARG
     assert lib.lsk_wait_flag(A, 0, -1, B, None) == L.LS_ERR_ARG
     assert lib.lsk_wait_flag(A, 0, 1000, None, None) == L.LS_ERR_ARG
+
+
+def test_kernel_entry_points_refuse_misaligned_pointers_on_the_host():
+    """The kernels move whole 4-, 8- and 16-byte words, so a pointer below a call's
+    alignment would fault on the device: each call refuses it with LS_ERR_ARG before
+    any launch (no GPU needed).  Each case shifts one pointer of an otherwise valid call."""
+    lib = L.lib()
+    A, B, C_, D, E, F = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000   # 16-byte aligned
+    ws = 0x100000
+    wsb = int(lib.lsk_nf4_gemm_workspace_bytes())
+    cases = [
+        # dequant: codes 4-byte, output 16-byte
+        ("lsk_nf4_dequant", [A + 2, B, 4, 64, C_, None]),
+        ("lsk_nf4_dequant", [A, B, 4, 64, C_ + 8, None]),
+        # GEMM: activation, codes, output, residual 16-byte; absmax 4-byte
+        ("lsk_nf4_gemm", [0, A + 8, 64, 16, B, C_, 64, 64, None, None, 0, 0, D, 64, None, 0, 0, 0, None]),
+        ("lsk_nf4_gemm", [0, A, 64, 16, B + 8, C_, 64, 64, None, None, 0, 0, D, 64, None, 0, 0, 0, None]),
+        ("lsk_nf4_gemm", [0, A, 64, 16, B, C_ + 2, 64, 64, None, None, 0, 0, D, 64, None, 0, 0, 0, None]),
+        ("lsk_nf4_gemm", [0, A, 64, 16, B, C_, 64, 64, None, None, 0, 0, D + 8, 64, None, 0, 0, 0, None]),
+        ("lsk_nf4_gemm", [0, A, 64, 16, B, C_, 64, 64, None, None, 0, 0, D, 64, E + 8, 64, 0, 0, None]),
+        ("lsk_nf4_gemm", [0, A, 64, 16, B, C_, 64, 64, E + 8, F, 16, 0, D, 64, None, 0, 0, 0, None]),
+        ("lsk_nf4_gemm_sk", [1, A, 64, 16, B, C_, 64, 64, None, None, 0, 1, D + 4, 64, None, 0, 0, 0, 0, 0,
+                             ws, wsb, None]),
+        # RMSNorm: forward 16-byte; backward fp32 16-byte, bf16 8-byte
+        ("lsk_rmsnorm_fwd", [A + 8, B, C_, D, 4, 64, 1e-5, None]),
+        ("lsk_rmsnorm_bwd", [A + 8, B, C_, D, E, None, 4, 64, 0, None]),
+        ("lsk_rmsnorm_bwd", [A, B + 4, C_, D, E, None, 4, 64, 0, None]),
+        ("lsk_rmsnorm_bwd", [A, B, C_, D, E, F + 4, 4, 64, 0, None]),
+        # SwiGLU: forward 16-byte; backward dh 16-byte, bf16 8-byte
+        ("lsk_swiglu_fwd", [A + 8, B, 4, 64, None]),
+        ("lsk_swiglu_bwd", [A, B + 4, C_, 4, 64, None]),
+        # LoRA: projections read 4-byte words; the outer product writes float2 partials
+        ("lsk_lora_down", [A + 2, 64, B, C_, 16, 64, 1.0, D, 4, None]),
+        ("lsk_lora_down", [A, 64, B + 2, C_, 16, 64, 1.0, D, 4, None]),
+        ("lsk_lora_du", [A + 2, 64, 0, 16, B, 16, 16, C_, 16, 1.0, D, E, 4, None]),
+        ("lsk_lora_outer", [A, 64, 64, B, None, 16, 16, 4, 0, 0, C_ + 4, 4, D, None]),
+        # embedding rows 16-byte, codes 4-byte; vocabulary products as the GEMM
+        ("lsk_embed_gather", [A, B + 2, C_, 128, D, 4, 64, None]),
+        ("lsk_embed_gather", [A, B, C_, 128, D + 8, 4, 64, None]),
+        ("lsk_vocab_logprob", [A + 8, 4, 64, B, C_, 128, D, E, F, F, F, None]),
+        ("lsk_vocab_bwd", [A, 4, 64, B, C_, 0, 64, D, E, F, F, A + 0x1000 + 8, 0, None]),
+        ("lsk_vocab_bwd", [A, 4, 64, B, C_, 0, 64, D, E, F, A + 0x1000, A + 0x2000 + 4, 0, None]),
+    ]
+    for name, args in cases:
+        assert getattr(lib, name)(*args) == L.LS_ERR_ARG, (name, args)
+        assert name in L.last_error()
+    # build_ext: row counts whose element count overflows int32
+    assert lib.lsk_build_ext_fwd(A, 0, 16, None, 0, 0, 16, 2 ** 31 // 64 + 1, B, None) == L.LS_ERR_ARG
+    assert lib.lsk_build_ext_bwd(A, None, 16, 2 ** 31 // 64 + 1, B, None) == L.LS_ERR_ARG
