@@ -78,6 +78,28 @@ def test_gemm_fwd_and_residual(M, N, K, bn, nacc):
     assert rel_err(to_np(out), want) <= TOL
 
 
+@pytest.mark.parametrize("bn,nacc", [(128, 1), (256, 2)])
+def test_gemm_fwd_into_a_column_window_of_a_wider_output(bn, nacc):
+    """bf16 outputs leave through 32-row x 64-column tensor-store boxes clipped at the
+    product's own rows and columns: written into columns 8 .. 8 + N of a 512-wide buffer
+    (row pitch 512, ragged M and N), the product equals the compact one bit for bit and
+    every other column keeps its old value."""
+    M, N, K = 300, 384, 256
+    x = synth.gaussian((M, K), 31, M, K)
+    w = _w(N, K, seed=32)
+    p, a, _, _ = nf4_dev(w)
+    xd = bf16_dev(x)
+    buf = torch.full((M, 512), 7.0, dtype=torch.bfloat16, device=DEV)
+    compact = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    k("lsk_nf4_gemm", 0, xd, K, M, p, a, N, K, None, None, 0, 0, buf[:, 8:8 + N], 512, None, 0, bn, nacc)
+    k("lsk_nf4_gemm", 0, xd, K, M, p, a, N, K, None, None, 0, 0, compact, N, None, 0, bn, nacc)
+    want = om.linear(om.t64(x), om.t64(_oracle_deq(w))).numpy()
+    torch.cuda.synchronize()
+    assert torch.equal(buf[:, 8:8 + N], compact)
+    assert bool((buf[:, :8] == 7.0).all()) and bool((buf[:, 8 + N:] == 7.0).all())
+    assert rel_err(to_np(compact), want) <= TOL
+
+
 @pytest.mark.parametrize("M,N,K,bn,nacc", GEMM_CASES)
 def test_gemm_dx(M, N, K, bn, nacc):
     dy = synth.gaussian((M, N), 5, M, N)
