@@ -22,8 +22,10 @@
 //               -- W's own orientation -- for DX); then run the epilogue.
 //   warp 1      one thread issues tcgen05.mma (M=128, N=BN, K=16) into TMEM
 //               accumulators, NACC of them sharing each dequantised B tile.
-// Epilogues: bf16 store (+ residual), fp32 store / accumulate, vocabulary
-// log-sum-exp partials with target-logit capture, and dlogits for the backward.
+// Epilogues (TMEM read 32 columns at a time): bf16 store (+ residual; without one, the
+// rows are staged in the idle B ring as 128-byte-swizzled boxes and leave by TMA
+// tensor stores), fp32 store / accumulate, vocabulary log-sum-exp partials with
+// target-logit capture, and dlogits for the backward.
 #pragma once
 #include "common.cuh"
 
@@ -206,7 +208,7 @@ struct ItemCursor {
 //    producer keeps it LOOK k-steps ahead of the A ring, so a dequant never waits for an
 //    MMA to finish before its codes can be fetched;
 //  - B ring (SB stages): dequantised bf16 tiles, written by the dequant warps, released
-//    by the MMAs.
+//    by the MMAs; idle during a tile's epilogue, when it holds the staged output boxes.
 // Dequant: TPU threads per 64-code row of the B tile (1: the whole row, 2: 32 codes
 // each), in NGRP groups taking alternate k-steps (group g owns B buffer g); the first 8
 // dequant warps also run the epilogue (two per TMEM lane quarter).  The 256-wide tiles
